@@ -1,0 +1,55 @@
+/*
+ * Seeded synthetic inputs for the MoE FFN layer: data only, none of the layer's arithmetic.
+ *
+ * Both the CPU oracle (through the host functions) and the CUDA library (through the device
+ * fill) receive their inputs from this one generator, so the two sides see identical bits.
+ *
+ * Random words: the splitmix64 sequence (Steele, Lea & Flood, "Fast splittable pseudorandom
+ * number generators", OOPSLA 2014): state_i = key + (i+1)*0x9E3779B97F4A7C15, output =
+ * the splitmix64 finaliser of state_i.  key = fin(fin(seed) + stream*0x9E3779B97F4A7C15).
+ * The sequence is counter-based: any element can be produced on its own.
+ *
+ * Approximately normal values: Irwin-Hall with 12 terms.  Element i of a stream takes the
+ * words 3i, 3i+1, 3i+2, splits them into twelve 16-bit fields b_0..b_11 and forms the
+ * integer n = sum(b) - 393210 (= 12*32767.5 rounded so that E[n] = 0).  z = n / 65536 has
+ * mean 0 and variance 1 - 2^-32, and is bounded by |z| < 6.  The element is
+ * bf16_rne(float(z) * sigma): z is exact in fp32, the product is one IEEE fp32 multiply,
+ * then one round-to-nearest-even to bf16, so every machine produces the same bits.
+ * (Exact normal samplers need log/cos, whose last bit differs between libraries; the
+ * integer Irwin-Hall sum keeps host and device bit-identical.)
+ */
+#ifndef SYNTH_H
+#define SYNTH_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Key of one stream.  stream identifies a tensor, a layer and a redraw round. */
+uint64_t synth_key(uint64_t seed, uint64_t stream);
+
+/* Word i of the stream with the given key. */
+uint64_t synth_word(uint64_t key, uint64_t i);
+
+/* out[j] = bf16 bits of element (offset + j) of the stream, j < n, scaled by sigma.
+ * Splits the work over nthreads host threads (<= 0: one); the result does not depend on it. */
+void synth_normal_bf16(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n,
+                       float sigma, uint16_t* out, int nthreads);
+
+/* A uniformly random permutation of 0..n-1 (Fisher-Yates, Knuth vol. 2 Algorithm 3.4.2P,
+ * with each index drawn by rejection so that it is exactly uniform). */
+void synth_permutation(uint64_t seed, uint64_t stream, int32_t n, int32_t* out);
+
+/* Device fill: the same elements as synth_normal_bf16, written to device memory `dst`
+ * (n elements) on the CUDA stream `cuda_stream` (a cudaStream_t, 0 = legacy default).
+ * Returns 0 on success or the cudaError_t of the launch. */
+int synth_normal_bf16_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n,
+                             float sigma, void* dst, void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
