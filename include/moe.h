@@ -1,0 +1,138 @@
+/*
+ * libmoe -- one mixture-of-experts FFN layer on one GB300 GPU (sm_103a), behind a C ABI.
+ *
+ * What the layer computes (source: "Optimizing on-device inference for Apple Silicon"):
+ *   - § "three distinct workload shapes": a router scores E = 256 experts per token and keeps
+ *     eight; a shared expert processes every token; experts receive uneven token counts.
+ *   - § "Keep expert routing on the GPU": after selection, a histogram counts the
+ *     assignments of each expert, a prefix scan turns counts into start offsets, a scatter
+ *     places rows in their expert groups, and a block map lists the fixed-size blocks the
+ *     grouped GEMM processes -- all on the GPU, with no CPU-GPU synchronisation in the layer.
+ *   - § "Match tile size to expert load": the grouped GEMM's tile fits the rows an expert has.
+ *   - § "Dequantize weights during matrix multiplication": fp32 accumulation, bf16 output.
+ *   - § "Optimize the one-row weight path" and § "Reduce intermediate and state traffic":
+ *     batch-1 decode is a matrix-vector product; the two expert input projections are fused
+ *     with their gated activation, and the output projection with its routing score and the
+ *     shared expert's result.
+ * Readings where the page is silent (fixed by this library):
+ *   logits[t][e] = x[t] . w_router[e] (+ router_bias[e]); the k = 8 largest are kept (ties to
+ *   the lower expert id) and listed in ascending expert id; their weights are the softmax
+ *   over the kept logits; every expert (and the shared expert) is a SwiGLU FFN
+ *   o = W_down (silu(W_gate x) * (W_up x)) with silu(g) = g / (1 + e^-g); the shared expert
+ *   is ungated with weight 1;  y[t] = sum_j w[t][j] o_{e_j}(x[t]) + o_shared(x[t]),
+ *   accumulated in fp32 in ascending expert id and then the shared expert, rounded once
+ *   to bf16.
+ *
+ * Data types and layouts (row-major; "bf16" = IEEE bfloat16 bits, 2 bytes):
+ *   x [T][d] bf16, y [T][d] bf16.
+ *   w_router [E][d] bf16 (the d x E router matrix stored transposed, input dim contiguous).
+ *   w_gate, w_up [E][f][d] bf16; w_down [E][d][f] bf16: every weight is output-major with the
+ *   input dimension contiguous, like a linear layer's weight matrix.
+ *   ws_gate, ws_up [fs][d] bf16; ws_down [d][fs] bf16 (shared expert).
+ *   router_bias [E] fp32 or NULL.
+ *
+ * Ownership and threading:
+ *   - Weights are BORROWED device pointers: the caller keeps them alive and unchanged for the
+ *     lifetime of the handle; nothing is copied.
+ *   - The handle owns its device workspace, sized for cfg.max_tokens at moe_create.
+ *   - x, y and the routing outputs are owned by the caller.
+ *   - moe_route / moe_forward / moe_forward_host only enqueue work on the given stream (a
+ *     cudaStream_t passed as void*, NULL = the legacy default stream) and return; they never
+ *     synchronise with the host.  A handle must be used on one stream at a time.
+ *   - All device pointers must be 16-byte aligned; y must not overlap x.
+ *
+ * Errors: every call returns a moe_status.  Invalid arguments are rejected before anything is
+ * enqueued.  Kernels never trap: a device-side failure (a bounded wait that timed out) is
+ * recorded in a device error word that moe_get_device_error reads and clears.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* NULL handle/pointer, T < 0, bad config value */
+  MOE_ERR_UNSUPPORTED = 2, /* E != 256, k != 8, d/f/fs not a multiple of 128 or out of range,
+                              T > max_tokens */
+  MOE_ERR_ALIGNMENT = 3,   /* a device pointer is not 16-byte aligned */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (see moe_last_cuda_error) */
+  MOE_ERR_TIMEOUT = 5,     /* a kernel's bounded wait expired (device error word) */
+  MOE_ERR_DEVICE = 6,      /* a kernel detected an inconsistent internal state */
+  MOE_ERR_NO_MEMORY = 7    /* workspace allocation failed */
+} moe_status;
+
+/* Kernel schedule: AUTO uses the batch-1 matrix-vector path when T == 1 and the tensor-core
+ * grouped-GEMM path otherwise; the other two force one path (GEMV requires T == 1). */
+typedef enum { MOE_SCHEDULE_AUTO = 0, MOE_SCHEDULE_GEMM = 1, MOE_SCHEDULE_GEMV = 2 } moe_schedule;
+
+typedef struct moe_handle_s* moe_handle;
+
+typedef struct {
+  int d;              /* hidden size: multiple of 128, 128 <= d <= 8192 */
+  int n_experts;      /* E: must be 256 */
+  int top_k;          /* k: must be 8 */
+  int ffn_dim;        /* f, routed expert inner dim: multiple of 128, 128 <= f <= 2048 */
+  int shared_ffn_dim; /* fs, shared expert inner dim: multiple of 128, 128 <= fs <= 2048 */
+  int max_tokens;     /* largest T accepted later: 1 <= max_tokens <= 1048576 */
+  int schedule;       /* a moe_schedule value */
+} moe_config;
+
+typedef struct {           /* device pointers, borrowed (see above) */
+  const void* w_router;    /* bf16 [E][d] */
+  const float* router_bias;/* fp32 [E], or NULL for no bias */
+  const void* w_gate;      /* bf16 [E][f][d] */
+  const void* w_up;        /* bf16 [E][f][d] */
+  const void* w_down;      /* bf16 [E][d][f] */
+  const void* ws_gate;     /* bf16 [fs][d] */
+  const void* ws_up;       /* bf16 [fs][d] */
+  const void* ws_down;     /* bf16 [d][fs] */
+} moe_weights;
+
+/* Validates cfg and w, allocates the workspace on the current CUDA device, prepares the
+ * kernels, and returns a handle in *out.  May synchronise the device.  On failure *out is
+ * NULL and nothing stays allocated. */
+int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out);
+
+/* Routing only (§ "Keep expert routing on the GPU"): the same kernels moe_forward runs for
+ * this T, so moe_forward's routing equals what this returns.  Device outputs, each may be
+ * NULL if not wanted:
+ *   topk_idx [T][k] int32  kept experts of each token, ascending expert id;
+ *   topk_w   [T][k] fp32   their softmax weights, aligned with topk_idx;
+ *   offsets  [E+1] int32   offsets[e] = number of assignments to experts < e, offsets[E]=T*k;
+ *   perm     [T*k] int32   slot -> t*k + j: assignments grouped by expert (ascending), tokens
+ *                          ascending within a group.
+ * T == 0 enqueues nothing and returns MOE_OK. */
+int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w,
+              int32_t* offsets, int32_t* perm, void* stream);
+
+/* The layer: y [T][d] bf16 from x [T][d] bf16 (device pointers).  T == 0: no-op. */
+int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream);
+
+/* moe_forward on HOST buffers: enqueues the copy of x_host [T][d] (pinned memory for an
+ * asynchronous copy) into a handle-owned device buffer, the layer, and the copy of the result
+ * into y_host [T][d].  The caller synchronises the stream before reading y_host. */
+int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void* stream);
+
+/* Synchronises `stream`, then returns and clears the handle's device error word
+ * (MOE_OK if no kernel reported a failure since the last call). */
+int moe_get_device_error(moe_handle h, void* stream);
+
+/* Frees the workspace and the handle (synchronises the device).  NULL is accepted. */
+int moe_destroy(moe_handle h);
+
+/* Static description of a status code. */
+const char* moe_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call made by this library in this thread. */
+int moe_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,362 @@
+// The C ABI of libmoe (declared and documented in include/moe.h): argument checks, the
+// device workspace, TMA tensor maps, and the order of the kernel launches of one layer.
+// Nothing here synchronises with the host inside moe_route / moe_forward.
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "layer.cuh"
+#include "moe.h"
+
+using moe::Dims;
+using moe::kE;
+using moe::kTopK;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  g_last_cuda_error = (int)e;
+  return MOE_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows][inner] (row pitch inner*2 bytes), box [box_rows][box_inner],
+// 128-byte swizzle (the layout the tcgen05 descriptors expect).
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+               uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+struct moe_handle_s {
+  moe_config cfg;
+  moe_weights w;
+  Dims D;
+  int device = 0, sms = 0;
+  int P_max = 0, max_units_gu = 0, max_units_dn = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  moe::RouteWs rws{};
+  moe::DecodeWs dws{};
+  __nv_bfloat16* h = nullptr;
+  __nv_bfloat16* ys = nullptr;
+  __nv_bfloat16* x_stage = nullptr;
+  __nv_bfloat16* y_stage = nullptr;
+  CUtensorMap tm_wr, tm_wg, tm_wu, tm_wsg, tm_wsu, tm_wd, tm_wsd, tm_h;
+};
+
+namespace {
+
+int check_config(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->d <= 0 || c->ffn_dim <= 0 || c->shared_ffn_dim <= 0 || c->max_tokens <= 0 ||
+      c->n_experts <= 0 || c->top_k <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->schedule < MOE_SCHEDULE_AUTO || c->schedule > MOE_SCHEDULE_GEMV)
+    return MOE_ERR_INVALID_ARG;
+  if (c->n_experts != kE || c->top_k != kTopK) return MOE_ERR_UNSUPPORTED;
+  if (c->d % 128 || c->d > 8192) return MOE_ERR_UNSUPPORTED;
+  if (c->ffn_dim % 128 || c->ffn_dim > 2048) return MOE_ERR_UNSUPPORTED;
+  if (c->shared_ffn_dim % 128 || c->shared_ffn_dim > 2048) return MOE_ERR_UNSUPPORTED;
+  if (c->max_tokens > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int check_weights(const moe_weights* w) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  const void* req[] = {w->w_router, w->w_gate, w->w_up, w->w_down, w->ws_gate, w->ws_up,
+                       w->ws_down};
+  for (const void* p : req) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MOE_ERR_ALIGNMENT;
+  }
+  if (w->router_bias && !aligned4(w->router_bias)) return MOE_ERR_ALIGNMENT;
+  return MOE_OK;
+}
+
+// Bump allocator over the single workspace allocation (256-byte aligned pieces).
+struct Carve {
+  char* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t n) {
+    off = (off + 255) & ~size_t(255);
+    T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+    off += n * sizeof(T);
+    return p;
+  }
+};
+
+void layout(moe_handle_s* h, char* base, size_t* total) {
+  const int Tm = h->cfg.max_tokens;
+  const int nblk = (Tm + moe::kBlockTokens - 1) / moe::kBlockTokens;
+  const size_t S = (size_t)Tm * kTopK;
+  Carve c{base};
+  h->rws.topk_idx = c.take<int32_t>(S);
+  h->rws.topk_w = c.take<float>(S);
+  h->rws.hist = c.take<int32_t>((size_t)nblk * kE);
+  h->rws.blkpre = c.take<int32_t>((size_t)nblk * kE);
+  h->rws.offsets = c.take<int32_t>(kE + 1);
+  h->rws.poff = c.take<int32_t>(kE + 2);
+  h->rws.perm = c.take<int32_t>(S);
+  h->rws.prow = c.take<int32_t>((size_t)Tm * 9);
+  h->rws.grow = c.take<int32_t>((size_t)h->P_max);
+  h->rws.units_gu = c.take<moe::Unit>((size_t)h->max_units_gu);
+  h->rws.units_dn = c.take<moe::Unit>((size_t)h->max_units_dn);
+  h->rws.n_units = c.take<int32_t>(2);
+  h->rws.err = c.take<int>(1);
+  h->dws.logits = c.take<float>(kE);
+  h->dws.counter = c.take<int>(1);
+  h->dws.hdec = c.take<float>((size_t)9 * h->D.hdim);
+  h->h = c.take<__nv_bfloat16>((size_t)h->P_max * h->D.hdim);
+  h->ys = c.take<__nv_bfloat16>((size_t)h->P_max * h->D.d);
+  h->x_stage = c.take<__nv_bfloat16>((size_t)Tm * h->D.d);
+  h->y_stage = c.take<__nv_bfloat16>((size_t)Tm * h->D.d);
+  *total = c.off + 256;
+}
+
+moe::DecodeWeights decode_weights(const moe_handle_s* h) {
+  moe::DecodeWeights W;
+  W.w_r = static_cast<const __nv_bfloat16*>(h->w.w_router);
+  W.w_gate = static_cast<const __nv_bfloat16*>(h->w.w_gate);
+  W.w_up = static_cast<const __nv_bfloat16*>(h->w.w_up);
+  W.w_down = static_cast<const __nv_bfloat16*>(h->w.w_down);
+  W.ws_gate = static_cast<const __nv_bfloat16*>(h->w.ws_gate);
+  W.ws_up = static_cast<const __nv_bfloat16*>(h->w.ws_up);
+  W.ws_down = static_cast<const __nv_bfloat16*>(h->w.ws_down);
+  W.bias = h->w.router_bias;
+  return W;
+}
+
+int check_call(moe_handle h, const void* x, int T) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > h->cfg.max_tokens) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && !x) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x)) return MOE_ERR_ALIGNMENT;
+  if (h->cfg.schedule == MOE_SCHEDULE_GEMV && T > 1) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool use_gemv(const moe_handle_s* h, int T) {
+  return T == 1 && h->cfg.schedule != MOE_SCHEDULE_GEMM;
+}
+
+// The routing chain of the tensor-core schedule.
+int run_route_gemm(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w,
+                   int32_t* offsets, int32_t* perm, cudaStream_t s, CUtensorMap* tm_xg) {
+  CUtensorMap tm_x;
+  if (!encode_2d(&tm_x, x, h->D.d, T, moe::kBK, moe::kBlockTokens)) return MOE_ERR_CUDA;
+  if (tm_xg && !encode_2d(tm_xg, x, h->D.d, T, moe::kBK, 1)) return MOE_ERR_CUDA;
+  moe::RouteWs w = h->rws;
+  if (offsets) w.offsets = offsets;
+  int st = cuda_status(moe::launch_router_topk(tm_x, h->tm_wr, h->w.router_bias, T, h->D,
+                                               topk_idx, topk_w, w, s));
+  if (st) return st;
+  if ((st = cuda_status(moe::launch_route_plan(T, h->D, w, s)))) return st;
+  return cuda_status(moe::launch_route_scatter(T, topk_idx, perm, w, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  int st = check_config(cfg);
+  if (st) return st;
+  if ((st = check_weights(w))) return st;
+
+  moe_handle_s* h = new (std::nothrow) moe_handle_s();
+  if (!h) return MOE_ERR_NO_MEMORY;
+  h->cfg = *cfg;
+  h->w = *w;
+  h->D = Dims{cfg->d, cfg->ffn_dim, cfg->shared_ffn_dim,
+              cfg->ffn_dim > cfg->shared_ffn_dim ? cfg->ffn_dim : cfg->shared_ffn_dim};
+  auto fail = [&](int status) {
+    if (h->ws) cudaFree(h->ws);
+    delete h;
+    return status;
+  };
+  cudaDeviceProp prop;
+  if ((st = cuda_status(cudaGetDevice(&h->device)))) return fail(st);
+  if ((st = cuda_status(cudaGetDeviceProperties(&prop, h->device)))) return fail(st);
+  if (prop.major != 10 || prop.minor != 3) return fail(MOE_ERR_UNSUPPORTED);  // sm_103 only
+  h->sms = prop.multiProcessorCount;
+
+  const int Tm = cfg->max_tokens;
+  const int S = Tm * kTopK;
+  // every group padded to 16 rows: routed groups add at most 15 rows each
+  h->P_max = moe::round_up(S + kE * (moe::kRowAlign - 1) + moe::round_up(Tm, moe::kRowAlign), 256);
+  const int chunks_routed = (S + moe::kChunkRows - 1) / moe::kChunkRows + kE;
+  const int chunks_shared = (Tm + moe::kChunkRows - 1) / moe::kChunkRows;
+  h->max_units_gu = chunks_routed * (cfg->ffn_dim / moe::kMTile) +
+                    chunks_shared * (cfg->shared_ffn_dim / moe::kMTile);
+  h->max_units_dn = (chunks_routed + chunks_shared) * (cfg->d / moe::kMTile);
+
+  size_t total = 0;
+  layout(h, nullptr, &total);
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MOE_ERR_NO_MEMORY);
+  }
+  h->ws_bytes = total;
+  layout(h, static_cast<char*>(h->ws), &total);
+  // zero everything once: error word, decode counter, padding rows of h and grow
+  if ((st = cuda_status(cudaMemset(h->ws, 0, total)))) return fail(st);
+
+  const Dims& D = h->D;
+  bool ok = encode_2d(&h->tm_wr, w->w_router, D.d, kE, moe::kBK, kE) &&
+            encode_2d(&h->tm_wg, w->w_gate, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
+            encode_2d(&h->tm_wu, w->w_up, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
+            encode_2d(&h->tm_wsg, w->ws_gate, D.d, D.fs, moe::kBK, moe::kMTile) &&
+            encode_2d(&h->tm_wsu, w->ws_up, D.d, D.fs, moe::kBK, moe::kMTile) &&
+            encode_2d(&h->tm_wd, w->w_down, D.f, (uint64_t)kE * D.d, moe::kBK, moe::kMTile) &&
+            encode_2d(&h->tm_wsd, w->ws_down, D.fs, D.d, moe::kBK, moe::kMTile) &&
+            encode_2d(&h->tm_h, h->h, D.hdim, h->P_max, moe::kBK, 16);
+  if (!ok) return fail(MOE_ERR_CUDA);
+  if ((st = cuda_status(moe::prepare_route_kernels()))) return fail(st);
+  if ((st = cuda_status(moe::prepare_expert_kernels()))) return fail(st);
+  if ((st = cuda_status(moe::prepare_decode_kernels(D.hdim)))) return fail(st);
+  if ((st = cuda_status(cudaDeviceSynchronize()))) return fail(st);
+  *out = h;
+  return MOE_OK;
+}
+
+int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w,
+              int32_t* offsets, int32_t* perm, void* stream) {
+  int st = check_call(h, x, T);
+  if (st) return st;
+  if (!aligned16(topk_idx) || !aligned16(topk_w) || !aligned4(offsets) || !aligned4(perm))
+    return MOE_ERR_ALIGNMENT;
+  if (T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* idx = topk_idx ? topk_idx : h->rws.topk_idx;
+  float* wt = topk_w ? topk_w : h->rws.topk_w;
+  int32_t* pm = perm ? perm : h->rws.perm;
+  if (use_gemv(h, T))
+    return cuda_status(moe::launch_decode_router_shared(
+        static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, idx, wt,
+        offsets ? offsets : h->rws.offsets, pm, h->dws, h->rws.err, s, false));
+  return run_route_gemm(h, x, T, idx, wt, offsets, pm, s, nullptr);
+}
+
+int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
+  int st = check_call(h, x, T);
+  if (st) return st;
+  if (T > 0 && !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y)) return MOE_ERR_ALIGNMENT;
+  if (T == 0) return MOE_OK;
+  const size_t bytes = (size_t)T * h->D.d * 2;
+  const char *xb = static_cast<const char*>(x), *yb = static_cast<const char*>(y);
+  if (xb < yb + bytes && yb < xb + bytes) return MOE_ERR_INVALID_ARG;  // y overlaps x
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* xd = static_cast<const __nv_bfloat16*>(x);
+  __nv_bfloat16* yd = static_cast<__nv_bfloat16*>(y);
+
+  if (use_gemv(h, T)) {
+    const moe::DecodeWeights W = decode_weights(h);
+    if ((st = cuda_status(moe::launch_decode_router_shared(xd, W, h->D, h->rws.topk_idx,
+                                                           h->rws.topk_w, nullptr, nullptr,
+                                                           h->dws, h->rws.err, s, true))))
+      return st;
+    if ((st = cuda_status(moe::launch_decode_gateup(xd, W, h->D, h->rws.topk_idx, h->dws, s))))
+      return st;
+    return cuda_status(moe::launch_decode_down_combine(W, h->D, h->rws.topk_idx, h->rws.topk_w,
+                                                       h->dws, yd, s));
+  }
+
+  CUtensorMap tm_xg;
+  if ((st = run_route_gemm(h, x, T, h->rws.topk_idx, h->rws.topk_w, nullptr, h->rws.perm, s,
+                           &tm_xg)))
+    return st;
+  if ((st = cuda_status(moe::launch_gateup(tm_xg, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu, h->D,
+                                           h->rws, h->h, h->sms, s))))
+    return st;
+  if ((st = cuda_status(
+           moe::launch_down(h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->ys, h->sms, s))))
+    return st;
+  return cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, s));
+}
+
+int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T > h->cfg.max_tokens) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)T * h->D.d * 2;
+  int st = cuda_status(cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s));
+  if (st) return st;
+  if ((st = moe_forward(h, h->x_stage, T, h->y_stage, stream))) return st;
+  return cuda_status(cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s));
+}
+
+int moe_get_device_error(moe_handle h, void* stream) {
+  if (!h) return MOE_ERR_INVALID_ARG;
+  int st = cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  if (st) return st;
+  int v = 0;
+  if ((st = cuda_status(cudaMemcpy(&v, h->rws.err, sizeof(int), cudaMemcpyDeviceToHost))))
+    return st;
+  if (v != 0 && (st = cuda_status(cudaMemset(h->rws.err, 0, sizeof(int))))) return st;
+  return v;
+}
+
+int moe_destroy(moe_handle h) {
+  if (!h) return MOE_OK;
+  int st = MOE_OK;
+  if (h->ws) st = cuda_status(cudaFree(h->ws));
+  delete h;
+  return st;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration or size";
+    case MOE_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "a kernel's bounded wait expired";
+    case MOE_ERR_DEVICE: return "kernel detected an inconsistent state";
+    case MOE_ERR_NO_MEMORY: return "out of memory";
+    default: return "unknown status";
+  }
+}
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,130 @@
+// Internal interface between the C ABI (api.cu) and the kernel files: sizes, the
+// routing-workspace layout, kernel argument blocks and launcher declarations.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kE = 256;            // experts
+constexpr int kTopK = 8;           // kept per token
+constexpr int kBlockTokens = 128;  // tokens per router / scatter block (the MMA M)
+constexpr int kChunkRows = 256;    // most token rows in one grouped-GEMM work unit (MMA N)
+constexpr int kRowAlign = 16;      // expert groups start on 16-row boundaries (MMA N step)
+constexpr int kMTile = 128;        // weight rows per work unit (MMA M)
+constexpr int kBK = 64;            // K elements per pipeline stage (one 128-byte swizzle row)
+
+__host__ __device__ constexpr int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// One grouped-GEMM work unit: expert group g (g == kE: the shared expert), first padded row
+// p0, valid rows nrows (<= kChunkRows), weight row tile mt.
+struct Unit {
+  int g, p0, nrows, mt;
+};
+
+// Device workspace of the routing chain (all sized for max_tokens at create time).
+struct RouteWs {
+  int32_t* topk_idx;  // [T][8] when the caller does not supply one
+  float* topk_w;      // [T][8]
+  int32_t* hist;      // [nblk][E] assignments per (token block, expert)
+  int32_t* blkpre;    // [nblk][E] assignments of earlier blocks, per expert
+  int32_t* offsets;   // [E+1]
+  int32_t* poff;      // [E+2] padded start row of each group (E = shared), poff[E+1] = total
+  int32_t* perm;      // [T*8] slot -> t*8+j
+  int32_t* prow;      // [T][9] padded row of (t, j); column 8 = the shared expert's row
+  int32_t* grow;      // [P] token of each padded row (0 for padding rows)
+  Unit* units_gu;     // gate/up work units
+  Unit* units_dn;     // down work units
+  int32_t* n_units;   // [2]: gate/up, down
+  int* err;           // device error word
+};
+
+struct Dims {
+  int d, f, fs, hdim;  // hdim = max(f, fs): row pitch of the h buffer
+};
+
+// Launch with programmatic dependent launch allowed: the kernel may start while its
+// predecessor on the stream finishes; every kernel here calls griddepcontrol.wait before it
+// touches memory that earlier work on the stream writes.
+template <typename K, typename... Args>
+inline cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Sets the dynamic shared-memory limits of the kernels that need more than 48 KB.
+cudaError_t prepare_route_kernels();
+cudaError_t prepare_expert_kernels();
+cudaError_t prepare_decode_kernels(int hdim);
+
+// ---------------------------------------------------------------- launchers (stream-ordered)
+
+// Router GEMM + top-8 + softmax + per-block histogram (tensor cores), one block per 128 tokens.
+cudaError_t launch_router_topk(const CUtensorMap& tm_x, const CUtensorMap& tm_wr,
+                               const float* bias, int T, const Dims& D, int32_t* topk_idx,
+                               float* topk_w, const RouteWs& ws, cudaStream_t s);
+
+// Per-expert totals, offsets, padded group starts and the work-unit lists (one block).
+cudaError_t launch_route_plan(int T, const Dims& D, const RouteWs& ws, cudaStream_t s);
+
+// Counting-sort scatter: perm, prow, grow (one block per 128 tokens).
+cudaError_t launch_route_scatter(int T, const int32_t* topk_idx, int32_t* perm,
+                                 const RouteWs& ws, cudaStream_t s);
+
+// Grouped gate/up GEMM with SwiGLU epilogue: h [P][hdim] bf16.
+cudaError_t launch_gateup(const CUtensorMap& tm_xg, const CUtensorMap& tm_wg,
+                          const CUtensorMap& tm_wu, const CUtensorMap& tm_wsg,
+                          const CUtensorMap& tm_wsu, const Dims& D, const RouteWs& ws,
+                          __nv_bfloat16* h, int grid, cudaStream_t s);
+
+// Grouped down GEMM: ys [P][d] bf16.
+cudaError_t launch_down(const CUtensorMap& tm_h, const CUtensorMap& tm_wd,
+                        const CUtensorMap& tm_wsd, const Dims& D, const RouteWs& ws,
+                        __nv_bfloat16* ys, int grid, cudaStream_t s);
+
+// y[t] = sum_j w[t][j] ys[prow[t][j]] + ys[prow[t][8]] in fp32, rounded once to bf16.
+cudaError_t launch_combine(int T, const Dims& D, const float* topk_w, const RouteWs& ws,
+                           const __nv_bfloat16* ys, __nv_bfloat16* y, cudaStream_t s);
+
+// ---------------------------------------------------------------- batch-1 decode path
+
+struct DecodeWs {
+  float* logits;   // [E]
+  int* counter;    // last-block detection of the router
+  float* hdec;     // [9][hdim] fp32: routed experts j = 0..7, shared = 8
+};
+
+struct DecodeWeights {
+  const __nv_bfloat16 *w_r, *w_gate, *w_up, *w_down, *ws_gate, *ws_up, *ws_down;
+  const float* bias;
+};
+
+// Router GEMV + top-8 (last block) and the shared expert's gate/up GEMV, one launch.
+cudaError_t launch_decode_router_shared(const __nv_bfloat16* x, const DecodeWeights& W,
+                                        const Dims& D, int32_t* topk_idx, float* topk_w,
+                                        int32_t* offsets, int32_t* perm, const DecodeWs& dw,
+                                        int* err, cudaStream_t s, bool with_shared);
+
+// Gate/up GEMV of the 8 selected experts with the SwiGLU fused.
+cudaError_t launch_decode_gateup(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
+                                 const int32_t* topk_idx, const DecodeWs& dw, cudaStream_t s);
+
+// Down GEMV of the 8 experts and the shared expert, weighted and combined in fixed order.
+cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D,
+                                       const int32_t* topk_idx, const float* topk_w,
+                                       const DecodeWs& dw, __nv_bfloat16* y, cudaStream_t s);
+
+}  // namespace moe

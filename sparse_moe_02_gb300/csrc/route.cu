@@ -1,0 +1,350 @@
+// Routing chain of the MoE layer on the GPU ("Optimizing on-device inference for Apple
+// Silicon", § "Keep expert routing on the GPU"): router scores and top-8 selection, a
+// histogram of assignments per expert, a prefix scan into start offsets, a scatter of the
+// rows into their expert groups, and the block map (work units) of the grouped GEMMs.
+// Nothing here waits for the host, and every result is deterministic: the histogram is
+// kept per 128-token block and combined in block order, and ranks inside a block come
+// from bit masks in token order, so no atomic ordering reaches an output.
+#include "layer.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------- router GEMM + top-8
+
+constexpr int kRtStages = 4;
+constexpr int kRtA = kBlockTokens * kBK * 2;  // x tile: 128 tokens x 64 (16 KB)
+constexpr int kRtB = kE * kBK * 2;            // router tile: 256 experts x 64 (32 KB)
+constexpr int kRtStage = kRtA + kRtB;
+constexpr int kRtSmem = kRtStages * kRtStage + 1024 + 2048;
+
+struct RouterArgs {
+  const float* bias;
+  int T, d;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* hist;
+  int* err;
+};
+
+// Keeps the 8 largest (value, id) pairs in v/id, sorted by value descending; among equal
+// values the earlier (lower) id stays ahead, because ids arrive in ascending order and a
+// new pair only moves past strictly smaller values.
+__device__ __forceinline__ void top8_insert(float (&v)[8], int (&id)[8], float x, int e) {
+  if (x > v[7]) {
+    v[7] = x;
+    id[7] = e;
+#pragma unroll
+    for (int i = 7; i > 0; --i) {
+      if (v[i] > v[i - 1]) {
+        float tv = v[i]; v[i] = v[i - 1]; v[i - 1] = tv;
+        int ti = id[i]; id[i] = id[i - 1]; id[i - 1] = ti;
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(192, 1)
+    router_topk_kernel(const __grid_constant__ CUtensorMap tm_x,
+                       const __grid_constant__ CUtensorMap tm_wr, RouterArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtStages * kRtStage);
+  uint64_t* empty = full + kRtStages;
+  uint64_t* tfull = empty + kRtStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  int* hist_s = reinterpret_cast<int*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x;
+  const int KB = a.d / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRtStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i < kE; i += blockDim.x) hist_s[i] = 0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // x (and the bias) may come from the previous kernel on the stream
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tensormap(&tm_x);
+      prefetch_tensormap(&tm_wr);
+      const uint64_t keep = policy_evict_last();  // x and the router weights are re-read
+      int stage = 0;
+      uint32_t ph = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) break;
+        uint8_t* st = smem + stage * kRtStage;
+        mbar_arrive_expect_tx(&full[stage], kRtStage);
+        tma_load_2d(st, &tm_x, &full[stage], kb * kBK, blk * kBlockTokens, keep);
+        tma_load_2d(st + kRtA, &tm_wr, &full[stage], kb * kBK, 0, keep);
+        if (++stage == kRtStages) { stage = 0; ph ^= 1; }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, kE);
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&full[stage], ph, a.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + stage * kRtStage), sb = sa + kRtA;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_bf16(tmem, sdesc_k128(sa + kk * 32), sdesc_k128(sb + kk * 32), idesc,
+                   (kb | kk) != 0);
+        mma_commit(&empty[stage]);
+        if (++stage == kRtStages) { stage = 0; ph ^= 1; }
+      }
+      if (ok) mma_commit(tfull);
+    }
+  } else {
+    // epilogue: one thread per token row of the tile
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const int t = blk * kBlockTokens + m;
+    const bool have = mbar_wait(tfull, 0, a.err);
+    tc_fence_after();
+    float v[8];
+    int id[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { v[i] = -INFINITY; id[i] = 0; }
+    if (have) {
+      for (int c0 = 0; c0 < kE; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float x = __uint_as_float(r[i]);
+          if (a.bias) x += __ldg(a.bias + c0 + i);
+          top8_insert(v, id, x, c0 + i);
+        }
+      }
+    }
+    // list the kept experts in ascending id
+#pragma unroll
+    for (int i = 0; i < 7; ++i)
+#pragma unroll
+      for (int j = 0; j < 7 - i; ++j)
+        if (id[j] > id[j + 1]) {
+          int ti = id[j]; id[j] = id[j + 1]; id[j + 1] = ti;
+          float tv = v[j]; v[j] = v[j + 1]; v[j + 1] = tv;
+        }
+    float mx = v[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) mx = fmaxf(mx, v[j]);
+    float ex[8], s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { ex[j] = __expf(v[j] - mx); s += ex[j]; }
+    if (have && t < a.T) {
+      int4* pi = reinterpret_cast<int4*>(a.topk_idx + (size_t)t * kTopK);
+      float4* pw = reinterpret_cast<float4*>(a.topk_w + (size_t)t * kTopK);
+      pi[0] = make_int4(id[0], id[1], id[2], id[3]);
+      pi[1] = make_int4(id[4], id[5], id[6], id[7]);
+      pw[0] = make_float4(ex[0] / s, ex[1] / s, ex[2] / s, ex[3] / s);
+      pw[1] = make_float4(ex[4] / s, ex[5] / s, ex[6] / s, ex[7] / s);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) atomicAdd(&hist_s[id[j]], 1);
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+    const int et = threadIdx.x - 64;
+    a.hist[(size_t)blk * kE + et] = hist_s[et];
+    a.hist[(size_t)blk * kE + et + 128] = hist_s[et + 128];
+  }
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------- plan
+
+// Exclusive scan of v over the 256 threads of the block; *total receives the sum.
+__device__ int block_scan_256(int v, int* tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < 8 ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < 8) tmp[8 + lane] = w;
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? tmp[8 + warp - 1] : 0) + x - v;
+  *total = tmp[15];
+  __syncthreads();
+  return before;
+}
+
+struct PlanArgs {
+  int T, nblk, mt_f, mt_fs, mt_d;
+};
+
+// Thread e: totals of expert e over the token blocks (and the per-block prefix), the
+// exclusive scan into offsets, the padded group starts (groups start on 16-row boundaries;
+// the shared expert's T rows follow the routed groups), and the work units: each group is
+// cut into ceil(n / 256) nearly equal chunks of rows, and each chunk is paired with every
+// weight row tile.  Units are listed shared group first, then experts ascending; inside a
+// group, weight tile major and chunk minor, so units that read the same weights are
+// adjacent and run at the same time on neighbouring blocks.
+__global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws) {
+  __shared__ int tmp[16];
+  pdl_wait();
+  const int e = threadIdx.x;
+  int run = 0;
+#pragma unroll 8
+  for (int b = 0; b < p.nblk; ++b) {
+    const int c = ws.hist[(size_t)b * kE + e];
+    ws.blkpre[(size_t)b * kE + e] = run;
+    run += c;
+  }
+  const int cnt = run;
+  const int pc = round_up(cnt, kRowAlign);
+  const int nch = (cnt + kChunkRows - 1) / kChunkRows;
+  int tot_cnt, tot_pc, tot_gu, tot_dn;
+  const int off = block_scan_256(cnt, tmp, &tot_cnt);
+  const int poff = block_scan_256(pc, tmp, &tot_pc);
+  const int ugu = block_scan_256(nch * p.mt_f, tmp, &tot_gu);
+  const int udn = block_scan_256(nch * p.mt_d, tmp, &tot_dn);
+
+  // shared group
+  const int nch_s = (p.T + kChunkRows - 1) / kChunkRows;
+  const int cs_s = nch_s ? round_up((p.T + nch_s - 1) / nch_s, kRowAlign) : 0;
+  const int gu_s = nch_s * p.mt_fs, dn_s = nch_s * p.mt_d;
+  const int p_shared = tot_pc;
+
+  ws.offsets[e] = off;
+  ws.poff[e] = poff;
+  if (e == kE - 1) {
+    ws.offsets[kE] = tot_cnt;
+    ws.poff[kE] = p_shared;
+    ws.poff[kE + 1] = p_shared + round_up(p.T, kRowAlign);
+    ws.n_units[0] = gu_s + tot_gu;
+    ws.n_units[1] = dn_s + tot_dn;
+  }
+  for (int r = poff + cnt; r < poff + pc; ++r) ws.grow[r] = 0;
+  if (e == 0)
+    for (int r = p_shared + p.T; r < p_shared + round_up(p.T, kRowAlign); ++r) ws.grow[r] = 0;
+
+  if (nch > 0) {
+    const int cs = round_up((cnt + nch - 1) / nch, kRowAlign);
+    for (int mt = 0; mt < p.mt_f; ++mt)
+      for (int c = 0; c < nch; ++c)
+        ws.units_gu[gu_s + ugu + mt * nch + c] =
+            Unit{e, poff + c * cs, min(cs, cnt - c * cs), mt};
+    for (int mt = 0; mt < p.mt_d; ++mt)
+      for (int c = 0; c < nch; ++c)
+        ws.units_dn[dn_s + udn + mt * nch + c] =
+            Unit{e, poff + c * cs, min(cs, cnt - c * cs), mt};
+  }
+  for (int i = threadIdx.x; i < gu_s; i += blockDim.x) {
+    const int mt = i / nch_s, c = i % nch_s;
+    ws.units_gu[i] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt};
+  }
+  for (int i = threadIdx.x; i < dn_s; i += blockDim.x) {
+    const int mt = i / nch_s, c = i % nch_s;
+    ws.units_dn[i] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt};
+  }
+  pdl_trigger();
+}
+
+// ---------------------------------------------------------------- scatter
+
+// One block per 128 tokens, one thread per token, four warps of 32 tokens.  The rank of
+// (t, e) among the assignments to expert e = assignments in earlier blocks (blkpre) +
+// those of earlier warps of this block + those of lower lanes of this warp, each counted
+// from per-warp bit masks of the tokens that chose e.
+__global__ void __launch_bounds__(128) route_scatter_kernel(int T, const int32_t* topk_idx,
+                                                            int32_t* perm, RouteWs ws) {
+  __shared__ uint32_t mask[4][kE];
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int blk = blockIdx.x;
+  const int t = blk * kBlockTokens + threadIdx.x;
+  const bool valid = t < T;
+  for (int i = threadIdx.x; i < 4 * kE; i += blockDim.x) (&mask[0][0])[i] = 0u;
+  __syncthreads();
+  int e[8];
+  if (valid) {
+    const int4* pi = reinterpret_cast<const int4*>(topk_idx + (size_t)t * kTopK);
+    const int4 a = pi[0], b = pi[1];
+    e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
+    e[4] = b.x; e[5] = b.y; e[6] = b.z; e[7] = b.w;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) atomicOr(&mask[warp][e[j]], 1u << lane);
+  }
+  __syncthreads();
+  if (valid) {
+    const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int ee = e[j];
+      int rank = ws.blkpre[(size_t)blk * kE + ee] + __popc(mask[warp][ee] & below);
+      for (int w = 0; w < warp; ++w) rank += __popc(mask[w][ee]);
+      perm[ws.offsets[ee] + rank] = t * kTopK + j;
+      const int pr = ws.poff[ee] + rank;
+      ws.prow[(size_t)t * 9 + j] = pr;
+      ws.grow[pr] = t;
+    }
+    const int ps = ws.poff[kE] + t;
+    ws.prow[(size_t)t * 9 + 8] = ps;
+    ws.grow[ps] = t;
+  }
+  pdl_trigger();
+}
+
+}  // namespace
+
+cudaError_t prepare_route_kernels() {
+  return cudaFuncSetAttribute(router_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kRtSmem);
+}
+
+cudaError_t launch_router_topk(const CUtensorMap& tm_x, const CUtensorMap& tm_wr,
+                               const float* bias, int T, const Dims& D, int32_t* topk_idx,
+                               float* topk_w, const RouteWs& ws, cudaStream_t s) {
+  RouterArgs a{bias, T, D.d, topk_idx, topk_w, ws.hist, ws.err};
+  const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
+  return launch_pdl(router_topk_kernel, dim3(nblk), dim3(192), kRtSmem, s, tm_x, tm_wr, a);
+}
+
+cudaError_t launch_route_plan(int T, const Dims& D, const RouteWs& ws, cudaStream_t s) {
+  PlanArgs p{T, (T + kBlockTokens - 1) / kBlockTokens, D.f / kMTile, D.fs / kMTile,
+             D.d / kMTile};
+  return launch_pdl(route_plan_kernel, dim3(1), dim3(256), 0, s, p, ws);
+}
+
+cudaError_t launch_route_scatter(int T, const int32_t* topk_idx, int32_t* perm,
+                                 const RouteWs& ws, cudaStream_t s) {
+  const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
+  return launch_pdl(route_scatter_kernel, dim3(nblk), dim3(128), 0, s, T, topk_idx, perm, ws);
+}
+
+}  // namespace moe

@@ -1,0 +1,185 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Bar: expert indices, offsets and the token permutation bit-exact; layer outputs within
+max|gpu - ref| <= 2e-2 * max|ref| + 1e-3 (bf16 output, fp32 accumulation); routing weights
+within 1e-5.  Inputs are seeded (synth/), x drawn under the 1e-3 logit-gap rule.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import sparse_moe_02_gb300 as moe
+from _cases import (assert_close, bf16_bits, build_case, oracle_outputs, oracle_route,
+                    sample_tokens, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    yield
+    torch.cuda.synchronize()
+
+
+def _layer(c, schedule, max_tokens=None, W=None):
+    if W is None:
+        W, _ = to_device(c)
+    return moe.MoeLayer(W, max_tokens or max(c.T, 1), schedule=schedule), W
+
+
+def _run(c, schedule, max_tokens=None):
+    import torch
+    W, x = to_device(c)
+    L, _ = _layer(c, schedule, max_tokens, W)
+    y = L.forward(x)
+    r = L.route(x)
+    torch.cuda.synchronize()
+    assert L.device_error() == moe.MOE_OK
+    out = {k: v.cpu().numpy() for k, v in r.items()}
+    out["y"] = bf16_bits(y)
+    L.close()
+    return out
+
+
+def _check_routing(c, got, tokens=None):
+    ref = oracle_route(c) if tokens is None else None
+    if ref is not None:
+        assert np.array_equal(got["topk_idx"], ref["topk_idx"]), "topk_idx differs"
+        assert np.max(np.abs(got["topk_w"] - ref["topk_w"])) <= 1e-5
+        assert np.array_equal(got["offsets"], ref["offsets"]), "offsets differ"
+        assert np.array_equal(got["perm"], ref["perm"]), "perm differs"
+        return
+    # sampled tokens: selection and weights per token; the structure by its invariants
+    idx, w = oracle.select(oracle.router_logits_f32(c.x[tokens], c.w_r, c.bias), c.dims.k)
+    assert np.array_equal(got["topk_idx"][tokens], idx)
+    assert np.max(np.abs(got["topk_w"][tokens] - w)) <= 1e-5
+    check_structure(got, c.T, c.dims.E, c.dims.k)
+
+
+def check_structure(got, T, E, k):
+    """perm/offsets are the stable counting sort of the GPU's own topk_idx."""
+    flat = got["topk_idx"].reshape(-1).astype(np.int64)
+    counts = np.bincount(flat, minlength=E)
+    assert np.array_equal(got["offsets"], np.concatenate([[0], np.cumsum(counts)]))
+    assert np.array_equal(got["perm"], np.argsort(flat, kind="stable"))
+
+
+# ---------------------------------------------------------------- tiny layer, every token
+
+@pytest.mark.parametrize("schedule", [moe.MOE_SCHEDULE_GEMM, moe.MOE_SCHEDULE_AUTO])
+def test_tiny_layer_all_tokens(schedule):
+    c = build_case("tiny", d=512, f=128, fs=128, T=64)
+    got = _run(c, schedule)
+    _check_routing(c, got)
+    assert_close(got["y"], oracle_outputs(c), "tiny T=64")
+
+
+@pytest.mark.parametrize("schedule", [moe.MOE_SCHEDULE_GEMM, moe.MOE_SCHEDULE_GEMV,
+                                      moe.MOE_SCHEDULE_AUTO])
+def test_single_token_both_paths(schedule):
+    c = build_case("tiny-t1", d=512, f=128, fs=128, T=1, seed=3)
+    got = _run(c, schedule)
+    _check_routing(c, got)
+    assert_close(got["y"], oracle_outputs(c), f"T=1 schedule {schedule}")
+
+
+@pytest.mark.parametrize("T", [2, 77, 129, 300, 1000])
+def test_ragged_token_counts(T):
+    c = build_case(f"ragged-{T}", d=512, f=128, fs=256, T=T, seed=T)
+    got = _run(c, moe.MOE_SCHEDULE_AUTO)
+    _check_routing(c, got)
+    assert_close(got["y"], oracle_outputs(c), f"T={T}")
+
+
+def test_all_tokens_pick_the_same_experts():
+    # zero router, bias on 8 experts: every token selects them; 248 groups stay empty and the
+    # 8 busy groups (T rows each) span several 256-row chunks
+    import synth
+    dims = synth.Dims(d=512, f=128, fs=128)
+    bias = np.zeros(256, dtype=np.float32)
+    hot = [3, 40, 41, 99, 128, 200, 201, 255]
+    bias[hot] = np.linspace(1.0, 2.0, 8, dtype=np.float32)
+    c = build_case("same-experts", d=512, f=128, fs=128, T=600, seed=5,
+                   w_r=np.zeros((256, 512), dtype=np.uint16), bias=bias)
+    got = _run(c, moe.MOE_SCHEDULE_AUTO)
+    _check_routing(c, got)
+    assert np.all(got["topk_idx"] == np.array(hot, dtype=np.int32))
+    assert_close(got["y"], oracle_outputs(c), "same experts")
+
+
+# ---------------------------------------------------------------- the benchmark shapes
+
+@pytest.mark.parametrize("schedule", [moe.MOE_SCHEDULE_GEMV, moe.MOE_SCHEDULE_GEMM])
+@pytest.mark.parametrize("layer", [0, 17, 39])
+def test_decode_layer(layer, schedule):
+    # batch-1 decode, d=2048, f=fs=512; weights generated on the device, oracle side only the
+    # selected experts on the host
+    c = build_case("decode", d=2048, f=512, fs=512, T=1, seed=0, layer=layer, full_host=False)
+    got = _run(c, schedule)
+    _check_routing(c, got)
+    assert_close(got["y"], oracle_outputs(c), f"decode layer {layer}")
+
+
+@pytest.mark.parametrize("skew", [False, True], ids=["balanced", "skewed"])
+def test_prefill_4096(skew):
+    c = build_case("prefill", d=2048, f=512, fs=512, T=4096, seed=0, skew=skew)
+    got = _run(c, moe.MOE_SCHEDULE_AUTO)
+    _check_routing(c, got)
+    counts = np.diff(got["offsets"])
+    if skew:
+        assert counts.max() > 1000 and (counts == 0).sum() > 0
+    else:
+        assert counts.min() > 64 and counts.max() < 256
+    toks = sample_tokens(c.T)
+    assert_close(got["y"][toks], oracle_outputs(c, toks), f"prefill skew={skew}")
+
+
+@pytest.mark.parametrize("T", [256, 1024, 8192])
+def test_prefill_sweep_sizes(T):
+    c = build_case("sweep", d=2048, f=512, fs=512, T=T, seed=11, full_host=False)
+    got = _run(c, moe.MOE_SCHEDULE_AUTO)
+    _check_routing(c, got)
+    toks = sample_tokens(T, n_edge=16, stride=97)
+    assert_close(got["y"][toks], oracle_outputs(c, toks), f"sweep T={T}")
+
+
+# ---------------------------------------------------------------- API behaviour on the GPU
+
+def test_deterministic_and_host_entry_point():
+    import torch
+    c = build_case("det", d=512, f=128, fs=128, T=333, seed=9)
+    W, x = to_device(c)
+    L = moe.MoeLayer(W, 400)
+    y1 = bf16_bits(L.forward(x))
+    y2 = bf16_bits(L.forward(x))
+    assert np.array_equal(y1, y2)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    L.forward_host(xh, yh)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(yh), y1)
+    assert L.device_error() == moe.MOE_OK
+    # T = 0 is a no-op; T beyond max_tokens is rejected before any launch
+    assert moe.moe_forward(L.handle, x.data_ptr(), 0, x.data_ptr(), None) == moe.MOE_OK
+    assert moe.moe_forward(L.handle, x.data_ptr(), 401, x.data_ptr(), None) == \
+        moe.MOE_ERR_UNSUPPORTED
+    y = torch.empty_like(x)
+    assert moe.moe_forward(L.handle, x.data_ptr() + 2, 10, y.data_ptr(), None) == \
+        moe.MOE_ERR_ALIGNMENT
+    assert moe.moe_forward(L.handle, x.data_ptr(), 10, x.data_ptr(), None) == \
+        moe.MOE_ERR_INVALID_ARG  # y aliases x
+    L.close()
+
+
+def test_gemv_schedule_rejects_more_than_one_token():
+    c = build_case("gemv-t2", d=512, f=128, fs=128, T=2, seed=4)
+    W, x = to_device(c)
+    L = moe.MoeLayer(W, 4, schedule=moe.MOE_SCHEDULE_GEMV)
+    import torch
+    y = torch.empty_like(x)
+    assert moe.moe_forward(L.handle, x.data_ptr(), 2, y.data_ptr(), None) == \
+        moe.MOE_ERR_UNSUPPORTED
+    L.close()
