@@ -1,0 +1,474 @@
+"""Benchmark of the MoE FFN layer on GB300 (one JSON line on rank 0).
+
+Workload (synthetic, seeded; shapes of the MoE layer in "Optimizing on-device inference for
+Apple Silicon": 256 experts, top 8 plus a shared expert, 4K-token prompts, batch-1 decode):
+  step = one layer forward at T=4096 tokens, d=2048, expert inner dim 512, balanced routing
+  (x ~ N(0,1), router ~ N(0,0.05), experts ~ N(0,0.02)), through moe_forward on device
+  buffers.  value = tokens/s over all ranks (each rank runs its own batch: weak scaling).
+Also measured in the same run and reported in the same line:
+  decode: batch-1 (T=1) over 40 independent layers' weights (64.7 GB, defeats L2), one CUDA
+          graph of 40 stream-ordered layer calls; us/layer and HBM GB/s;
+  roofline: the dominant kernel of the step, algorithmic bytes (or FLOPs) per launch over
+          its CUDA-event duration, against MEASURED_PEAKS.json;
+  e2e: the same tokens/s through moe_forward_host (pinned host x in, host y out, copies
+       inside the timed region);
+  cpu_baseline: the CPU oracle on a bounded sample of the same workload (rank 0 only).
+--impl reference times only the CPU oracle (the reference arm of this benchmark).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer prefill tokens/s @T=4096 & decode us/layer (T=1); % of roofline"
+T_PREFILL, D, F, FS, E, K = 4096, 2048, 512, 512, 256, 8
+DECODE_LAYERS = 40
+FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
+KERNELS_GEMM = ("router_topk", "route_plan", "route_scatter", "gateup", "down", "combine")
+KERNELS_GEMV = ("decode_router_shared", "decode_gateup", "decode_down_combine")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target duration of the CPU oracle sample")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        P = json.load(open(path))
+        return float(P["hbm_gbs"]), float(P["bf16_tflops"]), "of measured"
+    except Exception:
+        return 6800.0, 1900.0, "of fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- workload bytes and flops
+
+def algorithmic(counts, T):
+    """Algorithmic bytes and FLOPs of one prefill layer and of its kernels: weights of the
+    non-empty experts, the shared expert and the router, x in and y out; FLOPs of the GEMMs
+    actually needed (8 routed + 1 shared per token, router)."""
+    ne = int((counts > 0).sum())
+    S = T * K
+    b = dict(
+        router_topk=E * D * 2 + T * D * 2,
+        gateup=ne * 2 * F * D * 2 + 2 * FS * D * 2 + T * D * 2,
+        down=ne * D * F * 2 + D * FS * 2,
+        combine=T * D * 2,
+    )
+    fl = dict(
+        router_topk=2 * T * E * D,
+        gateup=2 * (S * 2 * F + T * 2 * FS) * D,
+        down=2 * (S * F + T * FS) * D,
+    )
+    layer_bytes = E * D * 2 + ne * 3 * F * D * 2 + 3 * FS * D * 2 + 2 * T * D * 2
+    layer_flops = sum(fl.values())
+    return b, fl, layer_bytes, layer_flops
+
+
+DECODE_BYTES_PER_LAYER = 9 * 3 * F * D * 2 + E * D * 2 + 2 * D * 2  # 9 experts + router + x + y
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [v.strip() for v in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_smi_id(torch, dev):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid).replace("GPU-", "")
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else dev
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample_rate(target_s, threads=None):
+    """tokens/s of the CPU oracle on a sample of the T=4096 prefill workload, sized to take
+    about target_s seconds; returns (rate, sample description, cores)."""
+    import oracle
+    dims = synth.Dims(d=D, f=F, fs=FS)
+    x = synth.x_rows(0, 0, T_PREFILL, D)
+    w_r = synth.host_weight(0, 0, "w_r", dims)
+    W = {n: synth.host_weight(0, 0, n, dims) for n in synth.WEIGHT_NAMES if n != "w_r"}
+    experts = (W["w_gate"], W["w_up"], W["w_down"])
+    shared = (W["ws_gate"], W["ws_up"], W["ws_down"])
+    cores = threads or host_cores()
+    n = max(1, cores)
+    toks = np.arange(n) * (T_PREFILL // n)
+    t0 = time.perf_counter()
+    oracle.forward(x, w_r, None, experts, shared, K, tokens=toks, nthreads=cores)
+    dt = time.perf_counter() - t0
+    n2 = int(min(T_PREFILL, max(n, n * target_s / max(dt, 1e-3))))
+    n2 = max(cores, n2 // cores * cores)
+    toks = np.linspace(0, T_PREFILL - 1, n2).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.forward(x, w_r, None, experts, shared, K, tokens=toks, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return n2 / dt, f"{n2} of the 4096 prefill tokens (evenly spaced), full layer per token", cores
+
+
+def reference_arm(args, rank):
+    if rank != 0:
+        return
+    import oracle
+    dims = synth.Dims(d=D, f=F, fs=FS)
+    x = synth.x_rows(0, 0, T_PREFILL, D)
+    w_r = synth.host_weight(0, 0, "w_r", dims)
+    W = {n: synth.host_weight(0, 0, n, dims) for n in synth.WEIGHT_NAMES if n != "w_r"}
+    experts = (W["w_gate"], W["w_up"], W["w_down"])
+    shared = (W["ws_gate"], W["ws_up"], W["ws_down"])
+    cores = host_cores()
+    # one step = the oracle on `n` tokens; n sized so that all steps fit in about 2 minutes
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = cores
+    t0 = time.perf_counter()
+    oracle.forward(x, w_r, None, experts, shared, K, tokens=np.arange(n), nthreads=cores)
+    per_tok = (time.perf_counter() - t0) / n
+    n = int(max(cores, min(T_PREFILL, budget / max(per_tok, 1e-6) // cores * cores)))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle.forward(x, w_r, None, experts, shared, K,
+                       tokens=rng.choice(T_PREFILL, n, replace=False), nthreads=cores)
+    times = []
+    for _ in range(args.steps):
+        toks = rng.choice(T_PREFILL, n, replace=False)
+        t0 = time.perf_counter()
+        oracle.forward(x, w_r, None, experts, shared, K, tokens=toks, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = n / (ms / 1e3)
+    sample = f"{n} random tokens of the T=4096 prefill workload per step, full layer per token"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "prefill T=4096 d=2048 E=256 top-8 f=512 + shared (balanced)",
+                   "T": T_PREFILL, "d": D, "experts": E, "top_k": K, "ffn_dim": F,
+                   "shared_ffn_dim": FS},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def device_weights(torch, seed, layer, dims, bias=None):
+    W = {}
+    s = torch.cuda.current_stream().cuda_stream
+    for nm in synth.WEIGHT_NAMES:
+        t = torch.empty(synth.weight_shape(nm, dims), dtype=torch.bfloat16, device="cuda")
+        synth.device_weight(seed, layer, nm, dims, t.data_ptr(), s)
+        W["w_router" if nm == "w_r" else nm] = t
+    if bias is not None:
+        W["router_bias"] = torch.from_numpy(bias).cuda()
+    return W
+
+
+def run_prefill(torch, moe, args, rank, world, P_hbm, P_tc, peak_note):
+    dims = synth.Dims(d=D, f=F, fs=FS)
+    seed = rank  # each rank its own batch and weights
+    W = device_weights(torch, seed, 0, dims)
+    x = torch.from_numpy(synth.x_rows(seed, 0, T_PREFILL, D).view(np.int16)).cuda() \
+        .view(torch.bfloat16)
+    y = torch.empty_like(x)
+    layer = moe.MoeLayer(W, T_PREFILL)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    counts = np.diff(layer.route(x)["offsets"].cpu().numpy())
+    for _ in range(args.warmup):
+        layer.forward(x, y)
+    torch.cuda.synchronize()
+    assert layer.device_error() == moe.MOE_OK
+
+    # headline: per-step device time of the layer, L2 flushed (untimed) before each step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        layer.forward(x, y)
+        b.record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = reduce_max(torch, world, statistics.mean(step_ms))
+
+    # per-kernel durations (events between the kernels; kernels serialised)
+    nprof = min(args.steps, 200)
+    assert moe.moe_profile_begin(layer.handle, nprof) == moe.MOE_OK
+    for _ in range(nprof):
+        flush.zero_()
+        layer.forward(x, y)
+    st, kms, ncalls = moe.moe_profile_end(layer.handle)
+    assert st == moe.MOE_OK and ncalls == nprof
+    kms = [t / ncalls for t in kms]
+
+    # end to end through the host entry point
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for _ in range(3):
+        layer.forward_host(xh, yh)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in ev2:
+        flush.zero_()
+        a.record()
+        layer.forward_host(xh, yh)
+        b.record()
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(torch, world, statistics.mean(a.elapsed_time(b) for a, b in ev2))
+    assert layer.device_error() == moe.MOE_OK
+
+    byts, flops, layer_bytes, layer_flops = algorithmic(counts, T_PREFILL)
+    kt = dict(zip(KERNELS_GEMM, kms))
+    dom = max(kt, key=kt.get)
+    t_dom = kt[dom] / 1e3
+    ridge = P_tc * 1e12 / (P_hbm * 1e9)
+    if dom in flops and flops[dom] / byts[dom] > ridge:
+        roof = {"bound": "tensor", "achieved": flops[dom] / t_dom / 1e12, "peak": P_tc,
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": byts[dom] / t_dom / 1e9, "peak": P_hbm,
+                "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["peak_source"] = peak_note
+    roof["traffic"] = profiled_traffic(dom)
+    roof["kernel_ms"] = {k: round(v, 5) for k, v in kt.items()}
+    t_layer = ms / 1e3
+    stats = {"hbm_frac": layer_bytes / t_layer / 1e9 / P_hbm,
+             "tensor_frac": layer_flops / t_layer / 1e12 / P_tc,
+             "algorithmic_bytes": layer_bytes, "flops": layer_flops,
+             "nonempty_experts": int((counts > 0).sum()), "timed_wall_s": t_wall}
+    layer.close()
+    return dict(ms=ms, e2e_ms=e2e_ms, roofline=roof, layer=stats, launches=len(KERNELS_GEMM))
+
+
+def run_decode(torch, moe, args, rank, world, P_hbm):
+    dims = synth.Dims(d=D, f=F, fs=FS)
+    seed = 1000 + rank
+    layers, Ws = [], []
+    for l in range(DECODE_LAYERS):
+        W = device_weights(torch, seed, l, dims)
+        Ws.append(W)
+        layers.append(moe.MoeLayer(W, 1, schedule=moe.MOE_SCHEDULE_GEMV))
+    x = torch.from_numpy(synth.x_rows(seed, 0, 1, D).view(np.int16)).cuda().view(torch.bfloat16)
+    ys = [torch.empty_like(x) for _ in range(DECODE_LAYERS)]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for L, y in zip(layers, ys):  # eager warm-up before capture
+            L.forward(x, y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for L, y in zip(layers, ys):
+            L.forward(x, y)
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        g.replay()
+        b.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = reduce_max(torch, world, statistics.median(a.elapsed_time(b) for a, b in ev))
+    us_layer = ms * 1e3 / DECODE_LAYERS
+    gbs = DECODE_BYTES_PER_LAYER / (us_layer * 1e-6) / 1e9
+    # per-kernel split of one layer (eager, serialised)
+    L0 = layers[0]
+    assert moe.moe_profile_begin(L0.handle, 50) == moe.MOE_OK
+    for _ in range(50):
+        L0.forward(x, ys[0])
+    st, kms, nc = moe.moe_profile_end(L0.handle)
+    for L in layers:
+        assert L.device_error() == moe.MOE_OK
+        L.close()
+    return {"us_per_layer": us_layer, "GB_per_s": gbs, "layers": DECODE_LAYERS,
+            "bytes_per_layer": DECODE_BYTES_PER_LAYER,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": P_hbm, "unit": "GB/s",
+                         "frac": gbs / P_hbm},
+            "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in zip(KERNELS_GEMV, kms)},
+            "gpu_launches": args.steps * DECODE_LAYERS * 3,
+            "graph": "40 stream-ordered layer calls, replayed per step"}
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on the
+    current source of that kernel (profiles/traffic.txt lines: kernel bytes source-sha)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"router_topk": "route.cu", "route_plan": "route.cu", "route_scatter": "route.cu",
+           "gateup": "experts.cu", "down": "experts.cu", "combine": "experts.cu"}.get(kernel)
+    if not src:
+        return None
+    sha = hashlib.sha1(open(os.path.join(ROOT, "sparse_moe_02_gb300", "csrc", src), "rb")
+                       .read()).hexdigest()[:12]
+    for ln in open(path):
+        f = ln.split()
+        if len(f) >= 3 and f[0] == kernel and f[2] == sha:
+            return float(f[1])
+    return None
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(torch, world, v):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+    import torch
+    import sparse_moe_02_gb300 as moe
+    moe.lib()  # fail loudly if the CUDA library is not built
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    P_hbm, P_tc, note = peaks()
+    clocks = ClockSampler(gpu_smi_id(torch, local))
+    clocks.start()
+    pre = run_prefill(torch, moe, args, rank, world, P_hbm, P_tc, note)
+    dec = None if args.no_decode else run_decode(torch, moe, args, rank, world, P_hbm)
+    clk = clocks.stop()
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, sample, cores = oracle_sample_rate(args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": sample}
+    if rank != 0:
+        return
+    value = world * T_PREFILL / (pre["ms"] / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "prefill T=4096 d=2048 E=256 top-8 f=512 + shared (balanced)",
+                   "T": T_PREFILL, "d": D, "experts": E, "top_k": K, "ffn_dim": F,
+                   "shared_ffn_dim": FS, "parallelism": f"dp{world} (independent batches)",
+                   "l2": "flushed (256 MB write, untimed) before every timed step; weights "
+                         "1.62 GB > L2"},
+        "roofline": pre["roofline"],
+        "layer": pre["layer"],
+        "decode": dec,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * T_PREFILL / (pre["e2e_ms"] / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": T_PREFILL * D * 2, "d2h_bytes_per_step": T_PREFILL * D * 2},
+        "gpu_launches": args.steps * pre["launches"],
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

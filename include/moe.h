@@ -131,6 +131,18 @@ const char* moe_status_string(int status);
 /* The cudaError_t of the last failed CUDA call made by this library in this thread. */
 int moe_last_cuda_error(void);
 
+/* Per-kernel timing, for benchmarks and profilers.  moe_profile_begin(h, n_calls) makes the
+ * next n_calls (1..1024) calls of moe_forward record a CUDA event on their stream before each
+ * kernel and after the last one (this serialises the kernels of those calls, so the times are
+ * per kernel without overlap).  moe_profile_end synchronises on those events, writes to
+ * ms[i] the device time of the i-th kernel summed over the recorded calls (i < *n_kernels,
+ * at most `capacity` entries), sets *n_calls to the number of calls recorded, and stops
+ * profiling.  Kernel order -- tensor-core schedule (6): router_topk, route_plan,
+ * route_scatter, gateup, down, combine; matrix-vector schedule (3): decode_router_shared,
+ * decode_gateup, decode_down_combine.  All recorded calls must use one schedule. */
+int moe_profile_begin(moe_handle h, int n_calls);
+int moe_profile_end(moe_handle h, float* ms, int capacity, int* n_kernels, int* n_calls);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,12 @@ MOE_SCHEDULE_GEMM = 1
 MOE_SCHEDULE_GEMV = 2
 
 EXPORTS = ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_get_device_error",
-           "moe_destroy", "moe_status_string", "moe_last_cuda_error")
+           "moe_destroy", "moe_status_string", "moe_last_cuda_error", "moe_profile_begin",
+           "moe_profile_end")
+
+# kernel order reported by moe_profile_end
+KERNELS_GEMM = ("router_topk", "route_plan", "route_scatter", "gateup", "down", "combine")
+KERNELS_GEMV = ("decode_router_shared", "decode_gateup", "decode_down_combine")
 
 _c_int, _c_void_p = ctypes.c_int, ctypes.c_void_p
 
@@ -65,8 +70,12 @@ def lib():
         L.moe_status_string.argtypes = [_c_int]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_last_cuda_error.argtypes = []
+        L.moe_profile_begin.argtypes = [_c_void_p, _c_int]
+        L.moe_profile_end.argtypes = [_c_void_p, ctypes.POINTER(ctypes.c_float), _c_int,
+                                      ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]
         for fn in ("moe_create", "moe_route", "moe_forward", "moe_forward_host",
-                   "moe_get_device_error", "moe_destroy", "moe_last_cuda_error"):
+                   "moe_get_device_error", "moe_destroy", "moe_last_cuda_error",
+                   "moe_profile_begin", "moe_profile_end"):
             getattr(L, fn).restype = _c_int
         _lib = L
     return _lib
@@ -105,6 +114,18 @@ def moe_status_string(status):
 
 def moe_last_cuda_error():
     return lib().moe_last_cuda_error()
+
+
+def moe_profile_begin(h, n_calls):
+    return lib().moe_profile_begin(h, n_calls)
+
+
+def moe_profile_end(h):
+    """Returns (status, [ms per kernel summed over the recorded calls], n_calls)."""
+    ms = (ctypes.c_float * 8)()
+    nk, nc = _c_int(), _c_int()
+    st = lib().moe_profile_end(h, ms, 8, ctypes.byref(nk), ctypes.byref(nc))
+    return st, list(ms)[:nk.value], nc.value
 
 
 class MoeError(RuntimeError):

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "layer.cuh"
 #include "moe.h"
@@ -73,6 +74,10 @@ struct moe_handle_s {
   __nv_bfloat16* x_stage = nullptr;
   __nv_bfloat16* y_stage = nullptr;
   CUtensorMap tm_wr, tm_wg, tm_wu, tm_wsg, tm_wsu, tm_wd, tm_wsd, tm_h;
+  // per-kernel timing (moe_profile_begin / moe_profile_end)
+  static constexpr int kMaxKernels = 6;
+  std::vector<cudaEvent_t> prof_ev;  // [n_calls][kMaxKernels + 1]
+  int prof_calls = 0, prof_done = 0, prof_nk = 0;
 };
 
 namespace {
@@ -168,22 +173,41 @@ int check_call(moe_handle h, const void* x, int T) {
   return MOE_OK;
 }
 
+// Records the profiling event before kernel i (or after the last kernel, i = nk) of the
+// current call when profiling is on.
+int prof_mark(moe_handle h, cudaStream_t s, int i) {
+  if (h->prof_done >= h->prof_calls) return MOE_OK;
+  return cuda_status(cudaEventRecord(
+      h->prof_ev[(size_t)h->prof_done * (moe_handle_s::kMaxKernels + 1) + i], s));
+}
+
+int prof_finish_call(moe_handle h, cudaStream_t s, int nk) {
+  if (h->prof_done >= h->prof_calls) return MOE_OK;
+  int st = prof_mark(h, s, nk);
+  h->prof_nk = nk;
+  ++h->prof_done;
+  return st;
+}
+
 bool use_gemv(const moe_handle_s* h, int T) {
   return T == 1 && h->cfg.schedule != MOE_SCHEDULE_GEMM;
 }
 
 // The routing chain of the tensor-core schedule.
 int run_route_gemm(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w,
-                   int32_t* offsets, int32_t* perm, cudaStream_t s, CUtensorMap* tm_xg) {
+                   int32_t* offsets, int32_t* perm, cudaStream_t s, bool prof) {
   CUtensorMap tm_x;
   if (!encode_2d(&tm_x, x, h->D.d, T, moe::kBK, moe::kBlockTokens)) return MOE_ERR_CUDA;
-  if (tm_xg && !encode_2d(tm_xg, x, h->D.d, T, moe::kBK, 1)) return MOE_ERR_CUDA;
   moe::RouteWs w = h->rws;
   if (offsets) w.offsets = offsets;
-  int st = cuda_status(moe::launch_router_topk(tm_x, h->tm_wr, h->w.router_bias, T, h->D,
-                                               topk_idx, topk_w, w, s));
-  if (st) return st;
+  int st;
+  if (prof && (st = prof_mark(h, s, 0))) return st;
+  if ((st = cuda_status(moe::launch_router_topk(tm_x, h->tm_wr, h->w.router_bias, T, h->D,
+                                                topk_idx, topk_w, w, s))))
+    return st;
+  if (prof && (st = prof_mark(h, s, 1))) return st;
   if ((st = cuda_status(moe::launch_route_plan(T, h->D, w, s)))) return st;
+  if (prof && (st = prof_mark(h, s, 2))) return st;
   return cuda_status(moe::launch_route_scatter(T, topk_idx, perm, w, s));
 }
 
@@ -269,7 +293,7 @@ int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk
     return cuda_status(moe::launch_decode_router_shared(
         static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, idx, wt,
         offsets ? offsets : h->rws.offsets, pm, h->dws, h->rws.err, s, false));
-  return run_route_gemm(h, x, T, idx, wt, offsets, pm, s, nullptr);
+  return run_route_gemm(h, x, T, idx, wt, offsets, pm, s, false);
 }
 
 int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
@@ -287,27 +311,36 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
 
   if (use_gemv(h, T)) {
     const moe::DecodeWeights W = decode_weights(h);
+    if ((st = prof_mark(h, s, 0))) return st;
     if ((st = cuda_status(moe::launch_decode_router_shared(xd, W, h->D, h->rws.topk_idx,
                                                            h->rws.topk_w, nullptr, nullptr,
                                                            h->dws, h->rws.err, s, true))))
       return st;
+    if ((st = prof_mark(h, s, 1))) return st;
     if ((st = cuda_status(moe::launch_decode_gateup(xd, W, h->D, h->rws.topk_idx, h->dws, s))))
       return st;
-    return cuda_status(moe::launch_decode_down_combine(W, h->D, h->rws.topk_idx, h->rws.topk_w,
-                                                       h->dws, yd, s));
+    if ((st = prof_mark(h, s, 2))) return st;
+    if ((st = cuda_status(moe::launch_decode_down_combine(W, h->D, h->rws.topk_idx,
+                                                          h->rws.topk_w, h->dws, yd, s))))
+      return st;
+    return prof_finish_call(h, s, 3);
   }
 
-  CUtensorMap tm_xg;
   if ((st = run_route_gemm(h, x, T, h->rws.topk_idx, h->rws.topk_w, nullptr, h->rws.perm, s,
-                           &tm_xg)))
+                           true)))
     return st;
-  if ((st = cuda_status(moe::launch_gateup(tm_xg, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu, h->D,
+  if ((st = prof_mark(h, s, 3))) return st;
+  if ((st = cuda_status(moe::launch_gateup(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu, h->D,
                                            h->rws, h->h, h->sms, s))))
     return st;
+  if ((st = prof_mark(h, s, 4))) return st;
   if ((st = cuda_status(
            moe::launch_down(h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->ys, h->sms, s))))
     return st;
-  return cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, s));
+  if ((st = prof_mark(h, s, 5))) return st;
+  if ((st = cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, s))))
+    return st;
+  return prof_finish_call(h, s, 6);
 }
 
 int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void* stream) {
@@ -335,8 +368,57 @@ int moe_get_device_error(moe_handle h, void* stream) {
   return v;
 }
 
+namespace {
+void prof_release(moe_handle h) {
+  for (cudaEvent_t e : h->prof_ev) cudaEventDestroy(e);
+  h->prof_ev.clear();
+  h->prof_calls = h->prof_done = h->prof_nk = 0;
+}
+}  // namespace
+
+int moe_profile_begin(moe_handle h, int n_calls) {
+  if (!h || n_calls < 1 || n_calls > 1024) return MOE_ERR_INVALID_ARG;
+  prof_release(h);
+  const size_t n = (size_t)n_calls * (moe_handle_s::kMaxKernels + 1);
+  h->prof_ev.reserve(n);
+  for (size_t i = 0; i < n; ++i) {
+    cudaEvent_t e;
+    int st = cuda_status(cudaEventCreate(&e));
+    if (st) {
+      prof_release(h);
+      return st;
+    }
+    h->prof_ev.push_back(e);
+  }
+  h->prof_calls = n_calls;
+  return MOE_OK;
+}
+
+int moe_profile_end(moe_handle h, float* ms, int capacity, int* n_kernels, int* n_calls) {
+  if (!h || !ms || capacity < 0 || !n_kernels || !n_calls) return MOE_ERR_INVALID_ARG;
+  const int nk = h->prof_nk, done = h->prof_done, stride = moe_handle_s::kMaxKernels + 1;
+  for (int i = 0; i < capacity; ++i) ms[i] = 0.f;
+  int st = MOE_OK;
+  for (int c = 0; c < done && st == MOE_OK; ++c) {
+    for (int i = 0; i < nk && i < capacity; ++i) {
+      float t = 0.f;
+      st = cuda_status(cudaEventSynchronize(h->prof_ev[(size_t)c * stride + i + 1]));
+      if (st) break;
+      st = cuda_status(cudaEventElapsedTime(&t, h->prof_ev[(size_t)c * stride + i],
+                                            h->prof_ev[(size_t)c * stride + i + 1]));
+      if (st) break;
+      ms[i] += t;
+    }
+  }
+  *n_kernels = nk;
+  *n_calls = done;
+  prof_release(h);
+  return st;
+}
+
 int moe_destroy(moe_handle h) {
   if (!h) return MOE_OK;
+  prof_release(h);
   int st = MOE_OK;
   if (h->ws) st = cuda_status(cudaFree(h->ws));
   delete h;

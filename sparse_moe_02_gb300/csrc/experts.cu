@@ -9,10 +9,10 @@
 // GB300 design: the weights take the MMA's M = 128 side and the routed token rows the
 // N side (16..256 in steps of 16), so an expert with few tokens still uses full-height MMAs
 // and its weight tile is read once per chunk of up to 256 tokens.  One persistent block per
-// SM walks the work-unit list: warp 0 feeds a shared-memory ring with TMA (weights as
-// 128-row tiles, token rows gathered four at a time straight from x with tile::gather4, so
-// no permuted copy of x is ever written), warp 1 issues tcgen05.mma into TMEM, and warps
-// 2-5 drain TMEM (SwiGLU for gate/up, plain bf16 for down) while the ring refills.
+// SM walks the work-unit list: the weight tiles reach a shared-memory ring by TMA (128-row
+// tiles) and the routed token rows by 16-byte cp.async gathers straight from x (so
+// no permuted copy of x is ever written), warp 1 issues tcgen05.mma into TMEM, and the
+// epilogue warps drain TMEM (SwiGLU for gate/up, plain bf16 for down) while the ring refills.
 #include "layer.cuh"
 #include "ptx.cuh"
 
@@ -27,20 +27,26 @@ constexpr int kTileB = kChunkRows * kBK * 2; // up to 256 token rows x 64 (32 KB
 constexpr int kGuStages = 3;
 constexpr int kGuStage = 2 * kTileA + kTileB;  // gate tile | up tile | token rows
 constexpr int kGuSmem = kGuStages * kGuStage + 1024 + 1024;
+constexpr int kGuThreads = 384;                // 12 warps, roles below
+constexpr int kGuRowThreads = 64;              // warps 2-3: token-row copies
+constexpr int kGuEpiWarps = 8;                 // warps 4-11: two per TMEM lane quadrant
 
 struct GuArgs {
   const Unit* units;
   const int32_t* n_units;
   const int32_t* grow;
+  const __nv_bfloat16* x;
   __nv_bfloat16* h;
   int d, f, hdim;
   int* err;
 };
 
-__global__ void __launch_bounds__(192, 1)
-    gateup_kernel(const __grid_constant__ CUtensorMap tm_xg,
-                  const __grid_constant__ CUtensorMap tm_wg,
-                  const __grid_constant__ CUtensorMap tm_wu,
+// Warp roles: 0 = TMA producer of the gate and up weight tiles; 1 = MMA issuer (and TMEM
+// owner); 2-3 = producers of the token rows (gathered from x by 16-byte cp.async straight
+// into the 128-byte-swizzled layout: row r, chunk c lands at r*128 + ((c ^ (r & 7)) * 16));
+// 4-11 = epilogue, two warps per TMEM lane quadrant, each taking alternate 16-column chunks.
+__global__ void __launch_bounds__(kGuThreads, 1)
+    gateup_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                   const __grid_constant__ CUtensorMap tm_wsg,
                   const __grid_constant__ CUtensorMap tm_wsu, GuArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -56,11 +62,11 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGuStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + kGuRowThreads);  // weight TMA + one arrival per row thread
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 4);
+    mbar_init(tempty, kGuEpiWarps);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -75,53 +81,30 @@ __global__ void __launch_bounds__(192, 1)
   const int n_units = *a.n_units;
 
   if (warp == 0) {
-    // ---- producer: weights by tiled TMA, token rows by 4-row gathers
+    // ---- weight tiles (gate and up, 128 rows x 64 each) by tiled TMA
     if (lane == 0) {
-      prefetch_tensormap(&tm_xg);
       prefetch_tensormap(&tm_wg);
       prefetch_tensormap(&tm_wu);
       prefetch_tensormap(&tm_wsg);
       prefetch_tensormap(&tm_wsu);
-    }
-    const uint64_t stream_w = policy_evict_first();  // each weight tile is read once
-    const uint64_t keep_x = policy_evict_last();     // x rows are gathered many times
-    int stage = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit U = a.units[u];
-      const int N = round_up(U.nrows, kRowAlign);
-      const int nq = N / 4;
-      const bool shared = U.g == kE;
-      const CUtensorMap* mg = shared ? &tm_wsg : &tm_wg;
-      const CUtensorMap* mu = shared ? &tm_wsu : &tm_wu;
-      const int arow = (shared ? 0 : U.g * a.f) + U.mt * kMTile;
-      int ra[4], rb[4];
-      const int qa = lane, qb = lane + 32;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        ra[i] = qa < nq ? a.grow[U.p0 + 4 * qa + i] : 0;
-        rb[i] = qb < nq ? a.grow[U.p0 + 4 * qb + i] : 0;
-      }
-      const uint32_t bytes = 2 * kTileA + (uint32_t)N * kBK * 2;
-      for (int kb = 0; kb < KB; ++kb) {
-        const bool w = mbar_wait(&empty[stage], ph ^ 1, a.err);
-        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        uint8_t* st = smem + stage * kGuStage;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], bytes);
+      const uint64_t stream_w = policy_evict_first();  // each weight tile is read once
+      int stage = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit U = a.units[u];
+        const bool shared = U.g == kE;
+        const CUtensorMap* mg = shared ? &tm_wsg : &tm_wg;
+        const CUtensorMap* mu = shared ? &tm_wsu : &tm_wu;
+        const int arow = (shared ? 0 : U.g * a.f) + U.mt * kMTile;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
+          uint8_t* st = smem + stage * kGuStage;
+          mbar_arrive_expect_tx(&full[stage], 2 * kTileA);
           tma_load_2d(st, mg, &full[stage], kb * kBK, arow, stream_w);
           tma_load_2d(st + kTileA, mu, &full[stage], kb * kBK, arow, stream_w);
+          if (++stage == kGuStages) { stage = 0; ph ^= 1; }
         }
-        __syncwarp();
-        uint8_t* sb = st + 2 * kTileA;
-        if (qa < nq)
-          tma_gather4(sb + qa * 512, &tm_xg, &full[stage], kb * kBK, ra[0], ra[1], ra[2], ra[3],
-                      keep_x);
-        if (qb < nq)
-          tma_gather4(sb + qb * 512, &tm_xg, &full[stage], kb * kBK, rb[0], rb[1], rb[2], rb[3],
-                      keep_x);
-        if (++stage == kGuStages) { stage = 0; ph ^= 1; }
       }
     }
   } else if (warp == 1) {
@@ -138,6 +121,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&full[stage], ph, a.err)) { ok = false; break; }
+          fence_proxy_async_smem();  // token rows were written by cp.async (generic proxy)
           tc_fence_after();
           const uint32_t sg = smem_u32(smem + stage * kGuStage);
           const uint32_t su = sg + kTileA, sb = sg + 2 * kTileA;
@@ -155,9 +139,38 @@ __global__ void __launch_bounds__(192, 1)
         tph ^= 1;
       }
     }
+  } else if (warp < 4) {
+    // ---- token rows: thread (crow, chunk) copies 16-byte chunk `chunk` of rows crow + 8i
+    const int bt = threadIdx.x - 64;
+    const int crow = bt >> 3, chunk = bt & 7;
+    const uint32_t swz = (uint32_t)((chunk ^ crow) << 4);  // (r & 7) == crow for every row
+    const uint64_t keep_x = policy_evict_last();            // x rows are gathered many times
+    int stage = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit U = a.units[u];
+      const int N = round_up(U.nrows, kRowAlign);
+      const int nr = N / 8;  // rows per thread, <= 32
+      const __nv_bfloat16* src[kChunkRows / 8];
+#pragma unroll
+      for (int i = 0; i < kChunkRows / 8; ++i)
+        src[i] = a.x + (size_t)(i < nr ? __ldg(a.grow + U.p0 + crow + 8 * i) : 0) * a.d +
+                 chunk * 8;
+      for (int kb = 0; kb < KB; ++kb) {
+        const bool w = mbar_wait(&empty[stage], ph ^ 1, a.err);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        const uint32_t sb = smem_u32(smem + stage * kGuStage + 2 * kTileA) + crow * 128 + swz;
+#pragma unroll
+        for (int i = 0; i < kChunkRows / 8; ++i)
+          if (i < nr) cp_async_16(sb + i * 1024, src[i] + kb * kBK, keep_x);
+        cp_async_arrive_noinc(&full[stage]);
+        if (++stage == kGuStages) { stage = 0; ph ^= 1; }
+      }
+    }
   } else {
     // ---- epilogue: thread = one feature row; h = silu(gate) * up for each token column
-    const int q = warp & 3;
+    const int q = warp & 3, half = (warp - 4) >> 2;
     const int m = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     uint32_t tph = 0;
@@ -168,7 +181,7 @@ __global__ void __launch_bounds__(192, 1)
       if (!__all_sync(0xffffffffu, w)) break;
       tc_fence_after();
       __nv_bfloat16* hp = a.h + (size_t)U.p0 * a.hdim + U.mt * kMTile + m;
-      for (int j0 = 0; j0 < N; j0 += 16) {
+      for (int j0 = half * 16; j0 < N; j0 += 32) {
         uint32_t g[16], v[16];
         tmem_ld16(tmem + lane_off + (uint32_t)j0, g);
         tmem_ld16(tmem + lane_off + 256u + (uint32_t)j0, v);
@@ -392,12 +405,12 @@ cudaError_t prepare_expert_kernels() {
   return cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDnSmem);
 }
 
-cudaError_t launch_gateup(const CUtensorMap& tm_xg, const CUtensorMap& tm_wg,
+cudaError_t launch_gateup(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
                           const CUtensorMap& tm_wu, const CUtensorMap& tm_wsg,
                           const CUtensorMap& tm_wsu, const Dims& D, const RouteWs& ws,
                           __nv_bfloat16* h, int grid, cudaStream_t s) {
-  GuArgs a{ws.units_gu, ws.n_units, ws.grow, h, D.d, D.f, D.hdim, ws.err};
-  return launch_pdl(gateup_kernel, dim3(grid), dim3(192), kGuSmem, s, tm_xg, tm_wg, tm_wu, tm_wsg,
+  GuArgs a{ws.units_gu, ws.n_units, ws.grow, x, h, D.d, D.f, D.hdim, ws.err};
+  return launch_pdl(gateup_kernel, dim3(grid), dim3(kGuThreads), kGuSmem, s, tm_wg, tm_wu, tm_wsg,
                     tm_wsu, a);
 }
 

@@ -85,7 +85,7 @@ cudaError_t launch_route_scatter(int T, const int32_t* topk_idx, int32_t* perm,
                                  const RouteWs& ws, cudaStream_t s);
 
 // Grouped gate/up GEMM with SwiGLU epilogue: h [P][hdim] bf16.
-cudaError_t launch_gateup(const CUtensorMap& tm_xg, const CUtensorMap& tm_wg,
+cudaError_t launch_gateup(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
                           const CUtensorMap& tm_wu, const CUtensorMap& tm_wsg,
                           const CUtensorMap& tm_wsu, const Dims& D, const RouteWs& ws,
                           __nv_bfloat16* h, int grid, cudaStream_t s);

@@ -1,4 +1,4 @@
-// Inline-PTX primitives for sm_103a: mbarriers, TMA (tiled and 4-row gather), tcgen05
+// Inline-PTX primitives for sm_103a: mbarriers, TMA (tiled), cp.async, tcgen05
 // (TMEM allocation, MMA, commit, loads), programmatic dependent launch, bounded waits.
 #pragma once
 
@@ -99,17 +99,24 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Gathers four rows r0..r3 (box one row high, inner coordinate c0) into four consecutive
-// box rows in shared memory.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int c0, int r0, int r1, int r2, int r3,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1),
-      "r"(r2), "r"(r3), "l"(policy)
-      : "memory");
+// 16-byte asynchronous copy global -> shared (L2 only), with an L2 cache policy.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(src), "l"(policy)
+               : "memory");
+}
+
+// Arrives on `bar` once every cp.async this thread issued so far has completed; the arrival
+// counts toward the barrier's expected count (no increment of the pending count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Orders this thread's view of shared memory written through the generic proxy (cp.async,
+// st.shared) before its later async-proxy accesses (tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -220,8 +227,10 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   return r;
 }
 
+// silu(g) * u with silu(g) = g / (1 + e^-g); fast exponential and division (the result is
+// rounded to bf16).  For g -> -inf the divisor overflows to +inf and the quotient is 0.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-  return (g / (1.0f + __expf(-g))) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 }  // namespace moe

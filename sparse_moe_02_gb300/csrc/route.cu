@@ -218,12 +218,19 @@ __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws)
   __shared__ int tmp[16];
   pdl_wait();
   const int e = threadIdx.x;
+  // loads first (read-only path), then the prefix stores: keeps 16 loads in flight
   int run = 0;
-#pragma unroll 8
-  for (int b = 0; b < p.nblk; ++b) {
-    const int c = ws.hist[(size_t)b * kE + e];
-    ws.blkpre[(size_t)b * kE + e] = run;
-    run += c;
+  for (int b0 = 0; b0 < p.nblk; b0 += 16) {
+    int c[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      c[i] = b0 + i < p.nblk ? __ldg(ws.hist + (size_t)(b0 + i) * kE + e) : 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (b0 + i < p.nblk) {
+        ws.blkpre[(size_t)(b0 + i) * kE + e] = run;
+        run += c[i];
+      }
   }
   const int cnt = run;
   const int pc = round_up(cnt, kRowAlign);
@@ -302,20 +309,30 @@ __global__ void __launch_bounds__(128) route_scatter_kernel(int T, const int32_t
   }
   __syncthreads();
   if (valid) {
+    // all loads (read-only path) before the scattered stores
     const uint32_t below = (1u << lane) - 1u;
+    int rank[8], off[8], po[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int ee = e[j];
-      int rank = ws.blkpre[(size_t)blk * kE + ee] + __popc(mask[warp][ee] & below);
-      for (int w = 0; w < warp; ++w) rank += __popc(mask[w][ee]);
-      perm[ws.offsets[ee] + rank] = t * kTopK + j;
-      const int pr = ws.poff[ee] + rank;
-      ws.prow[(size_t)t * 9 + j] = pr;
-      ws.grow[pr] = t;
+      rank[j] = __ldg(ws.blkpre + (size_t)blk * kE + ee) + __popc(mask[warp][ee] & below);
+      for (int w = 0; w < warp; ++w) rank[j] += __popc(mask[w][ee]);
+      off[j] = __ldg(ws.offsets + ee);
+      po[j] = __ldg(ws.poff + ee);
     }
-    const int ps = ws.poff[kE] + t;
-    ws.prow[(size_t)t * 9 + 8] = ps;
+    const int ps = __ldg(ws.poff + kE) + t;
+    int pr[9];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      perm[off[j] + rank[j]] = t * kTopK + j;
+      pr[j] = po[j] + rank[j];
+      ws.grow[pr[j]] = t;
+    }
+    pr[8] = ps;
     ws.grow[ps] = t;
+    int* prow = ws.prow + (size_t)t * 9;
+#pragma unroll
+    for (int j = 0; j < 9; ++j) prow[j] = pr[j];
   }
   pdl_trigger();
 }
