@@ -48,6 +48,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target duration of the CPU oracle sample")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-prefill", action="store_true", help="decode only (profiling runs)")
+    p.add_argument("--decode-layers", type=int, default=DECODE_LAYERS,
+                   help="layers in the decode graph (40 = the benchmark workload)")
     p.add_argument("--no-cpu", action="store_true")
     return p.parse_args()
 
@@ -335,12 +338,13 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
     dims = synth.Dims(d=D, f=F, fs=FS)
     seed = 1000 + rank
     layers, Ws = [], []
-    for l in range(DECODE_LAYERS):
+    nl = args.decode_layers
+    for l in range(nl):
         W = device_weights(torch, seed, l, dims)
         Ws.append(W)
         layers.append(moe.MoeLayer(W, 1, schedule=moe.MOE_SCHEDULE_GEMV))
     x = torch.from_numpy(synth.x_rows(seed, 0, 1, D).view(np.int16)).cuda().view(torch.bfloat16)
-    ys = [torch.empty_like(x) for _ in range(DECODE_LAYERS)]
+    ys = [torch.empty_like(x) for _ in range(nl)]
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for L, y in zip(layers, ys):  # eager warm-up before capture
@@ -364,7 +368,7 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
     torch.cuda.synchronize()
     barrier(world)
     ms = reduce_max(torch, world, statistics.median(a.elapsed_time(b) for a, b in ev))
-    us_layer = ms * 1e3 / DECODE_LAYERS
+    us_layer = ms * 1e3 / nl
     gbs = DECODE_BYTES_PER_LAYER / (us_layer * 1e-6) / 1e9
     # per-kernel split of one layer (eager, serialised)
     L0 = layers[0]
@@ -375,13 +379,13 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
     for L in layers:
         assert L.device_error() == moe.MOE_OK
         L.close()
-    return {"us_per_layer": us_layer, "GB_per_s": gbs, "layers": DECODE_LAYERS,
+    return {"us_per_layer": us_layer, "GB_per_s": gbs, "layers": nl,
             "bytes_per_layer": DECODE_BYTES_PER_LAYER,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": P_hbm, "unit": "GB/s",
                          "frac": gbs / P_hbm},
             "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in zip(KERNELS_GEMV, kms)},
-            "gpu_launches": args.steps * DECODE_LAYERS * 3,
-            "graph": "40 stream-ordered layer calls, replayed per step"}
+            "gpu_launches": args.steps * nl * 3,
+            "graph": f"{nl} stream-ordered layer calls, replayed per step"}
 
 
 def profiled_traffic(kernel):
@@ -437,6 +441,12 @@ def main():
     P_hbm, P_tc, note = peaks()
     clocks = ClockSampler(gpu_smi_id(torch, local))
     clocks.start()
+    if args.no_prefill:
+        dec = run_decode(torch, moe, args, rank, world, P_hbm)
+        clk = clocks.stop()
+        if rank == 0:
+            print(json.dumps({"decode": dec, "clocks": clk}), flush=True)
+        return
     pre = run_prefill(torch, moe, args, rank, world, P_hbm, P_tc, note)
     dec = None if args.no_decode else run_decode(torch, moe, args, rank, world, P_hbm)
     clk = clocks.stop()

@@ -312,17 +312,16 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
   if (use_gemv(h, T)) {
     const moe::DecodeWeights W = decode_weights(h);
     if ((st = prof_mark(h, s, 0))) return st;
-    if ((st = cuda_status(moe::launch_decode_router_shared(xd, W, h->D, h->rws.topk_idx,
-                                                           h->rws.topk_w, nullptr, nullptr,
-                                                           h->dws, h->rws.err, s, true))))
+    if ((st = cuda_status(moe::launch_decode_router_shared(xd, W, h->D, nullptr, nullptr,
+                                                           nullptr, nullptr, h->dws, h->rws.err,
+                                                           s, true))))
       return st;
     if ((st = prof_mark(h, s, 1))) return st;
-    if ((st = cuda_status(moe::launch_decode_gateup(xd, W, h->D, h->rws.topk_idx, h->dws, s))))
+    if ((st = cuda_status(moe::launch_decode_gateup(xd, W, h->D, h->rws.topk_idx, h->rws.topk_w,
+                                                    h->dws, s))))
       return st;
     if ((st = prof_mark(h, s, 2))) return st;
-    if ((st = cuda_status(moe::launch_decode_down_combine(W, h->D, h->rws.topk_idx,
-                                                          h->rws.topk_w, h->dws, yd, s))))
-      return st;
+    if ((st = cuda_status(moe::launch_decode_down_combine(W, h->D, h->dws, yd, s)))) return st;
     return prof_finish_call(h, s, 3);
   }
 

@@ -11,6 +11,8 @@
 // top-8 selection done by the last router block to finish; (2) the 8 selected experts'
 // gate/up rows; (3) the down rows of the 8 experts and the shared expert, weighted and
 // summed in fixed order per output.
+#include <algorithm>
+
 #include "layer.cuh"
 #include "ptx.cuh"
 
@@ -18,6 +20,7 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 8;  // warps per block in every decode kernel
+constexpr int kPre = 8;    // 16-byte chunks per lane held in registers per input row
 
 __device__ __forceinline__ float dot8(uint4 w, uint4 x) {
   const uint32_t a[4] = {w.x, w.y, w.z, w.w}, b[4] = {x.x, x.y, x.z, x.w};
@@ -30,18 +33,59 @@ __device__ __forceinline__ float dot8(uint4 w, uint4 x) {
   return s;
 }
 
+// 8 bf16 weights times 8 fp32 values from shared memory.
+__device__ __forceinline__ float dot8_f32(uint4 w, const float* h) {
+  const float4 h0 = *reinterpret_cast<const float4*>(h);
+  const float4 h1 = *reinterpret_cast<const float4*>(h + 4);
+  float acc = bf16_lo(w.x) * h0.x;
+  acc = fmaf(bf16_hi(w.x), h0.y, acc);
+  acc = fmaf(bf16_lo(w.y), h0.z, acc);
+  acc = fmaf(bf16_hi(w.y), h0.w, acc);
+  acc = fmaf(bf16_lo(w.z), h1.x, acc);
+  acc = fmaf(bf16_hi(w.z), h1.y, acc);
+  acc = fmaf(bf16_lo(w.w), h1.z, acc);
+  return fmaf(bf16_hi(w.w), h1.w, acc);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// Partial dot product of one bf16 row (nch 16-byte chunks) with x in shared memory.
-__device__ __forceinline__ float row_dot_partial(const __nv_bfloat16* row, const uint4* xs,
-                                                 int nch, int lane) {
+// Up to kPre*32 16-byte chunks of one bf16 row, chunk c = base + lane + 32*i in v[i].
+struct RowFrag {
+  uint4 v[kPre];
+};
+
+__device__ __forceinline__ void row_load(RowFrag& r, const __nv_bfloat16* row, int nch, int lane,
+                                         int base) {
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int c = base + lane + 32 * i;
+    if (c < nch) r.v[i] = ld_stream_u4(row + (size_t)c * 8);
+  }
+}
+
+__device__ __forceinline__ float row_dot(const RowFrag& r, const uint4* xs, int nch, int lane,
+                                         int base) {
   float acc = 0.f;
-#pragma unroll 4
-  for (int c = lane; c < nch; c += 32) acc += dot8(ld_stream_u4(row + (size_t)c * 8), xs[c]);
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    const int c = base + lane + 32 * i;
+    if (c < nch) acc += dot8(r.v[i], xs[c]);
+  }
+  return acc;
+}
+
+// Lane-partial dot product of a row with x; the first kPre*32 chunks are already in r.
+__device__ __forceinline__ float row_dot_rest(RowFrag& r, const __nv_bfloat16* row,
+                                              const uint4* xs, int nch, int lane) {
+  float acc = row_dot(r, xs, nch, lane, 0);
+  for (int base = kPre * 32; base < nch; base += kPre * 32) {
+    row_load(r, row, nch, lane, base);
+    acc += row_dot(r, xs, nch, lane, base);
+  }
   return acc;
 }
 
@@ -49,6 +93,75 @@ __device__ __forceinline__ void stage_x(const __nv_bfloat16* x, uint4* xs, int d
   const uint4* src = reinterpret_cast<const uint4*>(x);
   for (int i = threadIdx.x; i < d / 8; i += blockDim.x) xs[i] = src[i];
   __syncthreads();
+}
+
+// Order-preserving map of a float onto uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);  // -0 -> +0: equal floats get equal keys
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Warp-level selection from logits[256] (read through L2): the 8 largest (ties: lower id) in
+// ascending expert id and their softmax weights; lanes 0..7 write ids[lane], w[lane].
+// Each lane sorts its 8 logits (ids lane + 32i) by value, keeping ids ascending among equal
+// values; each round takes the warp-wide largest head value (redux max over order-preserving
+// keys), then the lowest id holding it (redux min), and that lane advances its head.
+__device__ __forceinline__ void select_top8(const float* logits, int lane, int* ids, float* w) {
+  float v[8];
+  int id[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[i] = __ldcg(logits + lane + 32 * i);
+    id[i] = lane + 32 * i;
+  }
+  // stable insertion sort, value descending (ids ascending within equal values)
+#pragma unroll
+  for (int i = 1; i < 8; ++i)
+#pragma unroll
+    for (int j = i; j > 0; --j)
+      if (v[j] > v[j - 1]) {
+        float tv = v[j]; v[j] = v[j - 1]; v[j - 1] = tv;
+        int ti = id[j]; id[j] = id[j - 1]; id[j - 1] = ti;
+      }
+  float wv[8];
+  int wi[8];
+#pragma unroll
+  for (int r = 0; r < kTopK; ++r) {
+    const uint32_t key = float_key(v[0]);
+    const uint32_t best = __reduce_max_sync(0xffffffffu, key);
+    const uint32_t win = __reduce_min_sync(0xffffffffu, key == best ? (uint32_t)id[0] : 0xffffffffu);
+    wi[r] = (int)win;
+    wv[r] = __shfl_sync(0xffffffffu, v[0], (int)(win & 31u));
+    if ((int)(win & 31u) == lane) {  // advance this lane's head
+#pragma unroll
+      for (int i = 0; i < 7; ++i) { v[i] = v[i + 1]; id[i] = id[i + 1]; }
+      v[7] = -INFINITY;
+      id[7] = 0x7fffffff;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 7; ++i)
+#pragma unroll
+    for (int j = 0; j < 7 - i; ++j)
+      if (wi[j] > wi[j + 1]) {
+        int ti = wi[j]; wi[j] = wi[j + 1]; wi[j + 1] = ti;
+        float tv = wv[j]; wv[j] = wv[j + 1]; wv[j + 1] = tv;
+      }
+  float mx = wv[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) mx = fmaxf(mx, wv[j]);
+  float ex[8], sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { ex[j] = __expf(wv[j] - mx); sum += ex[j]; }
+  if (lane < kTopK) {
+    int myi = wi[0];
+    float myw = ex[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j)
+      if (lane == j) { myi = wi[j]; myw = ex[j]; }
+    ids[lane] = myi;
+    w[lane] = myw / sum;
+  }
 }
 
 struct RouterSharedArgs {
@@ -62,198 +175,216 @@ struct RouterSharedArgs {
   int* err;
 };
 
+// Blocks [0, router_blocks): one router row per warp, then the last block to finish selects
+// the top 8.  Blocks after: one shared-expert feature (gate and up rows) per warp.  Weight
+// rows are requested before waiting on the previous kernel (they do not depend on it).
 __global__ void __launch_bounds__(kWarps * 32) dec_router_shared_kernel(RouterSharedArgs a) {
   extern __shared__ uint4 xs[];
   __shared__ int s_last;
   __shared__ int s_ids[kTopK];
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.D.d, nch = d / 8;
+  const bool router = (int)blockIdx.x < a.router_blocks;
+  const int c = ((int)blockIdx.x - a.router_blocks) * kWarps + warp;  // shared feature
+  RowFrag r0, r1;
+  if (router) {
+    row_load(r0, a.W.w_r + (size_t)(blockIdx.x * kWarps + warp) * d, nch, lane, 0);
+  } else if (c < a.D.fs) {
+    row_load(r0, a.W.ws_gate + (size_t)c * d, nch, lane, 0);
+    row_load(r1, a.W.ws_up + (size_t)c * d, nch, lane, 0);
+  }
+  pdl_wait();  // x may be written by the previous kernel
+  pdl_trigger();
   stage_x(a.x, xs, d);
 
-  if ((int)blockIdx.x >= a.router_blocks) {
-    // shared expert: h_s[c] = silu(gate_c . x) * (up_c . x), one feature per warp
-    const int c = ((int)blockIdx.x - a.router_blocks) * kWarps + warp;
+  if (!router) {
+    // shared expert: h_s[c] = silu(gate_c . x) * (up_c . x)
     if (c < a.D.fs) {
-      const float g = warp_sum(row_dot_partial(a.W.ws_gate + (size_t)c * d, xs, nch, lane));
-      const float u = warp_sum(row_dot_partial(a.W.ws_up + (size_t)c * d, xs, nch, lane));
+      const float g = warp_sum(row_dot_rest(r0, a.W.ws_gate + (size_t)c * d, xs, nch, lane));
+      const float u = warp_sum(row_dot_rest(r1, a.W.ws_up + (size_t)c * d, xs, nch, lane));
       if (lane == 0) a.dw.hdec[(size_t)8 * a.D.hdim + c] = silu_mul(g, u);
     }
-    pdl_trigger();
     return;
   }
 
-  // router rows: logits[e] = w_r[e] . x (+ bias[e])
-  for (int e = blockIdx.x * kWarps + warp; e < kE; e += a.router_blocks * kWarps) {
-    float l = warp_sum(row_dot_partial(a.W.w_r + (size_t)e * d, xs, nch, lane));
-    if (lane == 0) a.dw.logits[e] = l + (a.W.bias ? a.W.bias[e] : 0.f);
-  }
+  // router rows: logits[e] = w_r[e] . x (+ bias[e]); router_blocks * kWarps == E
+  const int e = blockIdx.x * kWarps + warp;
+  const float l = warp_sum(row_dot_rest(r0, a.W.w_r + (size_t)e * d, xs, nch, lane));
+  if (lane == 0) a.dw.logits[e] = l + (a.W.bias ? a.W.bias[e] : 0.f);
+  if (!a.topk_idx) return;  // the forward path selects in the next two kernels
+  // routing outputs requested: the last router block to finish selects the top 8
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     s_last = atomicAdd(a.dw.counter, 1) == a.router_blocks - 1;
   }
   __syncthreads();
-  if (!s_last) {
-    pdl_trigger();
-    return;
-  }
-  // last router block: top-8 of the 256 logits by 8 rounds of warp arg-max (ties: lower id)
+  if (!s_last) return;
   __threadfence();
+  __shared__ float s_w[kTopK];
   if (warp == 0) {
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __ldcg(a.dw.logits + lane + 32 * i);
-    uint32_t taken = 0;
-    float wv[8];
-    int wi[8];
-#pragma unroll
-    for (int r = 0; r < kTopK; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int id = lane + 32 * i;
-        if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && id < bi))) { bv = v[i]; bi = id; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      wv[r] = bv;
-      wi[r] = bi;
-    }
-    // ascending expert id, then softmax over the kept logits
-#pragma unroll
-    for (int i = 0; i < 7; ++i)
-#pragma unroll
-      for (int j = 0; j < 7 - i; ++j)
-        if (wi[j] > wi[j + 1]) {
-          int ti = wi[j]; wi[j] = wi[j + 1]; wi[j + 1] = ti;
-          float tv = wv[j]; wv[j] = wv[j + 1]; wv[j + 1] = tv;
-        }
-    float mx = wv[0];
-#pragma unroll
-    for (int j = 1; j < 8; ++j) mx = fmaxf(mx, wv[j]);
-    float ex[8], s = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) { ex[j] = __expf(wv[j] - mx); s += ex[j]; }
+    select_top8(a.dw.logits, lane, s_ids, s_w);
+    __syncwarp();
     if (lane < kTopK) {
-      int myi = wi[0];
-      float myw = ex[0];
-#pragma unroll
-      for (int j = 1; j < 8; ++j)
-        if (lane == j) { myi = wi[j]; myw = ex[j]; }
-      a.topk_idx[lane] = myi;
-      a.topk_w[lane] = myw / s;
-      s_ids[lane] = myi;
+      a.topk_idx[lane] = s_ids[lane];
+      a.topk_w[lane] = s_w[lane];
       if (a.perm) a.perm[lane] = lane;  // one token: slot j holds assignment (0, j)
     }
     if (lane == 0) *a.dw.counter = 0;  // ready for the next launch on the stream
   }
   __syncthreads();
   if (a.offsets) {
-    for (int e = threadIdx.x; e <= kE; e += blockDim.x) {
+    for (int e2 = threadIdx.x; e2 <= kE; e2 += blockDim.x) {
       int n = 0;
 #pragma unroll
-      for (int j = 0; j < kTopK; ++j) n += s_ids[j] < e;
-      a.offsets[e] = n;
+      for (int j = 0; j < kTopK; ++j) n += s_ids[j] < e2;
+      a.offsets[e2] = n;
     }
   }
-  pdl_trigger();
 }
 
 struct GateUpArgs {
   const __nv_bfloat16* x;
   DecodeWeights W;
   Dims D;
-  const int32_t* topk_idx;
+  int32_t* topk_idx;  // written by block 0 (the selection behind this forward)
+  float* topk_w;
   DecodeWs dw;
 };
 
-// One warp per (selected expert j, feature c): h[j][c] = silu(gate . x) * (up . x).
-__global__ void __launch_bounds__(kWarps * 32) dec_gateup_kernel(GateUpArgs a) {
+// Items (selected expert j, feature c), one warp per item in a grid-stride loop over a grid
+// that is fully resident: h[j][c] = silu(gate . x) * (up . x).  Warp 0 of every block
+// selects the top 8 from the router logits first.
+__global__ void __launch_bounds__(kWarps * 32, 2) dec_gateup_kernel(GateUpArgs a) {
   extern __shared__ uint4 xs[];
-  pdl_wait();
+  __shared__ int s_ids[kTopK];
+  __shared__ float s_w[kTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.D.d, f = a.D.f, nch = d / 8;
-  stage_x(a.x, xs, d);
-  const int gw = blockIdx.x * kWarps + warp;
-  const int j = gw / f, c = gw % f;
-  if (j < kTopK) {
-    const size_t row = ((size_t)a.topk_idx[j] * f + c) * d;
-    const float g = warp_sum(row_dot_partial(a.W.w_gate + row, xs, nch, lane));
-    const float u = warp_sum(row_dot_partial(a.W.w_up + row, xs, nch, lane));
+  pdl_wait();     // the router logits come from the previous kernel
+  pdl_trigger();  // the down kernel may start selecting and streaming its rows now
+  if (warp == 0) select_top8(a.dw.logits, lane, s_ids, s_w);
+  const uint4* src = reinterpret_cast<const uint4*>(a.x);
+  for (int i = threadIdx.x; i < nch; i += blockDim.x) xs[i] = src[i];
+  __syncthreads();
+  if (blockIdx.x == 0 && threadIdx.x < kTopK) {
+    a.topk_idx[threadIdx.x] = s_ids[threadIdx.x];
+    a.topk_w[threadIdx.x] = s_w[threadIdx.x];
+  }
+  const int nwarps = gridDim.x * kWarps;
+  for (int it = blockIdx.x * kWarps + warp; it < kTopK * f; it += nwarps) {
+    const int j = it / f, c = it % f;
+    const size_t row = ((size_t)s_ids[j] * f + c) * d;
+    const __nv_bfloat16* gr = a.W.w_gate + row;
+    const __nv_bfloat16* ur = a.W.w_up + row;
+    RowFrag rg, ru;
+    row_load(rg, gr, nch, lane, 0);
+    row_load(ru, ur, nch, lane, 0);
+    const float g = warp_sum(row_dot_rest(rg, gr, xs, nch, lane));
+    const float u = warp_sum(row_dot_rest(ru, ur, xs, nch, lane));
     if (lane == 0) a.dw.hdec[(size_t)j * a.D.hdim + c] = silu_mul(g, u);
   }
-  pdl_trigger();
 }
 
 struct DownArgs {
   DecodeWeights W;
   Dims D;
-  const int32_t* topk_idx;
-  const float* topk_w;
   DecodeWs dw;
   __nv_bfloat16* y;
 };
 
-// One warp per output n: o_j = down_{e_j}[n] . h_j for the 8 experts and the shared expert;
-// y[n] = bf16(sum_j w_j o_j (ascending expert id) + o_shared), accumulated in fp32.
-__global__ void __launch_bounds__(kWarps * 32) dec_down_combine_kernel(DownArgs a) {
+constexpr int kPreDown = 2;  // 16-byte chunks per lane held per down row (f <= 512 fully)
+
+// One warp per output n (grid-stride over a fully resident grid): o_j = down_{e_j}[n] . h_j
+// for the 8 experts and the shared expert; y[n] = bf16(sum_j w_j o_j (ascending expert id) +
+// o_shared), accumulated in fp32.  The top 8 is selected again from the router logits (final:
+// the router kernel completed before the gate/up kernel let this one start), so the down rows
+// of the first output are requested before waiting for the gate/up kernel's h.
+__global__ void __launch_bounds__(kWarps * 32, 2) dec_down_combine_kernel(DownArgs a) {
   extern __shared__ float hs[];  // [9][hdim]
-  pdl_wait();
+  __shared__ int s_ids[kTopK];
+  __shared__ float s_w[kTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.D.d, f = a.D.f, fs = a.D.fs, hdim = a.D.hdim;
-  for (int i = threadIdx.x; i < 9 * hdim; i += blockDim.x) hs[i] = a.dw.hdec[i];
+  if (warp == 0) select_top8(a.dw.logits, lane, s_ids, s_w);
   __syncthreads();
-  const int n = blockIdx.x * kWarps + warp;
-  if (n < d) {
-    float p[9];
+  const int nwarps = gridDim.x * kWarps;
+  int n = blockIdx.x * kWarps + warp;
+  uint4 pre[9][kPreDown];
+  auto row_of = [&](int j, int nn) {
+    return j < 8 ? a.W.w_down + ((size_t)s_ids[j] * d + nn) * f : a.W.ws_down + (size_t)nn * fs;
+  };
+  auto prefetch = [&](int nn) {
 #pragma unroll
     for (int j = 0; j < 9; ++j) {
-      const int len = j < 8 ? f : fs;
-      const __nv_bfloat16* row = j < 8 ? a.W.w_down + ((size_t)a.topk_idx[j] * d + n) * f
-                                       : a.W.ws_down + (size_t)n * fs;
-      const float* hj = hs + (size_t)j * hdim;
-      float acc = 0.f;
-#pragma unroll 2
-      for (int c = lane; c < len / 8; c += 32) {
-        const uint4 w = ld_stream_u4(row + (size_t)c * 8);
-        const float4 h0 = *reinterpret_cast<const float4*>(hj + c * 8);
-        const float4 h1 = *reinterpret_cast<const float4*>(hj + c * 8 + 4);
-        acc = fmaf(bf16_lo(w.x), h0.x, acc);
-        acc = fmaf(bf16_hi(w.x), h0.y, acc);
-        acc = fmaf(bf16_lo(w.y), h0.z, acc);
-        acc = fmaf(bf16_hi(w.y), h0.w, acc);
-        acc = fmaf(bf16_lo(w.z), h1.x, acc);
-        acc = fmaf(bf16_hi(w.z), h1.y, acc);
-        acc = fmaf(bf16_lo(w.w), h1.z, acc);
-        acc = fmaf(bf16_hi(w.w), h1.w, acc);
+      const __nv_bfloat16* row = row_of(j, nn);
+      const int nc = (j < 8 ? f : fs) / 8;
+#pragma unroll
+      for (int i = 0; i < kPreDown; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nc) pre[j][i] = ld_stream_u4(row + (size_t)c * 8);
       }
-      p[j] = acc;
     }
+  };
+  if (n < d) prefetch(n);
+  pdl_wait();  // h comes from the gate/up kernel
+  pdl_trigger();
+  {
+    const float4* src = reinterpret_cast<const float4*>(a.dw.hdec);
+    float4* dst = reinterpret_cast<float4*>(hs);
+#pragma unroll 4
+    for (int i = threadIdx.x; i < 9 * hdim / 4; i += blockDim.x) dst[i] = __ldcg(src + i);
+  }
+  __syncthreads();
+  for (; n < d; n += nwarps) {
     float y = 0.f;
 #pragma unroll
     for (int j = 0; j < 9; ++j) {
-      const float o = warp_sum(p[j]);
-      y += (j < 8 ? a.topk_w[j] : 1.0f) * o;
+      const int nc = (j < 8 ? f : fs) / 8;
+      const float* hj = hs + (size_t)j * hdim;
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPreDown; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nc) acc += dot8_f32(pre[j][i], hj + c * 8);
+      }
+      const __nv_bfloat16* row = row_of(j, n);
+      for (int c = lane + 32 * kPreDown; c < nc; c += 32)
+        acc += dot8_f32(ld_stream_u4(row + (size_t)c * 8), hj + c * 8);
+      y += (j < 8 ? s_w[j] : 1.0f) * warp_sum(acc);
     }
     if (lane == 0) a.y[n] = __float2bfloat16_rn(y);
+    if (n + nwarps < d) prefetch(n + nwarps);
   }
-  pdl_trigger();
 }
 
 }  // namespace
 
+namespace {
+int g_gateup_grid = 0, g_down_grid = 0;  // blocks that are resident at once (all SMs)
+}
+
 cudaError_t prepare_decode_kernels(int hdim) {
   const int need = 9 * hdim * (int)sizeof(float);
-  if (need <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(dec_down_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              need);
+  cudaError_t e = cudaSuccess;
+  if (need > 48 * 1024) {
+    e = cudaFuncSetAttribute(dec_down_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             need);
+    if (e != cudaSuccess) return e;
+  }
+  int dev = 0, sms = 0, b1 = 0, b2 = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, dec_gateup_kernel, kWarps * 32,
+                                                         8192 * 2)) != cudaSuccess)
+    return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, dec_down_combine_kernel,
+                                                         kWarps * 32, need)) != cudaSuccess)
+    return e;
+  g_gateup_grid = sms * (b1 > 0 ? b1 : 1);
+  g_down_grid = sms * (b2 > 0 ? b2 : 1);
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode_router_shared(const __nv_bfloat16* x, const DecodeWeights& W,
@@ -267,18 +398,19 @@ cudaError_t launch_decode_router_shared(const __nv_bfloat16* x, const DecodeWeig
 }
 
 cudaError_t launch_decode_gateup(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
-                                 const int32_t* topk_idx, const DecodeWs& dw, cudaStream_t s) {
-  GateUpArgs a{x, W, D, topk_idx, dw};
-  return launch_pdl(dec_gateup_kernel, dim3(kTopK * D.f / kWarps), dim3(kWarps * 32),
-                    (size_t)D.d * 2, s, a);
+                                 int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
+                                 cudaStream_t s) {
+  GateUpArgs a{x, W, D, topk_idx, topk_w, dw};
+  const int grid = std::min(g_gateup_grid, kTopK * D.f / kWarps);
+  return launch_pdl(dec_gateup_kernel, dim3(grid), dim3(kWarps * 32), (size_t)D.d * 2, s, a);
 }
 
-cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D,
-                                       const int32_t* topk_idx, const float* topk_w,
-                                       const DecodeWs& dw, __nv_bfloat16* y, cudaStream_t s) {
-  DownArgs a{W, D, topk_idx, topk_w, dw, y};
-  return launch_pdl(dec_down_combine_kernel, dim3((D.d + kWarps - 1) / kWarps),
-                    dim3(kWarps * 32), (size_t)9 * D.hdim * sizeof(float), s, a);
+cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D, const DecodeWs& dw,
+                                       __nv_bfloat16* y, cudaStream_t s) {
+  DownArgs a{W, D, dw, y};
+  const int grid = std::min(g_down_grid, (D.d + kWarps - 1) / kWarps);
+  return launch_pdl(dec_down_combine_kernel, dim3(grid), dim3(kWarps * 32),
+                    (size_t)9 * D.hdim * sizeof(float), s, a);
 }
 
 }  // namespace moe

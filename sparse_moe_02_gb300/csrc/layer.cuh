@@ -112,19 +112,21 @@ struct DecodeWeights {
   const float* bias;
 };
 
-// Router GEMV + top-8 (last block) and the shared expert's gate/up GEMV, one launch.
+// Router GEMV (logits) and the shared expert's gate/up GEMV, one launch.  When topk_idx is
+// not NULL (routing requested) the last router block to finish also writes the top 8.
 cudaError_t launch_decode_router_shared(const __nv_bfloat16* x, const DecodeWeights& W,
                                         const Dims& D, int32_t* topk_idx, float* topk_w,
                                         int32_t* offsets, int32_t* perm, const DecodeWs& dw,
                                         int* err, cudaStream_t s, bool with_shared);
 
-// Gate/up GEMV of the 8 selected experts with the SwiGLU fused.
+// Top-8 selection from the logits and the gate/up GEMV of the 8 selected experts with the
+// SwiGLU fused; block 0 writes the selection to topk_idx / topk_w.
 cudaError_t launch_decode_gateup(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
-                                 const int32_t* topk_idx, const DecodeWs& dw, cudaStream_t s);
+                                 int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
+                                 cudaStream_t s);
 
 // Down GEMV of the 8 experts and the shared expert, weighted and combined in fixed order.
-cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D,
-                                       const int32_t* topk_idx, const float* topk_w,
-                                       const DecodeWs& dw, __nv_bfloat16* y, cudaStream_t s);
+cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D, const DecodeWs& dw,
+                                       __nv_bfloat16* y, cudaStream_t s);
 
 }  // namespace moe
