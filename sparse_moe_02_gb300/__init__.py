@@ -29,7 +29,7 @@ MOE_SCHEDULE_GEMV = 2
 
 EXPORTS = ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_get_device_error",
            "moe_destroy", "moe_status_string", "moe_last_cuda_error", "moe_profile_begin",
-           "moe_profile_end")
+           "moe_profile_end", "moe_route_one_noalloc")
 
 # kernel order reported by moe_profile_end
 KERNELS_GEMM = ("router_topk", "route_plan", "route_scatter", "gateup", "down", "combine")
@@ -73,9 +73,11 @@ def lib():
         L.moe_profile_begin.argtypes = [_c_void_p, _c_int]
         L.moe_profile_end.argtypes = [_c_void_p, ctypes.POINTER(ctypes.c_float), _c_int,
                                       ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]
+        L.moe_route_one_noalloc.argtypes = [_c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
+                                            _c_void_p, _c_void_p]
         for fn in ("moe_create", "moe_route", "moe_forward", "moe_forward_host",
                    "moe_get_device_error", "moe_destroy", "moe_last_cuda_error",
-                   "moe_profile_begin", "moe_profile_end"):
+                   "moe_profile_begin", "moe_profile_end", "moe_route_one_noalloc"):
             getattr(L, fn).restype = _c_int
         _lib = L
     return _lib
@@ -114,6 +116,11 @@ def moe_status_string(status):
 
 def moe_last_cuda_error():
     return lib().moe_last_cuda_error()
+
+
+def moe_route_one_noalloc(x, d, w_router, router_bias, topk_idx, topk_w, stream):
+    """Routing of one token with no device allocation (see include/moe.h)."""
+    return lib().moe_route_one_noalloc(x, d, w_router, router_bias, topk_idx, topk_w, stream)
 
 
 def moe_profile_begin(h, n_calls):
