@@ -330,13 +330,24 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_down_combine_kernel(DownAr
   pdl_wait();  // h comes from the gate/up kernel
   pdl_trigger();
   {
+    // all loads of a batch are in flight before the first store (one L2 round trip per batch)
     const float4* src = reinterpret_cast<const float4*>(a.dw.hdec);
     float4* dst = reinterpret_cast<float4*>(hs);
-#pragma unroll 4
-    for (int i = threadIdx.x; i < 9 * hdim / 4; i += blockDim.x) dst[i] = __ldcg(src + i);
+    const int n4 = 9 * hdim / 4;
+    for (int base = threadIdx.x; base < n4; base += 8 * blockDim.x) {
+      float4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (base + i * (int)blockDim.x < n4) v[i] = __ldcg(src + base + i * blockDim.x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (base + i * (int)blockDim.x < n4) dst[base + i * blockDim.x] = v[i];
+    }
   }
   __syncthreads();
   for (; n < d; n += nwarps) {
+    // per lane: sum over j (ascending expert id, then shared) of w_j * (its chunks of
+    // down_j[n] . h_j); one warp reduction of those partials gives y[n] (fixed order)
     float y = 0.f;
 #pragma unroll
     for (int j = 0; j < 9; ++j) {
@@ -351,8 +362,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_down_combine_kernel(DownAr
       const __nv_bfloat16* row = row_of(j, n);
       for (int c = lane + 32 * kPreDown; c < nc; c += 32)
         acc += dot8_f32(ld_stream_u4(row + (size_t)c * 8), hj + c * 8);
-      y += (j < 8 ? s_w[j] : 1.0f) * warp_sum(acc);
+      y = fmaf(j < 8 ? s_w[j] : 1.0f, acc, y);
     }
+    y = warp_sum(y);
     if (lane == 0) a.y[n] = __float2bfloat16_rn(y);
     if (n + nwarps < d) prefetch(n + nwarps);
   }
