@@ -35,7 +35,7 @@ METRIC = "MoE-layer prefill tokens/s @T=4096 & decode us/layer (T=1); % of roofl
 T_PREFILL, D, F, FS, E, K = 4096, 2048, 512, 512, 256, 8
 DECODE_LAYERS = 40
 FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
-KERNELS_GEMM = ("router_topk", "route_plan", "route_scatter", "gateup", "down", "combine")
+KERNELS_GEMM = ("router_topk", "route_plan", "route_scatter", "experts", "combine")
 KERNELS_GEMV = ("decode_router_shared", "decode_gateup", "decode_down_combine")
 
 
@@ -81,17 +81,15 @@ def algorithmic(counts, T):
     S = T * K
     b = dict(
         router_topk=E * D * 2 + T * D * 2,
-        gateup=ne * 2 * F * D * 2 + 2 * FS * D * 2 + T * D * 2,
-        down=ne * D * F * 2 + D * FS * 2,
+        experts=ne * 3 * F * D * 2 + 3 * FS * D * 2 + T * D * 2,  # weights + x
         combine=T * D * 2,
     )
     fl = dict(
         router_topk=2 * T * E * D,
-        gateup=2 * (S * 2 * F + T * 2 * FS) * D,
-        down=2 * (S * F + T * FS) * D,
+        experts=2 * (S * 3 * F + T * 3 * FS) * D,
     )
     layer_bytes = E * D * 2 + ne * 3 * F * D * 2 + 3 * FS * D * 2 + 2 * T * D * 2
-    layer_flops = sum(fl.values())
+    layer_flops = fl["router_topk"] + fl["experts"]
     return b, fl, layer_bytes, layer_flops
 
 
@@ -396,7 +394,7 @@ def profiled_traffic(kernel):
     if not os.path.exists(path):
         return None
     src = {"router_topk": "route.cu", "route_plan": "route.cu", "route_scatter": "route.cu",
-           "gateup": "experts.cu", "down": "experts.cu", "combine": "experts.cu"}.get(kernel)
+           "experts": "experts.cu", "combine": "experts.cu"}.get(kernel)
     if not src:
         return None
     sha = hashlib.sha1(open(os.path.join(ROOT, "sparse_moe_02_gb300", "csrc", src), "rb")

@@ -64,7 +64,7 @@ struct moe_handle_s {
   moe_weights w;
   Dims D;
   int device = 0, sms = 0;
-  int P_max = 0, max_units_gu = 0, max_units_dn = 0;
+  int P_max = 0, max_units_gu = 0, max_units_dn = 0, max_chunks = 0;
   void* ws = nullptr;
   size_t ws_bytes = 0;
   moe::RouteWs rws{};
@@ -139,6 +139,8 @@ void layout(moe_handle_s* h, char* base, size_t* total) {
   h->rws.units_gu = c.take<moe::Unit>((size_t)h->max_units_gu);
   h->rws.units_dn = c.take<moe::Unit>((size_t)h->max_units_dn);
   h->rws.n_units = c.take<int32_t>(2);
+  h->rws.next_unit = c.take<int32_t>(1);
+  h->rws.chunk_done = c.take<int32_t>((size_t)h->max_chunks);
   h->rws.err = c.take<int>(1);
   h->dws.logits = c.take<float>(kE);
   h->dws.counter = c.take<int>(1);
@@ -248,6 +250,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
   h->max_units_gu = chunks_routed * (cfg->ffn_dim / moe::kMTile) +
                     chunks_shared * (cfg->shared_ffn_dim / moe::kMTile);
   h->max_units_dn = (chunks_routed + chunks_shared) * (cfg->d / moe::kMTile);
+  h->max_chunks = chunks_routed + chunks_shared;
 
   size_t total = 0;
   layout(h, nullptr, &total);
@@ -329,17 +332,14 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
                            true)))
     return st;
   if ((st = prof_mark(h, s, 3))) return st;
-  if ((st = cuda_status(moe::launch_gateup(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu, h->D,
-                                           h->rws, h->h, h->sms, s))))
+  if ((st = cuda_status(moe::launch_experts(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu,
+                                            h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->h,
+                                            h->ys, h->sms, s))))
     return st;
   if ((st = prof_mark(h, s, 4))) return st;
-  if ((st = cuda_status(
-           moe::launch_down(h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->ys, h->sms, s))))
-    return st;
-  if ((st = prof_mark(h, s, 5))) return st;
   if ((st = cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, s))))
     return st;
-  return prof_finish_call(h, s, 6);
+  return prof_finish_call(h, s, 5);
 }
 
 int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void* stream) {

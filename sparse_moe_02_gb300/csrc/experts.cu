@@ -22,51 +22,88 @@ namespace {
 constexpr int kTileA = kMTile * kBK * 2;     // 128 weight rows x 64 (16 KB)
 constexpr int kTileB = kChunkRows * kBK * 2; // up to 256 token rows x 64 (32 KB)
 
-// ---------------------------------------------------------------- gate/up + SwiGLU
+// ---------------------------------------------------------------- gate/up + down, one launch
 
-constexpr int kGuStages = 3;
-constexpr int kGuStage = 2 * kTileA + kTileB;  // gate tile | up tile | token rows
-constexpr int kGuSmem = kGuStages * kGuStage + 1024 + 1024;
-constexpr int kGuThreads = 384;                // 12 warps, roles below
-constexpr int kGuRowThreads = 64;              // warps 2-3: token-row copies
-constexpr int kGuEpiWarps = 8;                 // warps 4-11: two per TMEM lane quadrant
+constexpr int kXStages = 3;
+constexpr int kXStage = 2 * kTileA + kTileB;  // weight tile(s) | token rows
+constexpr int kXSmem = kXStages * kXStage + 1024 + 1024;
+constexpr int kXThreads = 384;                 // 12 warps, roles below
+constexpr int kXRowThreads = 64;               // warps 2-3: token-row copies (gate/up units)
+constexpr int kXEpiWarps = 8;                  // warps 4-11: two per TMEM lane quadrant
+constexpr int kXQueue = 4;                     // unit indices handed out ahead
+constexpr int kXQueueReaders = 2 + 1 + kXEpiWarps;  // row-producer warps, MMA, epilogue warps
 
-struct GuArgs {
-  const Unit* units;
-  const int32_t* n_units;
+struct XArgs {
+  const Unit* units_gu;
+  const Unit* units_dn;
+  const int32_t* n_units;  // [2]: gate/up, down
+  int32_t* next_unit;      // dynamic schedule: next unit index to hand out (zeroed by the plan)
+  int32_t* chunk_done;
   const int32_t* grow;
   const __nv_bfloat16* x;
   __nv_bfloat16* h;
-  int d, f, hdim;
+  __nv_bfloat16* ys;
+  int d, f, fs, hdim;
   int* err;
 };
 
-// Warp roles: 0 = TMA producer of the gate and up weight tiles; 1 = MMA issuer (and TMEM
-// owner); 2-3 = producers of the token rows (gathered from x by 16-byte cp.async straight
-// into the 128-byte-swizzled layout: row r, chunk c lands at r*128 + ((c ^ (r & 7)) * 16));
-// 4-11 = epilogue, two warps per TMEM lane quadrant, each taking alternate 16-column chunks.
-__global__ void __launch_bounds__(kGuThreads, 1)
-    gateup_kernel(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
-                  const __grid_constant__ CUtensorMap tm_wsg,
-                  const __grid_constant__ CUtensorMap tm_wsu, GuArgs a) {
+struct XUnit {
+  Unit u;
+  bool down;
+};
+
+__device__ __forceinline__ XUnit unit_at(const XArgs& a, int i, int n_gu) {
+  XUnit r;
+  r.down = i >= n_gu;
+  r.u = r.down ? a.units_dn[i - n_gu] : a.units_gu[i];
+  return r;
+}
+
+// One persistent block per SM walks a combined list: every gate/up unit, then every down unit,
+// handed out in list order by an atomic counter (the TMA producer lane takes the next index and
+// passes it to the other roles through a small shared-memory queue).  Gate/up unit: 128 features of one group against up to
+// 256 token rows; gate and up accumulators fill TMEM columns [0, N) and [256, 256 + N) (both
+// halves); epilogue h = silu(gate) * up -> bf16, then the unit's chunk counter is incremented.
+// Down unit: 256 outputs of one group as two 128-row weight tiles sharing the h rows, the two
+// accumulators in the two TMEM halves; its producer waits for the chunk's counter to reach the
+// number of gate/up tiles before loading h rows.
+// Warp roles: 0 = TMA producer (weight tiles; h rows of down units); 1 = MMA issuer (TMEM
+// owner); 2-3 = token-row producers of gate/up units (16-byte cp.async gathers from x into
+// the 128-byte swizzle; for down units they only arrive); 4-11 = epilogue.
+__global__ void __launch_bounds__(kXThreads, 1)
+    experts_kernel(const __grid_constant__ CUtensorMap tm_wg,
+                   const __grid_constant__ CUtensorMap tm_wu,
+                   const __grid_constant__ CUtensorMap tm_wsg,
+                   const __grid_constant__ CUtensorMap tm_wsu,
+                   const __grid_constant__ CUtensorMap tm_h,
+                   const __grid_constant__ CUtensorMap tm_wd,
+                   const __grid_constant__ CUtensorMap tm_wsd, XArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGuStages * kGuStage);
-  uint64_t* empty = full + kGuStages;
-  uint64_t* tfull = empty + kGuStages;
-  uint64_t* tempty = tfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kXStages * kXStage);
+  uint64_t* empty = full + kXStages;
+  uint64_t* tfull = empty + kXStages;  // [2] TMEM halves
+  uint64_t* tempty = tfull + 2;        // [2]
+  uint64_t* qfull = tempty + 2;        // [kXQueue] unit-index queue
+  uint64_t* qempty = qfull + kXQueue;  // [kXQueue]
+  int* qidx = reinterpret_cast<int*>(qempty + kXQueue);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qidx + kXQueue);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KB = a.d / kBK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGuStages; ++s) {
-      mbar_init(&full[s], 1 + kGuRowThreads);  // weight TMA + one arrival per row thread
+    for (int s = 0; s < kXStages; ++s) {
+      mbar_init(&full[s], 1 + kXRowThreads);  // TMA producer + one arrival per row thread
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, kGuEpiWarps);
+    for (int i = 0; i < kXQueue; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], kXQueueReaders);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], kXEpiWarps);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -78,69 +115,162 @@ __global__ void __launch_bounds__(kGuThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
-  const int n_units = *a.n_units;
+  const int n_gu = a.n_units[0];
+  const int n_all = n_gu + a.n_units[1];
+  // reader side of the unit queue: the k-th unit this block processes (-1: no more units);
+  // one arrival per reading warp releases the slot
+  auto next_unit = [&](int k, bool& ok) {
+    const int q = k % kXQueue;
+    const bool w = mbar_wait(&qfull[q], (k / kXQueue) & 1, a.err);
+    ok = __all_sync(0xffffffffu, w);
+    const int i = ok ? *reinterpret_cast<volatile int*>(&qidx[q]) : -1;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qempty[q]);
+    return i;
+  };
+  // the same for a role that runs on a single lane (the MMA issuer)
+  auto next_unit_1 = [&](int k, bool& ok) {
+    const int q = k % kXQueue;
+    ok = mbar_wait(&qfull[q], (k / kXQueue) & 1, a.err);
+    const int i = ok ? *reinterpret_cast<volatile int*>(&qidx[q]) : -1;
+    mbar_arrive(&qempty[q]);
+    return i;
+  };
 
   if (warp == 0) {
-    // ---- weight tiles (gate and up, 128 rows x 64 each) by tiled TMA
+    // ---- TMA producer
     if (lane == 0) {
       prefetch_tensormap(&tm_wg);
       prefetch_tensormap(&tm_wu);
       prefetch_tensormap(&tm_wsg);
       prefetch_tensormap(&tm_wsu);
+      prefetch_tensormap(&tm_h);
+      prefetch_tensormap(&tm_wd);
+      prefetch_tensormap(&tm_wsd);
       const uint64_t stream_w = policy_evict_first();  // each weight tile is read once
+      const uint64_t keep_h = policy_evict_last();
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit U = a.units[u];
+      // queue writer: index k goes to slot k % kXQueue once its previous use is read by all
+      int kq = 0;
+      auto push = [&](int i) {
+        const int q = kq % kXQueue;
+        if (kq >= kXQueue && !mbar_wait(&qempty[q], ((kq / kXQueue) - 1) & 1, a.err)) return false;
+        qidx[q] = i;
+        mbar_arrive(&qfull[q]);
+        ++kq;
+        return true;
+      };
+      int cur = atomicAdd(a.next_unit, 1);
+      if (!push(cur < n_all ? cur : -1)) ok = false;
+      while (ok && cur < n_all) {
+        const int nxt = atomicAdd(a.next_unit, 1);  // hand out the next unit ahead
+        const int i = cur;
+        cur = nxt;
+        const XUnit X = unit_at(a, i, n_gu);
+        const Unit& U = X.u;
         const bool shared = U.g == kE;
-        const CUtensorMap* mg = shared ? &tm_wsg : &tm_wg;
-        const CUtensorMap* mu = shared ? &tm_wsu : &tm_wu;
-        const int arow = (shared ? 0 : U.g * a.f) + U.mt * kMTile;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
-          uint8_t* st = smem + stage * kGuStage;
-          mbar_arrive_expect_tx(&full[stage], 2 * kTileA);
-          tma_load_2d(st, mg, &full[stage], kb * kBK, arow, stream_w);
-          tma_load_2d(st + kTileA, mu, &full[stage], kb * kBK, arow, stream_w);
-          if (++stage == kGuStages) { stage = 0; ph ^= 1; }
+        const int N = round_up(U.nrows, kRowAlign);
+        if (!push(nxt < n_all ? nxt : -1)) { ok = false; break; }
+        if (!X.down) {
+          const CUtensorMap* mg = shared ? &tm_wsg : &tm_wg;
+          const CUtensorMap* mu = shared ? &tm_wsu : &tm_wu;
+          const int arow = (shared ? 0 : U.g * a.f) + U.mt * kMTile;
+          for (int kb = 0; kb < a.d / kBK; ++kb) {
+            if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
+            uint8_t* st = smem + stage * kXStage;
+            mbar_arrive_expect_tx(&full[stage], 2 * kTileA);
+            tma_load_2d(st, mg, &full[stage], kb * kBK, arow, stream_w);
+            tma_load_2d(st + kTileA, mu, &full[stage], kb * kBK, arow, stream_w);
+            if (++stage == kXStages) { stage = 0; ph ^= 1; }
+          }
+        } else {
+          // the chunk's h rows are complete once all its gate/up tiles have published
+          const int need = (shared ? a.fs : a.f) / kMTile;
+          const uint64_t t0 = global_timer_ns();
+          while (true) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];"
+                         : "=r"(v)
+                         : "l"(a.chunk_done + U.cid)
+                         : "memory");
+            if (v >= need) break;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+              atomicExch(a.err, kDevErrTimeout);
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // h read by TMA next
+          // two 128-row tiles of the down weights (outputs mt*256 .. +255) share the h rows
+          const int K = shared ? a.fs : a.f;
+          const CUtensorMap* mw = shared ? &tm_wsd : &tm_wd;
+          const int arow = (shared ? 0 : U.g * a.d) + U.mt * 2 * kMTile;
+          const bool two = (U.mt * 2 + 1) * kMTile < a.d;
+          const uint32_t bytes = (two ? 2 : 1) * kTileA + (uint32_t)N * kBK * 2;
+          for (int kb = 0; kb < K / kBK; ++kb) {
+            if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
+            uint8_t* st = smem + stage * kXStage;
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            tma_load_2d(st, mw, &full[stage], kb * kBK, arow, stream_w);
+            if (two) tma_load_2d(st + kTileA, mw, &full[stage], kb * kBK, arow + kMTile, stream_w);
+            for (int r = 0; r < N / 16; ++r)
+              tma_load_2d(st + 2 * kTileA + r * 2048, &tm_h, &full[stage], kb * kBK,
+                          U.p0 + 16 * r, keep_h);
+            if (++stage == kXStages) { stage = 0; ph ^= 1; }
+          }
         }
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: gate accumulator in TMEM columns [0, N), up in [256, 256 + N)
+    // ---- MMA issuer
     if (lane == 0) {
       int stage = 0;
-      uint32_t ph = 0, tph = 0;
+      uint32_t ph = 0, tph[2] = {0, 0};
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit U = a.units[u];
+      for (int k = 0; ok; ++k) {
+        const int i = next_unit_1(k, ok);
+        if (i < 0) break;
+        const XUnit X = unit_at(a, i, n_gu);
+        const Unit& U = X.u;
         const int N = round_up(U.nrows, kRowAlign);
         const uint32_t idesc = idesc_bf16(128, N);
-        if (!mbar_wait(tempty, tph ^ 1, a.err)) break;
+        // both TMEM halves: gate (or down rows +0..127) in [0, N), up (or down rows
+        // +128..255) in [256, 256 + N)
+        const bool two = !X.down || (U.mt * 2 + 1) * kMTile < a.d;
+        const int KB = X.down ? (U.g == kE ? a.fs : a.f) / kBK : a.d / kBK;
+        if (!mbar_wait(&tempty[0], tph[0] ^ 1, a.err) ||
+            !mbar_wait(&tempty[1], tph[1] ^ 1, a.err))
+          break;
         tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&full[stage], ph, a.err)) { ok = false; break; }
-          fence_proxy_async_smem();  // token rows were written by cp.async (generic proxy)
+          fence_proxy_async_smem();  // token rows of gate/up units come from cp.async
           tc_fence_after();
-          const uint32_t sg = smem_u32(smem + stage * kGuStage);
-          const uint32_t su = sg + kTileA, sb = sg + 2 * kTileA;
+          const uint32_t s0 = smem_u32(smem + stage * kXStage);
+          const uint32_t s1 = s0 + kTileA, sb = s0 + 2 * kTileA;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t bd = sdesc_k128(sb + kk * 32);
             const uint32_t acc = (kb | kk) != 0;
-            mma_bf16(tmem, sdesc_k128(sg + kk * 32), bd, idesc, acc);
-            mma_bf16(tmem + 256, sdesc_k128(su + kk * 32), bd, idesc, acc);
+            mma_bf16(tmem, sdesc_k128(s0 + kk * 32), bd, idesc, acc);
+            if (two) mma_bf16(tmem + 256, sdesc_k128(s1 + kk * 32), bd, idesc, acc);
           }
           mma_commit(&empty[stage]);
-          if (++stage == kGuStages) { stage = 0; ph ^= 1; }
+          if (++stage == kXStages) { stage = 0; ph ^= 1; }
         }
-        if (ok) mma_commit(tfull);
-        tph ^= 1;
+        if (!ok) break;
+        mma_commit(&tfull[0]);
+        mma_commit(&tfull[1]);
+        tph[0] ^= 1;
+        tph[1] ^= 1;
       }
     }
   } else if (warp < 4) {
-    // ---- token rows: thread (crow, chunk) copies 16-byte chunk `chunk` of rows crow + 8i
+    // ---- token rows of gate/up units: thread (crow, chunk) copies 16-byte chunk `chunk` of
+    // rows crow + 8i; for down units the thread only arrives, keeping the ring's phases
     const int bt = threadIdx.x - 64;
     const int crow = bt >> 3, chunk = bt & 7;
     const uint32_t swz = (uint32_t)((chunk ^ crow) << 4);  // (r & 7) == crow for every row
@@ -148,202 +278,108 @@ __global__ void __launch_bounds__(kGuThreads, 1)
     int stage = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit U = a.units[u];
+    for (int k = 0; ok; ++k) {
+      const int i = next_unit(k, ok);
+      if (i < 0) break;
+      const XUnit X = unit_at(a, i, n_gu);
+      const Unit& U = X.u;
       const int N = round_up(U.nrows, kRowAlign);
       const int nr = N / 8;  // rows per thread, <= 32
+      const int KB = X.down ? (U.g == kE ? a.fs : a.f) / kBK : a.d / kBK;
       const __nv_bfloat16* src[kChunkRows / 8];
+      if (!X.down) {
 #pragma unroll
-      for (int i = 0; i < kChunkRows / 8; ++i)
-        src[i] = a.x + (size_t)(i < nr ? __ldg(a.grow + U.p0 + crow + 8 * i) : 0) * a.d +
-                 chunk * 8;
+        for (int r = 0; r < kChunkRows / 8; ++r)
+          src[r] = a.x + (size_t)(r < nr ? __ldg(a.grow + U.p0 + crow + 8 * r) : 0) * a.d +
+                   chunk * 8;
+      }
       for (int kb = 0; kb < KB; ++kb) {
         const bool w = mbar_wait(&empty[stage], ph ^ 1, a.err);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        const uint32_t sb = smem_u32(smem + stage * kGuStage + 2 * kTileA) + crow * 128 + swz;
+        if (!X.down) {
+          const uint32_t sb =
+              smem_u32(smem + stage * kXStage + 2 * kTileA) + crow * 128 + swz;
 #pragma unroll
-        for (int i = 0; i < kChunkRows / 8; ++i)
-          if (i < nr) cp_async_16(sb + i * 1024, src[i] + kb * kBK, keep_x);
-        cp_async_arrive_noinc(&full[stage]);
-        if (++stage == kGuStages) { stage = 0; ph ^= 1; }
+          for (int r = 0; r < kChunkRows / 8; ++r)
+            if (r < nr) cp_async_16(sb + r * 1024, src[r] + kb * kBK, keep_x);
+          cp_async_arrive_noinc(&full[stage]);
+        } else {
+          mbar_arrive(&full[stage]);
+        }
+        if (++stage == kXStages) { stage = 0; ph ^= 1; }
       }
     }
   } else {
-    // ---- epilogue: thread = one feature row; h = silu(gate) * up for each token column
+    // ---- epilogue: thread = one weight row of the tile; the two warps of a lane quadrant
+    // take alternate 16-column chunks
     const int q = warp & 3, half = (warp - 4) >> 2;
     const int m = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    uint32_t tph = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit U = a.units[u];
-      const int N = round_up(U.nrows, kRowAlign);
-      const bool w = mbar_wait(tfull, tph, a.err);
-      if (!__all_sync(0xffffffffu, w)) break;
-      tc_fence_after();
-      __nv_bfloat16* hp = a.h + (size_t)U.p0 * a.hdim + U.mt * kMTile + m;
-      for (int j0 = half * 16; j0 < N; j0 += 32) {
-        uint32_t g[16], v[16];
-        tmem_ld16(tmem + lane_off + (uint32_t)j0, g);
-        tmem_ld16(tmem + lane_off + 256u + (uint32_t)j0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          hp[(size_t)(j0 + i) * a.hdim] =
-              __float2bfloat16_rn(silu_mul(__uint_as_float(g[i]), __uint_as_float(v[i])));
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
-      tph ^= 1;
-    }
-  }
-  pdl_trigger();
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 512);
-}
-
-// ---------------------------------------------------------------- down
-
-constexpr int kDnStages = 4;
-constexpr int kDnStage = kTileA + kTileB;
-constexpr int kDnSmem = kDnStages * kDnStage + 1024 + 1024;
-
-struct DnArgs {
-  const Unit* units;
-  const int32_t* n_units;
-  __nv_bfloat16* ys;
-  int d, f, fs;
-  int* err;
-};
-
-__global__ void __launch_bounds__(192, 1)
-    down_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wd,
-                const __grid_constant__ CUtensorMap tm_wsd, DnArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kDnStages * kDnStage);
-  uint64_t* empty = full + kDnStages;
-  uint64_t* tfull = empty + kDnStages;  // [2]
-  uint64_t* tempty = tfull + 2;         // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kDnStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
-    }
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  pdl_wait();
-  const int n_units = *a.n_units;
-
-  if (warp == 0) {
-    // ---- producer: weight tile + 16-row tiles of h
-    if (lane == 0) {
-      prefetch_tensormap(&tm_h);
-      prefetch_tensormap(&tm_wd);
-      prefetch_tensormap(&tm_wsd);
-    }
-    const uint64_t stream_w = policy_evict_first();
-    const uint64_t keep_h = policy_evict_last();
-    int stage = 0;
-    uint32_t ph = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit U = a.units[u];
-      const int N = round_up(U.nrows, kRowAlign);
-      const bool shared = U.g == kE;
-      const int K = shared ? a.fs : a.f;
-      const CUtensorMap* mw = shared ? &tm_wsd : &tm_wd;
-      const int arow = (shared ? 0 : U.g * a.d) + U.mt * kMTile;
-      const uint32_t bytes = kTileA + (uint32_t)N * kBK * 2;
-      for (int kb = 0; kb < K / kBK; ++kb) {
-        const bool w = mbar_wait(&empty[stage], ph ^ 1, a.err);
-        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        uint8_t* st = smem + stage * kDnStage;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d(st, mw, &full[stage], kb * kBK, arow, stream_w);
-        }
-        __syncwarp();
-        if (lane < N / 16)
-          tma_load_2d(st + kTileA + lane * 2048, &tm_h, &full[stage], kb * kBK, U.p0 + 16 * lane,
-                      keep_h);
-        if (++stage == kDnStages) { stage = 0; ph ^= 1; }
-      }
-    }
-  } else if (warp == 1) {
-    // ---- MMA issuer: two accumulator slots of 256 columns, alternating per unit
-    if (lane == 0) {
-      int stage = 0, slot = 0;
-      uint32_t ph = 0, tph[2] = {0, 0};
-      bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit U = a.units[u];
-        const int N = round_up(U.nrows, kRowAlign);
-        const int K = U.g == kE ? a.fs : a.f;
-        const uint32_t idesc = idesc_bf16(128, N);
-        const uint32_t acc_col = tmem + 256u * slot;
-        if (!mbar_wait(&tempty[slot], tph[slot] ^ 1, a.err)) break;
-        tc_fence_after();
-        for (int kb = 0; kb < K / kBK; ++kb) {
-          if (!mbar_wait(&full[stage], ph, a.err)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * kDnStage), sb = sa + kTileA;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16(acc_col, sdesc_k128(sa + kk * 32), sdesc_k128(sb + kk * 32), idesc,
-                     (kb | kk) != 0);
-          mma_commit(&empty[stage]);
-          if (++stage == kDnStages) { stage = 0; ph ^= 1; }
-        }
-        if (ok) mma_commit(&tfull[slot]);
-        tph[slot] ^= 1;
-        slot ^= 1;
-      }
-    }
-  } else {
-    // ---- epilogue: thread = one output feature; ys[row][n] = bf16(acc)
-    const int q = warp & 3;
-    const int m = q * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     uint32_t tph[2] = {0, 0};
-    int slot = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit U = a.units[u];
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int i = next_unit(k, ok);
+      if (i < 0) break;
+      const XUnit X = unit_at(a, i, n_gu);
+      const Unit& U = X.u;
       const int N = round_up(U.nrows, kRowAlign);
-      const bool w = mbar_wait(&tfull[slot], tph[slot], a.err);
-      if (!__all_sync(0xffffffffu, w)) break;
-      tc_fence_after();
-      __nv_bfloat16* yp = a.ys + (size_t)U.p0 * a.d + U.mt * kMTile + m;
-      for (int j0 = 0; j0 < N; j0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_off + 256u * slot + (uint32_t)j0, r);
-        tmem_wait_ld();
+      if (!X.down) {
+        const bool w0 = mbar_wait(&tfull[0], tph[0], a.err);
+        const bool w1 = mbar_wait(&tfull[1], tph[1], a.err);
+        if (!__all_sync(0xffffffffu, w0 && w1)) break;
+        tc_fence_after();
+        __nv_bfloat16* hp = a.h + (size_t)U.p0 * a.hdim + U.mt * kMTile + m;
+        for (int j0 = half * 16; j0 < N; j0 += 32) {
+          uint32_t g[16], v[16];
+          tmem_ld16(tmem + lane_off + (uint32_t)j0, g);
+          tmem_ld16(tmem + lane_off + 256u + (uint32_t)j0, v);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          yp[(size_t)(j0 + i) * a.d] = __float2bfloat16_rn(__uint_as_float(r[i]));
+          for (int r = 0; r < 16; ++r)
+            hp[(size_t)(j0 + r) * a.hdim] =
+                __float2bfloat16_rn(silu_mul(__uint_as_float(g[r]), __uint_as_float(v[r])));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[0]);
+          mbar_arrive(&tempty[1]);
+        }
+        tph[0] ^= 1;
+        tph[1] ^= 1;
+        // publish: all epilogue warps' h stores of this unit, then the chunk counter
+        named_sync(2, kXEpiWarps * 32);
+        if (threadIdx.x == 128) {
+          __threadfence();
+          atomicAdd(a.chunk_done + U.cid, 1);
+        }
+      } else {
+        const bool w0 = mbar_wait(&tfull[0], tph[0], a.err);
+        const bool w1 = mbar_wait(&tfull[1], tph[1], a.err);
+        if (!__all_sync(0xffffffffu, w0 && w1)) break;
+        tc_fence_after();
+        const bool two = (U.mt * 2 + 1) * kMTile < a.d;
+        __nv_bfloat16* yp = a.ys + (size_t)U.p0 * a.d + U.mt * 2 * kMTile + m;
+        for (int j0 = half * 16; j0 < N; j0 += 32) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(tmem + lane_off + (uint32_t)j0, r0);
+          if (two) tmem_ld16(tmem + lane_off + 256u + (uint32_t)j0, r1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            yp[(size_t)(j0 + c) * a.d] = __float2bfloat16_rn(__uint_as_float(r0[c]));
+            if (two) yp[(size_t)(j0 + c) * a.d + kMTile] = __float2bfloat16_rn(__uint_as_float(r1[c]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[0]);
+          mbar_arrive(&tempty[1]);
+        }
+        tph[0] ^= 1;
+        tph[1] ^= 1;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[slot]);
-      tph[slot] ^= 1;
-      slot ^= 1;
     }
   }
   pdl_trigger();
@@ -399,26 +435,20 @@ __global__ void __launch_bounds__(256) combine_kernel(int d, const float* topk_w
 }  // namespace
 
 cudaError_t prepare_expert_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kGuSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDnSmem);
+  return cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kXSmem);
 }
 
-cudaError_t launch_gateup(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
-                          const CUtensorMap& tm_wu, const CUtensorMap& tm_wsg,
-                          const CUtensorMap& tm_wsu, const Dims& D, const RouteWs& ws,
-                          __nv_bfloat16* h, int grid, cudaStream_t s) {
-  GuArgs a{ws.units_gu, ws.n_units, ws.grow, x, h, D.d, D.f, D.hdim, ws.err};
-  return launch_pdl(gateup_kernel, dim3(grid), dim3(kGuThreads), kGuSmem, s, tm_wg, tm_wu, tm_wsg,
-                    tm_wsu, a);
-}
-
-cudaError_t launch_down(const CUtensorMap& tm_h, const CUtensorMap& tm_wd,
-                        const CUtensorMap& tm_wsd, const Dims& D, const RouteWs& ws,
-                        __nv_bfloat16* ys, int grid, cudaStream_t s) {
-  DnArgs a{ws.units_dn, ws.n_units + 1, ys, D.d, D.f, D.fs, ws.err};
-  return launch_pdl(down_kernel, dim3(grid), dim3(192), kDnSmem, s, tm_h, tm_wd, tm_wsd, a);
+cudaError_t launch_experts(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
+                           const CUtensorMap& tm_wu, const CUtensorMap& tm_wsg,
+                           const CUtensorMap& tm_wsu, const CUtensorMap& tm_h,
+                           const CUtensorMap& tm_wd, const CUtensorMap& tm_wsd, const Dims& D,
+                           const RouteWs& ws, __nv_bfloat16* h, __nv_bfloat16* ys, int grid,
+                           cudaStream_t s) {
+  XArgs a{ws.units_gu, ws.units_dn, ws.n_units, ws.next_unit, ws.chunk_done, ws.grow, x, h, ys,
+          D.d, D.f, D.fs, D.hdim, ws.err};
+  return launch_pdl(experts_kernel, dim3(grid), dim3(kXThreads), kXSmem, s, tm_wg, tm_wu, tm_wsg,
+                    tm_wsu, tm_h, tm_wd, tm_wsd, a);
 }
 
 cudaError_t launch_combine(int T, const Dims& D, const float* topk_w, const RouteWs& ws,

@@ -20,9 +20,10 @@ constexpr int kBK = 64;            // K elements per pipeline stage (one 128-byt
 __host__ __device__ constexpr int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
 // One grouped-GEMM work unit: expert group g (g == kE: the shared expert), first padded row
-// p0, valid rows nrows (<= kChunkRows), weight row tile mt.
+// p0, valid rows nrows (<= kChunkRows), weight row tile mt, and cid, the index of its chunk
+// (group, rows) -- the down units of a chunk wait for all gate/up units of the same chunk.
 struct Unit {
-  int g, p0, nrows, mt;
+  int g, p0, nrows, mt, cid;
 };
 
 // Device workspace of the routing chain (all sized for max_tokens at create time).
@@ -39,6 +40,8 @@ struct RouteWs {
   Unit* units_gu;     // gate/up work units
   Unit* units_dn;     // down work units
   int32_t* n_units;   // [2]: gate/up, down
+  int32_t* next_unit; // dynamic schedule counter of the expert kernel (zeroed by the plan)
+  int32_t* chunk_done;  // [chunks] gate/up units finished per chunk (zeroed by the plan)
   int* err;           // device error word
 };
 
@@ -84,16 +87,15 @@ cudaError_t launch_route_plan(int T, const Dims& D, const RouteWs& ws, cudaStrea
 cudaError_t launch_route_scatter(int T, const int32_t* topk_idx, int32_t* perm,
                                  const RouteWs& ws, cudaStream_t s);
 
-// Grouped gate/up GEMM with SwiGLU epilogue: h [P][hdim] bf16.
-cudaError_t launch_gateup(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
-                          const CUtensorMap& tm_wu, const CUtensorMap& tm_wsg,
-                          const CUtensorMap& tm_wsu, const Dims& D, const RouteWs& ws,
-                          __nv_bfloat16* h, int grid, cudaStream_t s);
-
-// Grouped down GEMM: ys [P][d] bf16.
-cudaError_t launch_down(const CUtensorMap& tm_h, const CUtensorMap& tm_wd,
-                        const CUtensorMap& tm_wsd, const Dims& D, const RouteWs& ws,
-                        __nv_bfloat16* ys, int grid, cudaStream_t s);
+// Both grouped GEMMs in one persistent launch: the gate/up units (SwiGLU epilogue, h [P][hdim]
+// bf16) and then the down units (ys [P][d] bf16), a down unit starting once every gate/up unit
+// of its chunk has published its h.
+cudaError_t launch_experts(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
+                           const CUtensorMap& tm_wu, const CUtensorMap& tm_wsg,
+                           const CUtensorMap& tm_wsu, const CUtensorMap& tm_h,
+                           const CUtensorMap& tm_wd, const CUtensorMap& tm_wsd, const Dims& D,
+                           const RouteWs& ws, __nv_bfloat16* h, __nv_bfloat16* ys, int grid,
+                           cudaStream_t s);
 
 // y[t] = sum_j w[t][j] ys[prow[t][j]] + ys[prow[t][8]] in fp32, rounded once to bf16.
 cudaError_t launch_combine(int T, const Dims& D, const float* topk_w, const RouteWs& ws,

@@ -235,11 +235,12 @@ __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws)
   const int cnt = run;
   const int pc = round_up(cnt, kRowAlign);
   const int nch = (cnt + kChunkRows - 1) / kChunkRows;
-  int tot_cnt, tot_pc, tot_gu, tot_dn;
+  int tot_cnt, tot_pc, tot_gu, tot_dn, tot_ch;
   const int off = block_scan_256(cnt, tmp, &tot_cnt);
   const int poff = block_scan_256(pc, tmp, &tot_pc);
   const int ugu = block_scan_256(nch * p.mt_f, tmp, &tot_gu);
   const int udn = block_scan_256(nch * p.mt_d, tmp, &tot_dn);
+  const int cbase = block_scan_256(nch, tmp, &tot_ch);  // chunk ids after the shared chunks
 
   // shared group
   const int nch_s = (p.T + kChunkRows - 1) / kChunkRows;
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws)
     ws.poff[kE + 1] = p_shared + round_up(p.T, kRowAlign);
     ws.n_units[0] = gu_s + tot_gu;
     ws.n_units[1] = dn_s + tot_dn;
+    *ws.next_unit = 0;
   }
   for (int r = poff + cnt; r < poff + pc; ++r) ws.grow[r] = 0;
   if (e == 0)
@@ -262,22 +264,25 @@ __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws)
 
   if (nch > 0) {
     const int cs = round_up((cnt + nch - 1) / nch, kRowAlign);
+    const int cid0 = nch_s + cbase;
+    for (int c = 0; c < nch; ++c) ws.chunk_done[cid0 + c] = 0;
     for (int mt = 0; mt < p.mt_f; ++mt)
       for (int c = 0; c < nch; ++c)
         ws.units_gu[gu_s + ugu + mt * nch + c] =
-            Unit{e, poff + c * cs, min(cs, cnt - c * cs), mt};
+            Unit{e, poff + c * cs, min(cs, cnt - c * cs), mt, cid0 + c};
     for (int mt = 0; mt < p.mt_d; ++mt)
       for (int c = 0; c < nch; ++c)
         ws.units_dn[dn_s + udn + mt * nch + c] =
-            Unit{e, poff + c * cs, min(cs, cnt - c * cs), mt};
+            Unit{e, poff + c * cs, min(cs, cnt - c * cs), mt, cid0 + c};
   }
+  for (int c = threadIdx.x; c < nch_s; c += blockDim.x) ws.chunk_done[c] = 0;
   for (int i = threadIdx.x; i < gu_s; i += blockDim.x) {
     const int mt = i / nch_s, c = i % nch_s;
-    ws.units_gu[i] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt};
+    ws.units_gu[i] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt, c};
   }
   for (int i = threadIdx.x; i < dn_s; i += blockDim.x) {
     const int mt = i / nch_s, c = i % nch_s;
-    ws.units_dn[i] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt};
+    ws.units_dn[i] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt, c};
   }
   pdl_trigger();
 }
@@ -353,8 +358,9 @@ cudaError_t launch_router_topk(const CUtensorMap& tm_x, const CUtensorMap& tm_wr
 }
 
 cudaError_t launch_route_plan(int T, const Dims& D, const RouteWs& ws, cudaStream_t s) {
+  // down units cover 256 outputs (two 128-row weight tiles; the last may have one)
   PlanArgs p{T, (T + kBlockTokens - 1) / kBlockTokens, D.f / kMTile, D.fs / kMTile,
-             D.d / kMTile};
+             (D.d + 2 * kMTile - 1) / (2 * kMTile)};
   return launch_pdl(route_plan_kernel, dim3(1), dim3(256), 0, s, p, ws);
 }
 
