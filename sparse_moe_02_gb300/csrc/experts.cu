@@ -7,8 +7,8 @@
 // into the input projections (§ "Reduce intermediate and state traffic").
 //
 // GB300 design: the weights take the MMA's M = 128 side and the routed token rows the
-// N side (16..256 in steps of 16), so an expert with few tokens still uses full-height MMAs
-// and its weight tile is read once per chunk of up to 256 tokens.  One persistent block per
+// N side (16..192 in steps of 16), so an expert with few tokens still uses full-height MMAs
+// and its weight tile is read once per chunk of up to 192 tokens.  One persistent block per
 // SM walks the work-unit list: the weight tiles reach a shared-memory ring by TMA (128-row
 // tiles) and the routed token rows by 16-byte cp.async gathers straight from x (so
 // no permuted copy of x is ever written), warp 1 issues tcgen05.mma into TMEM, and the
@@ -20,11 +20,11 @@ namespace moe {
 namespace {
 
 constexpr int kTileA = kMTile * kBK * 2;     // 128 weight rows x 64 (16 KB)
-constexpr int kTileB = kChunkRows * kBK * 2; // up to 256 token rows x 64 (32 KB)
+constexpr int kTileB = kChunkRows * kBK * 2; // up to 192 token rows x 64 (24 KB)
 
 // ---------------------------------------------------------------- gate/up + down, one launch
 
-constexpr int kXStages = 3;
+constexpr int kXStages = 4;
 constexpr int kXStage = 2 * kTileA + kTileB;  // weight tile(s) | token rows
 constexpr int kXSmem = kXStages * kXStage + 1024 + 1024;
 constexpr int kXThreads = 384;                 // 12 warps, roles below
@@ -62,7 +62,7 @@ __device__ __forceinline__ XUnit unit_at(const XArgs& a, int i, int n_gu) {
 // One persistent block per SM walks a combined list: every gate/up unit, then every down unit,
 // handed out in list order by an atomic counter (the TMA producer lane takes the next index and
 // passes it to the other roles through a small shared-memory queue).  Gate/up unit: 128 features of one group against up to
-// 256 token rows; gate and up accumulators fill TMEM columns [0, N) and [256, 256 + N) (both
+// 192 token rows; gate and up accumulators fill TMEM columns [0, N) and [256, 256 + N) (both
 // halves); epilogue h = silu(gate) * up -> bf16, then the unit's chunk counter is incremented.
 // Down unit: 256 outputs of one group as two 128-row weight tiles sharing the h rows, the two
 // accumulators in the two TMEM halves; its producer waits for the chunk's counter to reach the
@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
     const int q = warp & 3, half = (warp - 4) >> 2;
     const int m = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint64_t pol_keep = policy_evict_last();  // ys: read back soon by the combine
     uint32_t tph[2] = {0, 0};
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -367,8 +368,11 @@ __global__ void __launch_bounds__(kXThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            yp[(size_t)(j0 + c) * a.d] = __float2bfloat16_rn(__uint_as_float(r0[c]));
-            if (two) yp[(size_t)(j0 + c) * a.d + kMTile] = __float2bfloat16_rn(__uint_as_float(r1[c]));
+            st_b16_hint(yp + (size_t)(j0 + c) * a.d, __float2bfloat16_rn(__uint_as_float(r0[c])),
+                        pol_keep);
+            if (two)
+              st_b16_hint(yp + (size_t)(j0 + c) * a.d + kMTile,
+                          __float2bfloat16_rn(__uint_as_float(r1[c])), pol_keep);
           }
         }
         tc_fence_before();
@@ -405,13 +409,14 @@ __global__ void __launch_bounds__(256) combine_kernel(int d, const float* topk_w
   for (int j = 0; j < 8; ++j) w[j] = topk_w[(size_t)t * kTopK + j];
 #pragma unroll
   for (int j = 0; j < 9; ++j) r[j] = prow[(size_t)t * 9 + j];
+  const uint64_t pol_last = policy_evict_first();  // last use of ys
   for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
     for (int j = 0; j < 9; ++j) {
-      const uint4 v = *reinterpret_cast<const uint4*>(ys + (size_t)r[j] * d + c * 8);
+      const uint4 v = ld_u4_hint(ys + (size_t)r[j] * d + c * 8, pol_last);
       const float wj = j < 8 ? w[j] : 1.0f;
       const uint32_t p[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll

@@ -12,7 +12,7 @@ namespace moe {
 constexpr int kE = 256;            // experts
 constexpr int kTopK = 8;           // kept per token
 constexpr int kBlockTokens = 128;  // tokens per router / scatter block (the MMA M)
-constexpr int kChunkRows = 256;    // most token rows in one grouped-GEMM work unit (MMA N)
+constexpr int kChunkRows = 192;    // most token rows in one grouped-GEMM work unit (MMA N)
 constexpr int kRowAlign = 16;      // expert groups start on 16-row boundaries (MMA N step)
 constexpr int kMTile = 128;        // weight rows per work unit (MMA M)
 constexpr int kBK = 64;            // K elements per pipeline stage (one 128-byte swizzle row)

@@ -13,11 +13,20 @@ namespace {
 
 // ---------------------------------------------------------------- router GEMM + top-8
 
-constexpr int kRtStages = 4;
-constexpr int kRtA = kBlockTokens * kBK * 2;  // x tile: 128 tokens x 64 (16 KB)
-constexpr int kRtB = kE * kBK * 2;            // router tile: 256 experts x 64 (32 KB)
+// A cluster of four blocks per 128 tokens: block r computes the logits of experts
+// [64r, 64r + 64) (tcgen05, M = 128 tokens, N = 64 experts, K = d).  The x tile is shared:
+// each block loads a quarter of its rows and multicasts it to the four.  Each block keeps its
+// 8 largest logits per token and writes them into the leader block's shared memory; the leader
+// merges the 4 x 8 candidates, applies the softmax and counts the histogram.
+constexpr int kRtCluster = 4;
+constexpr int kRtN = kE / kRtCluster;                 // experts per block
+constexpr int kRtStages = 6;
+constexpr int kRtA = kBlockTokens * kBK * 2;          // x tile: 128 tokens x 64 (16 KB)
+constexpr int kRtASlice = kRtA / kRtCluster;          // rows loaded (and multicast) per block
+constexpr int kRtB = kRtN * kBK * 2;                  // router tile: 64 experts x 64 (8 KB)
 constexpr int kRtStage = kRtA + kRtB;
-constexpr int kRtSmem = kRtStages * kRtStage + 1024 + 2048;
+constexpr int kRtCand = kBlockTokens * kRtCluster * 8;  // candidates per cluster
+constexpr int kRtSmem = kRtStages * kRtStage + kRtCand * 8 + 1024 + 2048;
 
 struct RouterArgs {
   const float* bias;
@@ -29,8 +38,7 @@ struct RouterArgs {
 };
 
 // Keeps the 8 largest (value, id) pairs in v/id, sorted by value descending; among equal
-// values the earlier (lower) id stays ahead, because ids arrive in ascending order and a
-// new pair only moves past strictly smaller values.
+// values the earlier-inserted pair stays ahead (callers insert ids in ascending order).
 __device__ __forceinline__ void top8_insert(float (&v)[8], int (&id)[8], float x, int e) {
   if (x > v[7]) {
     v[7] = x;
@@ -50,31 +58,34 @@ __global__ void __launch_bounds__(192, 1)
                        const __grid_constant__ CUtensorMap tm_wr, RouterArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtStages * kRtStage);
+  float* cand_v = reinterpret_cast<float*>(smem + kRtStages * kRtStage);  // [128][32] (leader)
+  int* cand_i = reinterpret_cast<int*>(cand_v + kRtCand);
+  uint64_t* full = reinterpret_cast<uint64_t*>(cand_i + kRtCand);
   uint64_t* empty = full + kRtStages;
   uint64_t* tfull = empty + kRtStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
   int* hist_s = reinterpret_cast<int*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int blk = blockIdx.x;
+  const uint32_t rank = cluster_rank();
+  const int blk = (int)cluster_id_x();  // 128-token block
   const int KB = a.d / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRtStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], kRtCluster);  // released by the MMA of every block of the cluster
     }
     mbar_init(tfull, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, kRtN);
     tmem_relinquish();
   }
   for (int i = threadIdx.x; i < kE; i += blockDim.x) hist_s[i] = 0;
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barriers of every block initialised before any multicast lands
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // x (and the bias) may come from the previous kernel on the stream
@@ -90,14 +101,16 @@ __global__ void __launch_bounds__(192, 1)
         if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) break;
         uint8_t* st = smem + stage * kRtStage;
         mbar_arrive_expect_tx(&full[stage], kRtStage);
-        tma_load_2d(st, &tm_x, &full[stage], kb * kBK, blk * kBlockTokens, keep);
-        tma_load_2d(st + kRtA, &tm_wr, &full[stage], kb * kBK, 0, keep);
+        tma_load_2d_mc(st + rank * kRtASlice, &tm_x, &full[stage], kb * kBK,
+                       blk * kBlockTokens + (int)rank * (kBlockTokens / kRtCluster),
+                       (uint16_t)((1u << kRtCluster) - 1), keep);
+        tma_load_2d(st + kRtA, &tm_wr, &full[stage], kb * kBK, (int)rank * kRtN, keep);
         if (++stage == kRtStages) { stage = 0; ph ^= 1; }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, kE);
+      const uint32_t idesc = idesc_bf16(128, kRtN);
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -109,16 +122,15 @@ __global__ void __launch_bounds__(192, 1)
         for (int kk = 0; kk < kBK / 16; ++kk)
           mma_bf16(tmem, sdesc_k128(sa + kk * 32), sdesc_k128(sb + kk * 32), idesc,
                    (kb | kk) != 0);
-        mma_commit(&empty[stage]);
+        mma_commit_mc(&empty[stage], (uint16_t)((1u << kRtCluster) - 1));
         if (++stage == kRtStages) { stage = 0; ph ^= 1; }
       }
       if (ok) mma_commit(tfull);
     }
   } else {
-    // epilogue: one thread per token row of the tile
+    // epilogue: one thread per token row; local top-8 of this block's 64 experts
     const int q = warp & 3;
     const int m = q * 32 + lane;
-    const int t = blk * kBlockTokens + m;
     const bool have = mbar_wait(tfull, 0, a.err);
     tc_fence_after();
     float v[8];
@@ -126,18 +138,41 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
     for (int i = 0; i < 8; ++i) { v[i] = -INFINITY; id[i] = 0; }
     if (have) {
-      for (int c0 = 0; c0 < kE; c0 += 16) {
+      for (int c0 = 0; c0 < kRtN; c0 += 16) {
         uint32_t r[16];
         tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+          const int e = (int)rank * kRtN + c0 + i;
           float x = __uint_as_float(r[i]);
-          if (a.bias) x += __ldg(a.bias + c0 + i);
-          top8_insert(v, id, x, c0 + i);
+          if (a.bias) x += __ldg(a.bias + e);
+          top8_insert(v, id, x, e);
         }
       }
     }
+    const uint32_t dv = map_shared(cand_v + m * (kRtCluster * 8) + rank * 8, 0);
+    const uint32_t di = map_shared(cand_i + m * (kRtCluster * 8) + rank * 8, 0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      st_cluster_f32(dv + 4 * j, v[j]);
+      st_cluster_s32(di + 4 * j, id[j]);
+    }
+  }
+  tc_fence_before();
+  cluster_sync();  // candidates of all four blocks are in the leader's shared memory
+
+  if (rank == 0 && warp >= 2) {
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const int t = blk * kBlockTokens + m;
+    float v[8];
+    int id[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { v[i] = -INFINITY; id[i] = 0; }
+    // candidates in block-rank order: among equal values, ids arrive in ascending order
+    for (int c = 0; c < kRtCluster * 8; ++c)
+      top8_insert(v, id, cand_v[m * (kRtCluster * 8) + c], cand_i[m * (kRtCluster * 8) + c]);
     // list the kept experts in ascending id
 #pragma unroll
     for (int i = 0; i < 7; ++i)
@@ -153,7 +188,7 @@ __global__ void __launch_bounds__(192, 1)
     float ex[8], s = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) { ex[j] = __expf(v[j] - mx); s += ex[j]; }
-    if (have && t < a.T) {
+    if (t < a.T) {
       int4* pi = reinterpret_cast<int4*>(a.topk_idx + (size_t)t * kTopK);
       float4* pw = reinterpret_cast<float4*>(a.topk_w + (size_t)t * kTopK);
       pi[0] = make_int4(id[0], id[1], id[2], id[3]);
@@ -163,7 +198,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int j = 0; j < 8; ++j) atomicAdd(&hist_s[id[j]], 1);
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+    named_sync(1, 128);  // the four epilogue warps
     const int et = threadIdx.x - 64;
     a.hist[(size_t)blk * kE + et] = hist_s[et];
     a.hist[(size_t)blk * kE + et + 128] = hist_s[et + 128];
@@ -171,7 +206,7 @@ __global__ void __launch_bounds__(192, 1)
   pdl_trigger();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, kRtN);
 }
 
 // ---------------------------------------------------------------- plan
@@ -207,15 +242,27 @@ struct PlanArgs {
   int T, nblk, mt_f, mt_fs, mt_d;
 };
 
+// Last index e in [0, kE) with start[e] <= u (start is non-decreasing); the group holding unit u.
+__device__ __forceinline__ int find_group(const int* start, int u) {
+  int lo = 0, hi = kE - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (start[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // Thread e: totals of expert e over the token blocks (and the per-block prefix), the
 // exclusive scan into offsets, the padded group starts (groups start on 16-row boundaries;
 // the shared expert's T rows follow the routed groups), and the work units: each group is
-// cut into ceil(n / 256) nearly equal chunks of rows, and each chunk is paired with every
+// cut into ceil(n / 192) nearly equal chunks of rows, and each chunk is paired with every
 // weight row tile.  Units are listed shared group first, then experts ascending; inside a
 // group, weight tile major and chunk minor, so units that read the same weights are
-// adjacent and run at the same time on neighbouring blocks.
+// adjacent.  The unit lists are written cooperatively (consecutive threads, consecutive
+// units; the group of a unit found by binary search over the group starts).
 __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws) {
   __shared__ int tmp[16];
+  __shared__ int s_gu0[kE], s_dn0[kE], s_nch[kE], s_cs[kE], s_poff[kE], s_cnt[kE], s_cid0[kE];
   pdl_wait();
   const int e = threadIdx.x;
   // loads first (read-only path), then the prefix stores: keeps 16 loads in flight
@@ -247,6 +294,7 @@ __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws)
   const int cs_s = nch_s ? round_up((p.T + nch_s - 1) / nch_s, kRowAlign) : 0;
   const int gu_s = nch_s * p.mt_fs, dn_s = nch_s * p.mt_d;
   const int p_shared = tot_pc;
+  const int n_gu = gu_s + tot_gu, n_dn = dn_s + tot_dn;
 
   ws.offsets[e] = off;
   ws.poff[e] = poff;
@@ -254,35 +302,45 @@ __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws)
     ws.offsets[kE] = tot_cnt;
     ws.poff[kE] = p_shared;
     ws.poff[kE + 1] = p_shared + round_up(p.T, kRowAlign);
-    ws.n_units[0] = gu_s + tot_gu;
-    ws.n_units[1] = dn_s + tot_dn;
+    ws.n_units[0] = n_gu;
+    ws.n_units[1] = n_dn;
     *ws.next_unit = 0;
   }
   for (int r = poff + cnt; r < poff + pc; ++r) ws.grow[r] = 0;
   if (e == 0)
     for (int r = p_shared + p.T; r < p_shared + round_up(p.T, kRowAlign); ++r) ws.grow[r] = 0;
-
-  if (nch > 0) {
-    const int cs = round_up((cnt + nch - 1) / nch, kRowAlign);
-    const int cid0 = nch_s + cbase;
-    for (int c = 0; c < nch; ++c) ws.chunk_done[cid0 + c] = 0;
-    for (int mt = 0; mt < p.mt_f; ++mt)
-      for (int c = 0; c < nch; ++c)
-        ws.units_gu[gu_s + ugu + mt * nch + c] =
-            Unit{e, poff + c * cs, min(cs, cnt - c * cs), mt, cid0 + c};
-    for (int mt = 0; mt < p.mt_d; ++mt)
-      for (int c = 0; c < nch; ++c)
-        ws.units_dn[dn_s + udn + mt * nch + c] =
-            Unit{e, poff + c * cs, min(cs, cnt - c * cs), mt, cid0 + c};
-  }
+  const int cid0 = nch_s + cbase;
+  for (int c = 0; c < nch; ++c) ws.chunk_done[cid0 + c] = 0;
   for (int c = threadIdx.x; c < nch_s; c += blockDim.x) ws.chunk_done[c] = 0;
-  for (int i = threadIdx.x; i < gu_s; i += blockDim.x) {
-    const int mt = i / nch_s, c = i % nch_s;
-    ws.units_gu[i] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt, c};
+
+  s_gu0[e] = gu_s + ugu;
+  s_dn0[e] = dn_s + udn;
+  s_nch[e] = nch;
+  s_cs[e] = nch ? round_up((cnt + nch - 1) / nch, kRowAlign) : 0;
+  s_poff[e] = poff;
+  s_cnt[e] = cnt;
+  s_cid0[e] = cid0;
+  __syncthreads();
+
+  for (int u = threadIdx.x; u < n_gu; u += blockDim.x) {
+    if (u < gu_s) {
+      const int mt = u / nch_s, c = u % nch_s;
+      ws.units_gu[u] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt, c};
+    } else {
+      const int g = find_group(s_gu0, u), l = u - s_gu0[g], n = s_nch[g];
+      const int mt = l / n, c = l % n, cs = s_cs[g];
+      ws.units_gu[u] = Unit{g, s_poff[g] + c * cs, min(cs, s_cnt[g] - c * cs), mt, s_cid0[g] + c};
+    }
   }
-  for (int i = threadIdx.x; i < dn_s; i += blockDim.x) {
-    const int mt = i / nch_s, c = i % nch_s;
-    ws.units_dn[i] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt, c};
+  for (int u = threadIdx.x; u < n_dn; u += blockDim.x) {
+    if (u < dn_s) {
+      const int mt = u / nch_s, c = u % nch_s;
+      ws.units_dn[u] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt, c};
+    } else {
+      const int g = find_group(s_dn0, u), l = u - s_dn0[g], n = s_nch[g];
+      const int mt = l / n, c = l % n, cs = s_cs[g];
+      ws.units_dn[u] = Unit{g, s_poff[g] + c * cs, min(cs, s_cnt[g] - c * cs), mt, s_cid0[g] + c};
+    }
   }
   pdl_trigger();
 }
@@ -354,7 +412,21 @@ cudaError_t launch_router_topk(const CUtensorMap& tm_x, const CUtensorMap& tm_wr
                                float* topk_w, const RouteWs& ws, cudaStream_t s) {
   RouterArgs a{bias, T, D.d, topk_idx, topk_w, ws.hist, ws.err};
   const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
-  return launch_pdl(router_topk_kernel, dim3(nblk), dim3(192), kRtSmem, s, tm_x, tm_wr, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nblk * kRtCluster);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = kRtSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kRtCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, router_topk_kernel, tm_x, tm_wr, a);
 }
 
 cudaError_t launch_route_plan(int T, const Dims& D, const RouteWs& ws, cudaStream_t s) {
