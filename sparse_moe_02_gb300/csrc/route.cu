@@ -25,8 +25,10 @@ constexpr int kRtA = kBlockTokens * kBK * 2;          // x tile: 128 tokens x 64
 constexpr int kRtASlice = kRtA / kRtCluster;          // rows loaded (and multicast) per block
 constexpr int kRtB = kRtN * kBK * 2;                  // router tile: 64 experts x 64 (8 KB)
 constexpr int kRtStage = kRtA + kRtB;
-constexpr int kRtCand = kBlockTokens * kRtCluster * 8;  // candidates per cluster
-constexpr int kRtSmem = kRtStages * kRtStage + kRtCand * 8 + 1024 + 2048;
+constexpr int kRtThreads = 320;                       // producer, MMA, 8 epilogue warps
+constexpr int kRtCand = kBlockTokens * kRtCluster * 8;  // leader: 4 lists of 8 per token
+constexpr int kRtHalf = kBlockTokens * 2 * 8;           // each block: 2 half-lists per token
+constexpr int kRtSmem = kRtStages * kRtStage + (kRtCand + kRtHalf) * 8 + 1024 + 2048;
 
 struct RouterArgs {
   const float* bias;
@@ -53,14 +55,43 @@ __device__ __forceinline__ void top8_insert(float (&v)[8], int (&id)[8], float x
   }
 }
 
-__global__ void __launch_bounds__(192, 1)
+// The 8 largest of L lists of 8 (each sorted by value descending, ids ascending among equal
+// values; list l holding lower ids than list l + 1): eight steps, each taking the largest
+// head, the lower list on equal values -- so ties still go to the lower id.
+template <int L>
+__device__ __forceinline__ void merge_top8(const float* cv, const int* ci, float (&v)[8],
+                                           int (&id)[8]) {
+  int pos[L];
+#pragma unroll
+  for (int l = 0; l < L; ++l) pos[l] = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float bv = -INFINITY;
+    int bl = 0;
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+      const float hv = pos[l] < 8 ? cv[l * 8 + pos[l]] : -INFINITY;
+      if (hv > bv) { bv = hv; bl = l; }
+    }
+    int bi = 0;
+#pragma unroll
+    for (int l = 0; l < L; ++l)
+      if (l == bl) { bi = ci[l * 8 + pos[l]]; pos[l] += 1; }
+    v[k] = bv;
+    id[k] = bi;
+  }
+}
+
+__global__ void __launch_bounds__(kRtThreads, 1)
     router_topk_kernel(const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_wr, RouterArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  float* cand_v = reinterpret_cast<float*>(smem + kRtStages * kRtStage);  // [128][32] (leader)
+  float* cand_v = reinterpret_cast<float*>(smem + kRtStages * kRtStage);  // [128][4][8] leader
   int* cand_i = reinterpret_cast<int*>(cand_v + kRtCand);
-  uint64_t* full = reinterpret_cast<uint64_t*>(cand_i + kRtCand);
+  float* half_v = reinterpret_cast<float*>(cand_i + kRtCand);             // [128][2][8]
+  int* half_i = reinterpret_cast<int*>(half_v + kRtHalf);
+  uint64_t* full = reinterpret_cast<uint64_t*>(half_i + kRtHalf);
   uint64_t* empty = full + kRtStages;
   uint64_t* tfull = empty + kRtStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
@@ -128,8 +159,8 @@ __global__ void __launch_bounds__(192, 1)
       if (ok) mma_commit(tfull);
     }
   } else {
-    // epilogue: one thread per token row; local top-8 of this block's 64 experts
-    const int q = warp & 3;
+    // epilogue: thread = one token row and one half (32) of this block's 64 experts
+    const int q = warp & 3, half = (warp - 2) >> 2;
     const int m = q * 32 + lane;
     const bool have = mbar_wait(tfull, 0, a.err);
     tc_fence_after();
@@ -138,41 +169,47 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
     for (int i = 0; i < 8; ++i) { v[i] = -INFINITY; id[i] = 0; }
     if (have) {
-      for (int c0 = 0; c0 < kRtN; c0 += 16) {
+#pragma unroll
+      for (int c0 = 0; c0 < kRtN / 2; c0 += 16) {
         uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * (kRtN / 2) + c0), r);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int e = (int)rank * kRtN + c0 + i;
+          const int e = (int)rank * kRtN + half * (kRtN / 2) + c0 + i;
           float x = __uint_as_float(r[i]);
           if (a.bias) x += __ldg(a.bias + e);
           top8_insert(v, id, x, e);
         }
       }
     }
-    const uint32_t dv = map_shared(cand_v + m * (kRtCluster * 8) + rank * 8, 0);
-    const uint32_t di = map_shared(cand_i + m * (kRtCluster * 8) + rank * 8, 0);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      st_cluster_f32(dv + 4 * j, v[j]);
-      st_cluster_s32(di + 4 * j, id[j]);
+      half_v[(m * 2 + half) * 8 + j] = v[j];
+      half_i[(m * 2 + half) * 8 + j] = id[j];
+    }
+    named_sync(1, 8 * 32);  // both halves of every token listed
+    if (half == 0) {
+      merge_top8<2>(half_v + m * 16, half_i + m * 16, v, id);
+      const uint32_t dv = map_shared(cand_v + m * (kRtCluster * 8) + rank * 8, 0);
+      const uint32_t di = map_shared(cand_i + m * (kRtCluster * 8) + rank * 8, 0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        st_cluster_f32(dv + 4 * j, v[j]);
+        st_cluster_s32(di + 4 * j, id[j]);
+      }
     }
   }
   tc_fence_before();
   cluster_sync();  // candidates of all four blocks are in the leader's shared memory
 
-  if (rank == 0 && warp >= 2) {
+  if (rank == 0 && warp >= 2 && ((warp - 2) >> 2) == 0) {
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const int t = blk * kBlockTokens + m;
     float v[8];
     int id[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { v[i] = -INFINITY; id[i] = 0; }
-    // candidates in block-rank order: among equal values, ids arrive in ascending order
-    for (int c = 0; c < kRtCluster * 8; ++c)
-      top8_insert(v, id, cand_v[m * (kRtCluster * 8) + c], cand_i[m * (kRtCluster * 8) + c]);
+    merge_top8<kRtCluster>(cand_v + m * (kRtCluster * 8), cand_i + m * (kRtCluster * 8), v, id);
     // list the kept experts in ascending id
 #pragma unroll
     for (int i = 0; i < 7; ++i)
@@ -198,7 +235,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int j = 0; j < 8; ++j) atomicAdd(&hist_s[id[j]], 1);
     }
-    named_sync(1, 128);  // the four epilogue warps
+    named_sync(2, 128);  // the four merging warps
     const int et = threadIdx.x - 64;
     a.hist[(size_t)blk * kE + et] = hist_s[et];
     a.hist[(size_t)blk * kE + et + 128] = hist_s[et + 128];
@@ -414,7 +451,7 @@ cudaError_t launch_router_topk(const CUtensorMap& tm_x, const CUtensorMap& tm_wr
   const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nblk * kRtCluster);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(kRtThreads);
   cfg.dynamicSmemBytes = kRtSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
