@@ -35,7 +35,7 @@ METRIC = "MoE-layer prefill tokens/s @T=4096 & decode us/layer (T=1); % of roofl
 T_PREFILL, D, F, FS, E, K = 4096, 2048, 512, 512, 256, 8
 DECODE_LAYERS = 40
 FLUSH_BYTES = 256 << 20  # larger than the 129 MB L2
-KERNELS_GEMM = ("router_topk", "route_plan", "route_scatter", "experts", "combine")
+KERNELS_GEMM = ("router_topk", "route_plan_scatter", "experts", "combine")
 KERNELS_GEMV = ("decode_router_shared", "decode_gateup", "decode_down_combine")
 
 
@@ -393,7 +393,7 @@ def profiled_traffic(kernel):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    src = {"router_topk": "route.cu", "route_plan": "route.cu", "route_scatter": "route.cu",
+    src = {"router_topk": "route.cu", "route_plan_scatter": "route.cu",
            "experts": "experts.cu", "combine": "experts.cu"}.get(kernel)
     if not src:
         return None

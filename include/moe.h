@@ -137,8 +137,9 @@ int moe_last_cuda_error(void);
  * per kernel without overlap).  moe_profile_end synchronises on those events, writes to
  * ms[i] the device time of the i-th kernel summed over the recorded calls (i < *n_kernels,
  * at most `capacity` entries), sets *n_calls to the number of calls recorded, and stops
- * profiling.  Kernel order -- tensor-core schedule (5): router_topk, route_plan,
- * route_scatter, experts (gate/up and down), combine; matrix-vector schedule (3):
+ * profiling.  Kernel order -- tensor-core schedule (4): router_topk, route_plan_scatter (one
+ * launch up to T = 16384; above, a plan launch and a scatter launch share this slot),
+ * experts (gate/up and down), combine; matrix-vector schedule (3):
  * decode_router_shared, decode_gateup, decode_down_combine.  All recorded calls must use one
  * schedule. */
 int moe_profile_begin(moe_handle h, int n_calls);

@@ -32,7 +32,7 @@ EXPORTS = ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_ge
            "moe_profile_end", "moe_route_one_noalloc")
 
 # kernel order reported by moe_profile_end
-KERNELS_GEMM = ("router_topk", "route_plan", "route_scatter", "experts", "combine")
+KERNELS_GEMM = ("router_topk", "route_plan_scatter", "experts", "combine")
 KERNELS_GEMV = ("decode_router_shared", "decode_gateup", "decode_down_combine")
 
 _c_int, _c_void_p = ctypes.c_int, ctypes.c_void_p

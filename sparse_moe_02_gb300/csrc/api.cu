@@ -208,9 +208,7 @@ int run_route_gemm(moe_handle h, const void* x, int T, int32_t* topk_idx, float*
                                                 topk_idx, topk_w, w, s))))
     return st;
   if (prof && (st = prof_mark(h, s, 1))) return st;
-  if ((st = cuda_status(moe::launch_route_plan(T, h->D, w, s)))) return st;
-  if (prof && (st = prof_mark(h, s, 2))) return st;
-  return cuda_status(moe::launch_route_scatter(T, topk_idx, perm, w, s));
+  return cuda_status(moe::launch_route_plan_scatter(T, h->D, topk_idx, perm, w, s));
 }
 
 }  // namespace
@@ -331,15 +329,15 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
   if ((st = run_route_gemm(h, x, T, h->rws.topk_idx, h->rws.topk_w, nullptr, h->rws.perm, s,
                            true)))
     return st;
-  if ((st = prof_mark(h, s, 3))) return st;
+  if ((st = prof_mark(h, s, 2))) return st;
   if ((st = cuda_status(moe::launch_experts(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu,
                                             h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->h,
                                             h->ys, h->sms, s))))
     return st;
-  if ((st = prof_mark(h, s, 4))) return st;
+  if ((st = prof_mark(h, s, 3))) return st;
   if ((st = cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, s))))
     return st;
-  return prof_finish_call(h, s, 5);
+  return prof_finish_call(h, s, 4);
 }
 
 int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void* stream) {

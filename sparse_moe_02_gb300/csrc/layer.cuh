@@ -31,7 +31,7 @@ struct RouteWs {
   int32_t* topk_idx;  // [T][8] when the caller does not supply one
   float* topk_w;      // [T][8]
   int32_t* hist;      // [nblk][E] assignments per (token block, expert)
-  int32_t* blkpre;    // [nblk][E] assignments of earlier blocks, per expert
+  int32_t* blkpre;    // [nblk][E] assignments of earlier blocks, per expert (two-launch plan)
   int32_t* offsets;   // [E+1]
   int32_t* poff;      // [E+2] padded start row of each group (E = shared), poff[E+1] = total
   int32_t* perm;      // [T*8] slot -> t*8+j
@@ -80,12 +80,12 @@ cudaError_t launch_router_topk(const CUtensorMap& tm_x, const CUtensorMap& tm_wr
                                const float* bias, int T, const Dims& D, int32_t* topk_idx,
                                float* topk_w, const RouteWs& ws, cudaStream_t s);
 
-// Per-expert totals, offsets, padded group starts and the work-unit lists (one block).
-cudaError_t launch_route_plan(int T, const Dims& D, const RouteWs& ws, cudaStream_t s);
-
-// Counting-sort scatter: perm, prow, grow (one block per 128 tokens).
-cudaError_t launch_route_scatter(int T, const int32_t* topk_idx, int32_t* perm,
-                                 const RouteWs& ws, cudaStream_t s);
+// Per-expert totals, offsets, padded group starts, the work-unit lists and the counting-sort
+// scatter (perm, prow, grow): one launch of one block per token block while there are at most
+// kFusedPlanBlocks token blocks, else a one-block plan launch and a scatter launch.
+constexpr int kFusedPlanBlocks = 128;
+cudaError_t launch_route_plan_scatter(int T, const Dims& D, const int32_t* topk_idx,
+                                      int32_t* perm, const RouteWs& ws, cudaStream_t s);
 
 // Both grouped GEMMs in one persistent launch: the gate/up units (SwiGLU epilogue, h [P][hdim]
 // bf16) and then the down units (ys [P][d] bf16), a down unit starting once every gate/up unit

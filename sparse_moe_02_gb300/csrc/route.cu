@@ -248,36 +248,108 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 
 // ---------------------------------------------------------------- plan
 
-// Exclusive scan of v over the 256 threads of the block; *total receives the sum.
-__device__ int block_scan_256(int v, int* tmp, int* total) {
+// Exclusive scans of N values over the 256 threads of the block: v[n] becomes the sum of v[n]
+// over lower threads, total[n] the block sum.  Two barriers for all N scans.
+template <int N>
+__device__ __forceinline__ void block_scan_256(int (&v)[N], int* tmp, int (&total)[N]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  int x[N];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) tmp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < 8 ? tmp[lane] : 0;
+  for (int n = 0; n < N; ++n) {
+    x[n] = v[n];
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x[n], o);
+      if (lane >= o) x[n] += y;
     }
-    if (lane < 8) tmp[8 + lane] = w;
+    if (lane == 31) tmp[n * 8 + warp] = x[n];
   }
   __syncthreads();
-  const int before = (warp > 0 ? tmp[8 + warp - 1] : 0) + x - v;
-  *total = tmp[15];
-  __syncthreads();
-  return before;
+#pragma unroll
+  for (int n = 0; n < N; ++n) {
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const int c = tmp[n * 8 + w];
+      base += w < warp ? c : 0;
+      tot += c;
+    }
+    v[n] = base + x[n] - v[n];
+    total[n] = tot;
+  }
+  __syncthreads();  // tmp may be reused
 }
 
 struct PlanArgs {
   int T, nblk, mt_f, mt_fs, mt_d;
 };
+
+// The expert groups of one plan, in shared memory: per expert the first gate/up and down unit,
+// chunk count and size, padded start row, assignment count, first chunk id and offset; and the
+// shared group's figures.
+struct GroupTable {
+  int gu0[kE], dn0[kE], nch[kE], cs[kE], poff[kE], cnt[kE], cid0[kE], off[kE];
+  int tmp[8 * 5];
+  int n_gu, n_dn, gu_s, dn_s, nch_s, cs_s, p_shared;
+};
+
+// Thread e (all 256 threads call it) with cnt = assignments to expert e: the exclusive scan into
+// offsets, the padded group starts (groups start on 16-row boundaries; the shared expert's T rows
+// follow the routed groups), and the unit bookkeeping: each group is cut into ceil(n / 192)
+// nearly equal chunks of rows, and each chunk is paired with every weight row tile.  Units are
+// listed shared group first, then experts ascending; inside a group, weight tile major and chunk
+// minor, so units that read the same weights are adjacent.  The writer block also stores the
+// global offsets, group starts and unit counts, zeroes the schedule counter, the chunk counters
+// and the grow entries of padding rows.
+__device__ void plan_groups(const PlanArgs& p, int cnt, GroupTable& G, const RouteWs& ws,
+                            bool writer) {
+  const int e = threadIdx.x;
+  const int pc = round_up(cnt, kRowAlign);
+  const int nch = (cnt + kChunkRows - 1) / kChunkRows;
+  int v[5] = {cnt, pc, nch * p.mt_f, nch * p.mt_d, nch};
+  int tot[5];
+  block_scan_256<5>(v, G.tmp, tot);
+  const int nch_s = (p.T + kChunkRows - 1) / kChunkRows;
+  const int cs_s = nch_s ? round_up((p.T + nch_s - 1) / nch_s, kRowAlign) : 0;
+  const int gu_s = nch_s * p.mt_fs, dn_s = nch_s * p.mt_d;
+  const int p_shared = tot[1];
+  const int cid0 = nch_s + v[4];
+  G.gu0[e] = gu_s + v[2];
+  G.dn0[e] = dn_s + v[3];
+  G.nch[e] = nch;
+  G.cs[e] = nch ? round_up((cnt + nch - 1) / nch, kRowAlign) : 0;
+  G.poff[e] = v[1];
+  G.cnt[e] = cnt;
+  G.cid0[e] = cid0;
+  G.off[e] = v[0];
+  if (e == 0) {
+    G.n_gu = gu_s + tot[2];
+    G.n_dn = dn_s + tot[3];
+    G.gu_s = gu_s;
+    G.dn_s = dn_s;
+    G.nch_s = nch_s;
+    G.cs_s = cs_s;
+    G.p_shared = p_shared;
+  }
+  if (writer) {
+    ws.offsets[e] = v[0];
+    ws.poff[e] = v[1];
+    if (e == kE - 1) {
+      ws.offsets[kE] = tot[0];
+      ws.poff[kE] = p_shared;
+      ws.poff[kE + 1] = p_shared + round_up(p.T, kRowAlign);
+      ws.n_units[0] = gu_s + tot[2];
+      ws.n_units[1] = dn_s + tot[3];
+      *ws.next_unit = 0;
+    }
+    for (int r = v[1] + cnt; r < v[1] + pc; ++r) ws.grow[r] = 0;
+    if (e == 0)
+      for (int r = p_shared + p.T; r < p_shared + round_up(p.T, kRowAlign); ++r) ws.grow[r] = 0;
+    for (int c = 0; c < nch; ++c) ws.chunk_done[cid0 + c] = 0;
+    for (int c = threadIdx.x; c < nch_s; c += blockDim.x) ws.chunk_done[c] = 0;
+  }
+  __syncthreads();
+}
 
 // Last index e in [0, kE) with start[e] <= u (start is non-decreasing); the group holding unit u.
 __device__ __forceinline__ int find_group(const int* start, int u) {
@@ -289,17 +361,106 @@ __device__ __forceinline__ int find_group(const int* start, int u) {
   return lo;
 }
 
-// Thread e: totals of expert e over the token blocks (and the per-block prefix), the
-// exclusive scan into offsets, the padded group starts (groups start on 16-row boundaries;
-// the shared expert's T rows follow the routed groups), and the work units: each group is
-// cut into ceil(n / 192) nearly equal chunks of rows, and each chunk is paired with every
-// weight row tile.  Units are listed shared group first, then experts ascending; inside a
-// group, weight tile major and chunk minor, so units that read the same weights are
-// adjacent.  The unit lists are written cooperatively (consecutive threads, consecutive
-// units; the group of a unit found by binary search over the group starts).
+// Writes units [lo, hi) of one list (gate/up: dn = false) from the group table: consecutive
+// threads, consecutive units; the group of a unit found by binary search over the group starts.
+__device__ void plan_units(const GroupTable& G, Unit* units, bool dn, int lo, int hi, int T) {
+  const int* start = dn ? G.dn0 : G.gu0;
+  const int n_s = dn ? G.dn_s : G.gu_s;
+  for (int u = lo + (int)threadIdx.x; u < hi; u += blockDim.x) {
+    if (u < n_s) {
+      const int mt = u / G.nch_s, c = u % G.nch_s;
+      units[u] = Unit{kE, G.p_shared + c * G.cs_s, min(G.cs_s, T - c * G.cs_s), mt, c};
+    } else {
+      const int g = find_group(start, u), l = u - start[g], n = G.nch[g];
+      const int mt = l / n, c = l % n, cs = G.cs[g];
+      units[u] = Unit{g, G.poff[g] + c * cs, min(cs, G.cnt[g] - c * cs), mt, G.cid0[g] + c};
+    }
+  }
+}
+
+// Scatter of the tokens of token block `blk` (threads 0..127, one token each, four warps of
+// 32): the rank of (t, e) among the assignments to expert e = `pre[e]` (assignments of earlier
+// blocks) + those of earlier warps of this block + those of lower lanes of this warp, counted
+// from per-warp bit masks of the tokens that chose e.  mask must be zero on entry; every thread
+// of the block calls this (it holds one barrier).
+__device__ __forceinline__ void scatter_block(int blk, int T, const int32_t* topk_idx,
+                                              int32_t* perm, const RouteWs& ws,
+                                              uint32_t (*mask)[kE], const int* pre,
+                                              const int* off, const int* poff, int p_shared) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blk * kBlockTokens + (int)threadIdx.x;
+  const bool valid = threadIdx.x < kBlockTokens && t < T;
+  int e[8];
+  if (valid) {
+    const int4* pi = reinterpret_cast<const int4*>(topk_idx + (size_t)t * kTopK);
+    const int4 a = pi[0], b = pi[1];
+    e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
+    e[4] = b.x; e[5] = b.y; e[6] = b.z; e[7] = b.w;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) atomicOr(&mask[warp][e[j]], 1u << lane);
+  }
+  __syncthreads();
+  if (valid) {
+    const uint32_t below = (1u << lane) - 1u;
+    int pr[9];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int ee = e[j];
+      int rank = pre[ee] + __popc(mask[warp][ee] & below);
+      for (int w = 0; w < warp; ++w) rank += __popc(mask[w][ee]);
+      perm[off[ee] + rank] = t * kTopK + j;
+      pr[j] = poff[ee] + rank;
+      ws.grow[pr[j]] = t;
+    }
+    pr[8] = p_shared + t;
+    ws.grow[pr[8]] = t;
+    int* prow = ws.prow + (size_t)t * 9;
+#pragma unroll
+    for (int j = 0; j < 9; ++j) prow[j] = pr[j];
+  }
+}
+
+// Plan and scatter in one launch, one block of 256 threads per 128-token block (used while
+// the token blocks are few, so that every block can afford to read the whole histogram):
+// thread e sums expert e's counts over all token blocks (the total) and over the blocks before
+// this one (its scatter base); every block builds the same group table, writes its share of
+// the unit lists and scatters its own tokens; block 0 writes the global plan outputs.
+__global__ void __launch_bounds__(256)
+    route_plan_scatter_kernel(PlanArgs p, const int32_t* topk_idx, int32_t* perm, RouteWs ws) {
+  __shared__ GroupTable G;
+  __shared__ int s_pre[kE];
+  __shared__ uint32_t mask[4][kE];
+  pdl_wait();
+  const int e = threadIdx.x, blk = blockIdx.x;
+  int pre = 0, tot = 0;
+  for (int b0 = 0; b0 < p.nblk; b0 += 32) {
+    int c[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      c[i] = b0 + i < p.nblk ? __ldg(ws.hist + (size_t)(b0 + i) * kE + e) : 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      tot += c[i];
+      pre += b0 + i < blk ? c[i] : 0;
+    }
+  }
+  s_pre[e] = pre;
+  for (int i = threadIdx.x; i < 4 * kE; i += blockDim.x) (&mask[0][0])[i] = 0u;
+  plan_groups(p, tot, G, ws, blk == 0);  // ends with a barrier
+  const long long nb = gridDim.x;
+  plan_units(G, ws.units_gu, false, (int)(G.n_gu * blk / nb), (int)(G.n_gu * (blk + 1) / nb),
+             p.T);
+  plan_units(G, ws.units_dn, true, (int)(G.n_dn * blk / nb), (int)(G.n_dn * (blk + 1) / nb),
+             p.T);
+  scatter_block(blk, p.T, topk_idx, perm, ws, mask, s_pre, G.off, G.poff, G.p_shared);
+  pdl_trigger();
+}
+
+// The same for many token blocks, in two launches.  Plan (one block): thread e walks expert
+// e's counts over the token blocks, storing each block's base (blkpre), then builds the group
+// table, the global plan outputs and the whole unit lists.
 __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws) {
-  __shared__ int tmp[16];
-  __shared__ int s_gu0[kE], s_dn0[kE], s_nch[kE], s_cs[kE], s_poff[kE], s_cnt[kE], s_cid0[kE];
+  __shared__ GroupTable G;
   pdl_wait();
   const int e = threadIdx.x;
   // loads first (read-only path), then the prefix stores: keeps 16 loads in flight
@@ -316,124 +477,28 @@ __global__ void __launch_bounds__(256) route_plan_kernel(PlanArgs p, RouteWs ws)
         run += c[i];
       }
   }
-  const int cnt = run;
-  const int pc = round_up(cnt, kRowAlign);
-  const int nch = (cnt + kChunkRows - 1) / kChunkRows;
-  int tot_cnt, tot_pc, tot_gu, tot_dn, tot_ch;
-  const int off = block_scan_256(cnt, tmp, &tot_cnt);
-  const int poff = block_scan_256(pc, tmp, &tot_pc);
-  const int ugu = block_scan_256(nch * p.mt_f, tmp, &tot_gu);
-  const int udn = block_scan_256(nch * p.mt_d, tmp, &tot_dn);
-  const int cbase = block_scan_256(nch, tmp, &tot_ch);  // chunk ids after the shared chunks
-
-  // shared group
-  const int nch_s = (p.T + kChunkRows - 1) / kChunkRows;
-  const int cs_s = nch_s ? round_up((p.T + nch_s - 1) / nch_s, kRowAlign) : 0;
-  const int gu_s = nch_s * p.mt_fs, dn_s = nch_s * p.mt_d;
-  const int p_shared = tot_pc;
-  const int n_gu = gu_s + tot_gu, n_dn = dn_s + tot_dn;
-
-  ws.offsets[e] = off;
-  ws.poff[e] = poff;
-  if (e == kE - 1) {
-    ws.offsets[kE] = tot_cnt;
-    ws.poff[kE] = p_shared;
-    ws.poff[kE + 1] = p_shared + round_up(p.T, kRowAlign);
-    ws.n_units[0] = n_gu;
-    ws.n_units[1] = n_dn;
-    *ws.next_unit = 0;
-  }
-  for (int r = poff + cnt; r < poff + pc; ++r) ws.grow[r] = 0;
-  if (e == 0)
-    for (int r = p_shared + p.T; r < p_shared + round_up(p.T, kRowAlign); ++r) ws.grow[r] = 0;
-  const int cid0 = nch_s + cbase;
-  for (int c = 0; c < nch; ++c) ws.chunk_done[cid0 + c] = 0;
-  for (int c = threadIdx.x; c < nch_s; c += blockDim.x) ws.chunk_done[c] = 0;
-
-  s_gu0[e] = gu_s + ugu;
-  s_dn0[e] = dn_s + udn;
-  s_nch[e] = nch;
-  s_cs[e] = nch ? round_up((cnt + nch - 1) / nch, kRowAlign) : 0;
-  s_poff[e] = poff;
-  s_cnt[e] = cnt;
-  s_cid0[e] = cid0;
-  __syncthreads();
-
-  for (int u = threadIdx.x; u < n_gu; u += blockDim.x) {
-    if (u < gu_s) {
-      const int mt = u / nch_s, c = u % nch_s;
-      ws.units_gu[u] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt, c};
-    } else {
-      const int g = find_group(s_gu0, u), l = u - s_gu0[g], n = s_nch[g];
-      const int mt = l / n, c = l % n, cs = s_cs[g];
-      ws.units_gu[u] = Unit{g, s_poff[g] + c * cs, min(cs, s_cnt[g] - c * cs), mt, s_cid0[g] + c};
-    }
-  }
-  for (int u = threadIdx.x; u < n_dn; u += blockDim.x) {
-    if (u < dn_s) {
-      const int mt = u / nch_s, c = u % nch_s;
-      ws.units_dn[u] = Unit{kE, p_shared + c * cs_s, min(cs_s, p.T - c * cs_s), mt, c};
-    } else {
-      const int g = find_group(s_dn0, u), l = u - s_dn0[g], n = s_nch[g];
-      const int mt = l / n, c = l % n, cs = s_cs[g];
-      ws.units_dn[u] = Unit{g, s_poff[g] + c * cs, min(cs, s_cnt[g] - c * cs), mt, s_cid0[g] + c};
-    }
-  }
+  plan_groups(p, run, G, ws, true);
+  plan_units(G, ws.units_gu, false, 0, G.n_gu, p.T);
+  plan_units(G, ws.units_dn, true, 0, G.n_dn, p.T);
   pdl_trigger();
 }
 
-// ---------------------------------------------------------------- scatter
-
-// One block per 128 tokens, one thread per token, four warps of 32 tokens.  The rank of
-// (t, e) among the assignments to expert e = assignments in earlier blocks (blkpre) +
-// those of earlier warps of this block + those of lower lanes of this warp, each counted
-// from per-warp bit masks of the tokens that chose e.
+// Scatter (one block of 128 threads per token block) from the plan's global outputs.
 __global__ void __launch_bounds__(128) route_scatter_kernel(int T, const int32_t* topk_idx,
                                                             int32_t* perm, RouteWs ws) {
   __shared__ uint32_t mask[4][kE];
+  __shared__ int s_pre[kE], s_off[kE], s_poff[kE + 1];
   pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int blk = blockIdx.x;
-  const int t = blk * kBlockTokens + threadIdx.x;
-  const bool valid = t < T;
   for (int i = threadIdx.x; i < 4 * kE; i += blockDim.x) (&mask[0][0])[i] = 0u;
-  __syncthreads();
-  int e[8];
-  if (valid) {
-    const int4* pi = reinterpret_cast<const int4*>(topk_idx + (size_t)t * kTopK);
-    const int4 a = pi[0], b = pi[1];
-    e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
-    e[4] = b.x; e[5] = b.y; e[6] = b.z; e[7] = b.w;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) atomicOr(&mask[warp][e[j]], 1u << lane);
+  for (int i = threadIdx.x; i < kE; i += blockDim.x) {
+    s_pre[i] = __ldg(ws.blkpre + (size_t)blk * kE + i);
+    s_off[i] = __ldg(ws.offsets + i);
+    s_poff[i] = __ldg(ws.poff + i);
   }
+  if (threadIdx.x == 0) s_poff[kE] = __ldg(ws.poff + kE);
   __syncthreads();
-  if (valid) {
-    // all loads (read-only path) before the scattered stores
-    const uint32_t below = (1u << lane) - 1u;
-    int rank[8], off[8], po[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int ee = e[j];
-      rank[j] = __ldg(ws.blkpre + (size_t)blk * kE + ee) + __popc(mask[warp][ee] & below);
-      for (int w = 0; w < warp; ++w) rank[j] += __popc(mask[w][ee]);
-      off[j] = __ldg(ws.offsets + ee);
-      po[j] = __ldg(ws.poff + ee);
-    }
-    const int ps = __ldg(ws.poff + kE) + t;
-    int pr[9];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      perm[off[j] + rank[j]] = t * kTopK + j;
-      pr[j] = po[j] + rank[j];
-      ws.grow[pr[j]] = t;
-    }
-    pr[8] = ps;
-    ws.grow[ps] = t;
-    int* prow = ws.prow + (size_t)t * 9;
-#pragma unroll
-    for (int j = 0; j < 9; ++j) prow[j] = pr[j];
-  }
+  scatter_block(blk, T, topk_idx, perm, ws, mask, s_pre, s_off, s_poff, s_poff[kE]);
   pdl_trigger();
 }
 
@@ -466,16 +531,16 @@ cudaError_t launch_router_topk(const CUtensorMap& tm_x, const CUtensorMap& tm_wr
   return cudaLaunchKernelEx(&cfg, router_topk_kernel, tm_x, tm_wr, a);
 }
 
-cudaError_t launch_route_plan(int T, const Dims& D, const RouteWs& ws, cudaStream_t s) {
+cudaError_t launch_route_plan_scatter(int T, const Dims& D, const int32_t* topk_idx,
+                                      int32_t* perm, const RouteWs& ws, cudaStream_t s) {
   // down units cover 256 outputs (two 128-row weight tiles; the last may have one)
-  PlanArgs p{T, (T + kBlockTokens - 1) / kBlockTokens, D.f / kMTile, D.fs / kMTile,
-             (D.d + 2 * kMTile - 1) / (2 * kMTile)};
-  return launch_pdl(route_plan_kernel, dim3(1), dim3(256), 0, s, p, ws);
-}
-
-cudaError_t launch_route_scatter(int T, const int32_t* topk_idx, int32_t* perm,
-                                 const RouteWs& ws, cudaStream_t s) {
   const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
+  PlanArgs p{T, nblk, D.f / kMTile, D.fs / kMTile, (D.d + 2 * kMTile - 1) / (2 * kMTile)};
+  if (nblk <= kFusedPlanBlocks)
+    return launch_pdl(route_plan_scatter_kernel, dim3(nblk), dim3(256), 0, s, p, topk_idx, perm,
+                      ws);
+  cudaError_t e = launch_pdl(route_plan_kernel, dim3(1), dim3(256), 0, s, p, ws);
+  if (e != cudaSuccess) return e;
   return launch_pdl(route_scatter_kernel, dim3(nblk), dim3(128), 0, s, T, topk_idx, perm, ws);
 }
 

@@ -146,6 +146,18 @@ def test_prefill_sweep_sizes(T):
     assert_close(got["y"][toks], oracle_outputs(c, toks), f"sweep T={T}")
 
 
+# The plan and scatter run as one launch up to 128 token blocks (T <= 16384) and as two
+# launches above; both sides of that switch, routing checked on sampled tokens plus the
+# counting-sort invariants over every token.
+@pytest.mark.parametrize("T", [16384, 16385, 32768])
+def test_prefill_plan_paths(T):
+    c = build_case("plan-paths", d=512, f=128, fs=128, T=T, seed=21, full_host=False)
+    got = _run(c, moe.MOE_SCHEDULE_AUTO)
+    toks = sample_tokens(T, n_edge=16, stride=251)
+    _check_routing(c, got, toks)
+    assert_close(got["y"][toks], oracle_outputs(c, toks), f"plan paths T={T}")
+
+
 # ---------------------------------------------------------------- API behaviour on the GPU
 
 def test_deterministic_and_host_entry_point():
