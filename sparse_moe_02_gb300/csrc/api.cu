@@ -335,7 +335,7 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
                                             h->ys, h->sms, s))))
     return st;
   if ((st = prof_mark(h, s, 3))) return st;
-  if ((st = cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, s))))
+  if ((st = cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, h->sms, s))))
     return st;
   return prof_finish_call(h, s, 4);
 }

@@ -394,54 +394,128 @@ __global__ void __launch_bounds__(kXThreads, 1)
 
 // ---------------------------------------------------------------- combine
 
-// One block per token, one thread per 8 consecutive outputs (16-byte loads of ys rows).
-// acc = sum over j = 0..7 (ascending expert id) of w_j * ys[row_j], then + ys[shared row],
-// in fp32, rounded once to bf16.
-__global__ void __launch_bounds__(256) combine_kernel(int d, const float* topk_w,
-                                                      const int32_t* prow,
-                                                      const __nv_bfloat16* ys,
-                                                      __nv_bfloat16* y) {
-  pdl_wait();
-  const int t = blockIdx.x;
-  float w[8];
-  int r[9];
+constexpr int kCbCols = 2048;               // output columns per combine unit (256 threads x 8)
+constexpr int kCbStages = 6;
+constexpr int kCbStage = 9 * kCbCols * 2;   // the nine ys rows of one unit (36 KB)
+constexpr int kCbThreads = 288;             // warps 0-7 combine, warp 8 copies
+constexpr int kCbSmem = kCbStages * kCbStage + 256;
+
+// y[t] = sum over j = 0..7 (ascending expert id) of w_j * ys[prow[t][j]], then
+// + ys[prow[t][8]] (the shared expert), in fp32, rounded once to bf16.
+// Persistent blocks (one per SM) walk the units (token t, slice of up to 2048 columns) in a
+// static round robin.  Warp 8 stages the unit's nine ys rows in shared memory with bulk async
+// copies (one row per lane, six units in flight, so that enough bytes are in flight to cover
+// the HBM latency), and the eight combine warps take 8 consecutive outputs per thread.
+__global__ void __launch_bounds__(kCbThreads, 1)
+    combine_kernel(int T, int d, const float* topk_w, const int32_t* prow,
+                   const __nv_bfloat16* ys, __nv_bfloat16* y, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kCbStages * kCbStage);
+  uint64_t* empty = full + kCbStages;
+  __shared__ int s_fail;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kCbStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 8);
+    }
+    s_fail = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();  // prow, topk_w and ys come from earlier kernels on the stream
+  const int nslice = (d + kCbCols - 1) / kCbCols;
+  const int n_units = T * nslice;
+  const int G = (int)gridDim.x;
+  int k = 0;
+  if (warp == 8) {
+    const uint64_t pol = policy_evict_first();  // last use of ys
+    // the row indices of three units are loaded at once (lane 9 i + j: row j of unit i), one
+    // batch ahead of the copies, so the copy issue never waits on them
+    const int bi = lane / 9, bj = lane % 9;
+    auto rows_of = [&](int ub) {
+      const int u = ub + bi * G;
+      return lane < 27 && u < n_units ? __ldg(prow + (size_t)(u / nslice) * 9 + bj) : 0;
+    };
+    int rcur = rows_of(blockIdx.x);
+    bool ok = true;
+    for (int ub = blockIdx.x; ok && ub < n_units; ub += 3 * G) {
+      const int rnext = rows_of(ub + 3 * G);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) w[j] = topk_w[(size_t)t * kTopK + j];
-#pragma unroll
-  for (int j = 0; j < 9; ++j) r[j] = prow[(size_t)t * 9 + j];
-  const uint64_t pol_last = policy_evict_first();  // last use of ys
-  for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 9; ++j) {
-      const uint4 v = ld_u4_hint(ys + (size_t)r[j] * d + c * 8, pol_last);
-      const float wj = j < 8 ? w[j] : 1.0f;
-      const uint32_t p[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] += wj * bf16_lo(p[i]);
-        acc[2 * i + 1] += wj * bf16_hi(p[i]);
+      for (int i = 0; i < 3; ++i) {
+        const int u = ub + i * G;
+        if (u >= n_units) break;
+        const int r = __shfl_sync(0xffffffffu, rcur, i * 9 + (lane < 9 ? lane : 0));
+        const int st = k % kCbStages;
+        const int c0 = (u % nslice) * kCbCols;
+        const int cols = min(kCbCols, d - c0);
+        ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((k / kCbStages) & 1) ^ 1, err));
+        if (!ok) { s_fail = 1; break; }
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], 9u * cols * 2);
+        __syncwarp();
+        if (lane < 9)
+          bulk_load(smem + st * kCbStage + lane * (kCbCols * 2), ys + (size_t)r * d + c0,
+                    (uint32_t)cols * 2, &full[st], pol);
+        ++k;
       }
+      rcur = rnext;
     }
-    uint4 o;
-    uint32_t* po = reinterpret_cast<uint32_t*>(&o);
+  } else {
+    const int c = threadIdx.x * 8;
+    for (int u = blockIdx.x; u < n_units; u += G, ++k) {
+      const int st = k % kCbStages;
+      const int t = u / nslice, c0 = (u % nslice) * kCbCols;
+      const int cols = min(kCbCols, d - c0);
+      const float4 wa = __ldg(reinterpret_cast<const float4*>(topk_w + (size_t)t * kTopK));
+      const float4 wb = __ldg(reinterpret_cast<const float4*>(topk_w + (size_t)t * kTopK) + 1);
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (k / kCbStages) & 1, err));
+      if (!ok) { s_fail = 1; break; }
+      if (c < cols) {
+        const float w[9] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w, 1.0f};
+        const uint8_t* row = smem + st * kCbStage + c * 2;
+        float acc[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-      po[i] = *reinterpret_cast<uint32_t*>(&b2);
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+          const uint4 v = *reinterpret_cast<const uint4*>(row + j * (kCbCols * 2));
+          const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] += w[j] * bf16_lo(p[i]);
+            acc[2 * i + 1] += w[j] * bf16_hi(p[i]);
+          }
+        }
+        uint4 o;
+        uint32_t* po = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+          po[i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        *reinterpret_cast<uint4*>(y + (size_t)t * d + c0 + c) = o;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
     }
-    *reinterpret_cast<uint4*>(y + (size_t)t * d + c * 8) = o;
   }
   pdl_trigger();
+  __syncthreads();
+  // after a timed-out wait, let the copies already issued land (bounded) before exiting
+  if (s_fail && warp == 8 && lane == 0)
+    for (int kk = k > kCbStages ? k - kCbStages : 0; kk < k; ++kk)
+      mbar_wait(&full[kk % kCbStages], (kk / kCbStages) & 1, err);
 }
 
 }  // namespace
 
 cudaError_t prepare_expert_kernels() {
-  return cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kXSmem);
+  cudaError_t e = cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kXSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kCbSmem);
 }
 
 cudaError_t launch_experts(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
@@ -457,9 +531,10 @@ cudaError_t launch_experts(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
 }
 
 cudaError_t launch_combine(int T, const Dims& D, const float* topk_w, const RouteWs& ws,
-                           const __nv_bfloat16* ys, __nv_bfloat16* y, cudaStream_t s) {
-  return launch_pdl(combine_kernel, dim3(T), dim3(256), 0, s, D.d, topk_w,
-                    (const int32_t*)ws.prow, ys, y);
+                           const __nv_bfloat16* ys, __nv_bfloat16* y, int grid, cudaStream_t s) {
+  const int units = T * ((D.d + kCbCols - 1) / kCbCols);
+  return launch_pdl(combine_kernel, dim3(units < grid ? units : grid), dim3(kCbThreads), kCbSmem,
+                    s, T, D.d, topk_w, (const int32_t*)ws.prow, ys, y, ws.err);
 }
 
 }  // namespace moe

@@ -97,9 +97,10 @@ cudaError_t launch_experts(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
                            const RouteWs& ws, __nv_bfloat16* h, __nv_bfloat16* ys, int grid,
                            cudaStream_t s);
 
-// y[t] = sum_j w[t][j] ys[prow[t][j]] + ys[prow[t][8]] in fp32, rounded once to bf16.
+// y[t] = sum_j w[t][j] ys[prow[t][j]] + ys[prow[t][8]] in fp32, rounded once to bf16
+// (persistent: at most `grid` blocks, one per SM).
 cudaError_t launch_combine(int T, const Dims& D, const float* topk_w, const RouteWs& ws,
-                           const __nv_bfloat16* ys, __nv_bfloat16* y, cudaStream_t s);
+                           const __nv_bfloat16* ys, __nv_bfloat16* y, int grid, cudaStream_t s);
 
 // ---------------------------------------------------------------- batch-1 decode path
 
