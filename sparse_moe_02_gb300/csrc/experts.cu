@@ -147,8 +147,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
       prefetch_tensormap(&tm_h);
       prefetch_tensormap(&tm_wd);
       prefetch_tensormap(&tm_wsd);
-      const uint64_t stream_w = policy_evict_first();  // each weight tile is read once
-      const uint64_t keep_h = policy_evict_last();
+      const uint64_t stream_w = policy_evict_first();  // a routed weight tile is read once
+      const uint64_t keep_h = policy_evict_last();     // h rows; the shared expert's weights
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -177,12 +177,13 @@ __global__ void __launch_bounds__(kXThreads, 1)
           const CUtensorMap* mg = shared ? &tm_wsg : &tm_wg;
           const CUtensorMap* mu = shared ? &tm_wsu : &tm_wu;
           const int arow = (shared ? 0 : U.g * a.f) + U.mt * kMTile;
+          const uint64_t pw = shared ? keep_h : stream_w;
           for (int kb = 0; kb < a.d / kBK; ++kb) {
             if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
             uint8_t* st = smem + stage * kXStage;
             mbar_arrive_expect_tx(&full[stage], 2 * kTileA);
-            tma_load_2d(st, mg, &full[stage], kb * kBK, arow, stream_w);
-            tma_load_2d(st + kTileA, mu, &full[stage], kb * kBK, arow, stream_w);
+            tma_load_2d(st, mg, &full[stage], kb * kBK, arow, pw);
+            tma_load_2d(st + kTileA, mu, &full[stage], kb * kBK, arow, pw);
             if (++stage == kXStages) { stage = 0; ph ^= 1; }
           }
         } else {
@@ -214,8 +215,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
             if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
             uint8_t* st = smem + stage * kXStage;
             mbar_arrive_expect_tx(&full[stage], bytes);
-            tma_load_2d(st, mw, &full[stage], kb * kBK, arow, stream_w);
-            if (two) tma_load_2d(st + kTileA, mw, &full[stage], kb * kBK, arow + kMTile, stream_w);
+            const uint64_t pw = shared ? keep_h : stream_w;
+            tma_load_2d(st, mw, &full[stage], kb * kBK, arow, pw);
+            if (two) tma_load_2d(st + kTileA, mw, &full[stage], kb * kBK, arow + kMTile, pw);
             for (int r = 0; r < N / 16; ++r)
               tma_load_2d(st + 2 * kTileA + r * 2048, &tm_h, &full[stage], kb * kBK,
                           U.p0 + 16 * r, keep_h);

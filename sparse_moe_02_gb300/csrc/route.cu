@@ -296,9 +296,10 @@ struct GroupTable {
 // Thread e (all 256 threads call it) with cnt = assignments to expert e: the exclusive scan into
 // offsets, the padded group starts (groups start on 16-row boundaries; the shared expert's T rows
 // follow the routed groups), and the unit bookkeeping: each group is cut into ceil(n / 192)
-// nearly equal chunks of rows, and each chunk is paired with every weight row tile.  Units are
-// listed shared group first, then experts ascending; inside a group, weight tile major and chunk
-// minor, so units that read the same weights are adjacent.  The writer block also stores the
+// nearly equal chunks of rows, and each chunk is paired with every weight row tile.  Routed
+// units are listed by expert ascending; inside a group, weight tile major and chunk minor, so
+// units that read the same weights are adjacent (the shared group's units are spread among
+// them, see plan_units).  The writer block also stores the
 // global offsets, group starts and unit counts, zeroes the schedule counter, the chunk counters
 // and the grow entries of padding rows.
 __device__ void plan_groups(const PlanArgs& p, int cnt, GroupTable& G, const RouteWs& ws,
@@ -362,17 +363,26 @@ __device__ __forceinline__ int find_group(const int* start, int u) {
 }
 
 // Writes units [lo, hi) of one list (gate/up: dn = false) from the group table: consecutive
-// threads, consecutive units; the group of a unit found by binary search over the group starts.
+// threads, consecutive units.  The shared group's units (chunk major, weight tile minor) are
+// spread evenly through the list -- position u holds a shared unit when the count
+// floor((u + 1) s / n) of shared units up to u grows there -- so that at every point of the
+// schedule most blocks stream routed weights from HBM while a few run the shared expert,
+// whose weights stay in L2; the routed units keep their order (group of a routed unit found by
+// binary search over the group starts).
 __device__ void plan_units(const GroupTable& G, Unit* units, bool dn, int lo, int hi, int T) {
   const int* start = dn ? G.dn0 : G.gu0;
-  const int n_s = dn ? G.dn_s : G.gu_s;
+  const long long n = dn ? G.n_dn : G.n_gu;
+  const int ns = dn ? G.dn_s : G.gu_s;
+  const int mts = G.nch_s ? ns / G.nch_s : 1;  // weight tiles per shared chunk
   for (int u = lo + (int)threadIdx.x; u < hi; u += blockDim.x) {
-    if (u < n_s) {
-      const int mt = u / G.nch_s, c = u % G.nch_s;
+    const int upto = (int)(((long long)u + 1) * ns / n), before = (int)((long long)u * ns / n);
+    if (upto > before) {
+      const int c = before / mts, mt = before % mts;
       units[u] = Unit{kE, G.p_shared + c * G.cs_s, min(G.cs_s, T - c * G.cs_s), mt, c};
     } else {
-      const int g = find_group(start, u), l = u - start[g], n = G.nch[g];
-      const int mt = l / n, c = l % n, cs = G.cs[g];
+      const int v = u - upto + ns;  // position in the list with the shared units first
+      const int g = find_group(start, v), l = v - start[g], nc = G.nch[g];
+      const int mt = l / nc, c = l % nc, cs = G.cs[g];
       units[u] = Unit{g, G.poff[g] + c * cs, min(cs, G.cnt[g] - c * cs), mt, G.cid0[g] + c};
     }
   }
