@@ -198,8 +198,8 @@ bool use_gemv(const moe_handle_s* h, int T) {
 // The routing chain of the tensor-core schedule.
 int run_route_gemm(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w,
                    int32_t* offsets, int32_t* perm, cudaStream_t s, bool prof) {
-  CUtensorMap tm_x;  // the router loads x in quarter tiles of 32 rows (multicast in a cluster)
-  if (!encode_2d(&tm_x, x, h->D.d, T, moe::kBK, moe::kBlockTokens / 4)) return MOE_ERR_CUDA;
+  CUtensorMap tm_x;  // the router loads x in tiles of 128 rows x 64
+  if (!encode_2d(&tm_x, x, h->D.d, T, moe::kBK, moe::kBlockTokens)) return MOE_ERR_CUDA;
   moe::RouteWs w = h->rws;
   if (offsets) w.offsets = offsets;
   int st;
@@ -262,7 +262,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
   if ((st = cuda_status(cudaMemset(h->ws, 0, total)))) return fail(st);
 
   const Dims& D = h->D;
-  bool ok = encode_2d(&h->tm_wr, w->w_router, D.d, kE, moe::kBK, kE / 4) &&
+  bool ok = encode_2d(&h->tm_wr, w->w_router, D.d, kE, moe::kBK, kE) &&
             encode_2d(&h->tm_wg, w->w_gate, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wu, w->w_up, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wsg, w->ws_gate, D.d, D.fs, moe::kBK, moe::kMTile) &&

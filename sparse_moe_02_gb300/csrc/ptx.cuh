@@ -157,6 +157,18 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
+
+// Adds v to the 32-bit word at a shared::cluster address (no value returned).
+__device__ __forceinline__ void red_cluster_add(uint32_t addr, int v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Bulk (non-tensor) copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global to shared memory, completing as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,

@@ -13,22 +13,24 @@ namespace {
 
 // ---------------------------------------------------------------- router GEMM + top-8
 
-// A cluster of four blocks per 128 tokens: block r computes the logits of experts
-// [64r, 64r + 64) (tcgen05, M = 128 tokens, N = 64 experts, K = d).  The x tile is shared:
-// each block loads a quarter of its rows and multicasts it to the four.  Each block keeps its
-// 8 largest logits per token and writes them into the leader block's shared memory; the leader
-// merges the 4 x 8 candidates, applies the softmax and counts the histogram.
+// A cluster of four blocks per 128 tokens splits the reduction: block r multiplies the
+// k-blocks r, r + 4, r + 8, ... of x and the router matrix (tcgen05, M = 128 tokens, N = 256
+// experts) into a partial logit tile in TMEM, so each block streams a quarter of the tile's
+// inputs.  The partials are summed through distributed shared memory: the warps reading TMEM
+// lane quadrant q send those rows (tokens 32q .. 32q + 31) to block q, which then holds all
+// four partials of its 32 tokens, adds them in block order and selects each token's top 8
+// with eight threads per token.
 constexpr int kRtCluster = 4;
-constexpr int kRtN = kE / kRtCluster;                 // experts per block
-constexpr int kRtStages = 6;
+constexpr int kRtStages = 4;
 constexpr int kRtA = kBlockTokens * kBK * 2;          // x tile: 128 tokens x 64 (16 KB)
-constexpr int kRtASlice = kRtA / kRtCluster;          // rows loaded (and multicast) per block
-constexpr int kRtB = kRtN * kBK * 2;                  // router tile: 64 experts x 64 (8 KB)
+constexpr int kRtB = kE * kBK * 2;                    // router tile: 256 experts x 64 (32 KB)
 constexpr int kRtStage = kRtA + kRtB;
 constexpr int kRtThreads = 320;                       // producer, MMA, 8 epilogue warps
-constexpr int kRtCand = kBlockTokens * kRtCluster * 8;  // leader: 4 lists of 8 per token
-constexpr int kRtHalf = kBlockTokens * 2 * 8;           // each block: 2 half-lists per token
-constexpr int kRtSmem = kRtStages * kRtStage + (kRtCand + kRtHalf) * 8 + 1024 + 2048;
+constexpr int kRtTok = kBlockTokens / kRtCluster;     // tokens owned per block
+constexpr int kRtRow = kE + 4;                        // floats per received partial row (padded)
+constexpr int kRtRecv = kRtCluster * kRtTok * kRtRow * 4;
+static_assert(kRtRecv <= kRtStages * kRtStage, "received partials reuse the drained ring");
+constexpr int kRtSmem = kRtStages * kRtStage + 1024 + 2048;
 
 struct RouterArgs {
   const float* bias;
@@ -39,47 +41,61 @@ struct RouterArgs {
   int* err;
 };
 
-// Keeps the 8 largest (value, id) pairs in v/id, sorted by value descending; among equal
-// values the earlier-inserted pair stays ahead (callers insert ids in ascending order).
+// (v, e) ranks above (w, f): larger value, or equal value and lower expert id.
+__device__ __forceinline__ bool ranks_above(float v, int e, float w, int f) {
+  return v > w || (v == w && e < f);
+}
+
+__device__ __forceinline__ void cas_pair(float& v0, int& i0, float& v1, int& i1) {
+  const bool sw = ranks_above(v1, i1, v0, i0);
+  const float a = sw ? v1 : v0, b = sw ? v0 : v1;
+  const int ia = sw ? i1 : i0, ib = sw ? i0 : i1;
+  v0 = a; v1 = b; i0 = ia; i1 = ib;
+}
+
+// Inserts (x, e) into the descending list v/id (8 entries) when it ranks above the last one.
+// Values arrive with ascending e, so an equal value stays behind the entries already held.
+// The eight comparisons are independent (collected as bits: held as an array of bools, this
+// was miscompiled by nvcc 13.0 once fully unrolled); each slot then takes its own value, its
+// upper neighbour's or x.
 __device__ __forceinline__ void top8_insert(float (&v)[8], int (&id)[8], float x, int e) {
-  if (x > v[7]) {
-    v[7] = x;
-    id[7] = e;
+  uint32_t m = 0;
 #pragma unroll
-    for (int i = 7; i > 0; --i) {
-      if (v[i] > v[i - 1]) {
-        float tv = v[i]; v[i] = v[i - 1]; v[i - 1] = tv;
-        int ti = id[i]; id[i] = id[i - 1]; id[i - 1] = ti;
-      }
-    }
+  for (int i = 0; i < 8; ++i) m |= (x > v[i] ? 1u : 0u) << i;
+#pragma unroll
+  for (int i = 7; i > 0; --i) {
+    const bool ci = (m >> i) & 1u, cp = (m >> (i - 1)) & 1u;
+    v[i] = ci ? (cp ? v[i - 1] : x) : v[i];
+    id[i] = ci ? (cp ? id[i - 1] : e) : id[i];
+  }
+  if (m & 1u) {
+    v[0] = x;
+    id[0] = e;
   }
 }
 
-// The 8 largest of L lists of 8 (each sorted by value descending, ids ascending among equal
-// values; list l holding lower ids than list l + 1): eight steps, each taking the largest
-// head, the lower list on equal values -- so ties still go to the lower id.
-template <int L>
-__device__ __forceinline__ void merge_top8(const float* cv, const int* ci, float (&v)[8],
-                                           int (&id)[8]) {
-  int pos[L];
+// Merges the descending list of the lane `o` apart (xor) into this lane's: the better of
+// entry i and the partner's entry 7 - i keeps the top 8 of both as a bitonic sequence, which
+// three half-cleaner stages sort.
+__device__ __forceinline__ void top8_merge_xor(float (&v)[8], int (&id)[8], int o) {
+  float w[8];
+  int f[8];
 #pragma unroll
-  for (int l = 0; l < L; ++l) pos[l] = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    float bv = -INFINITY;
-    int bl = 0;
-#pragma unroll
-    for (int l = 0; l < L; ++l) {
-      const float hv = pos[l] < 8 ? cv[l * 8 + pos[l]] : -INFINITY;
-      if (hv > bv) { bv = hv; bl = l; }
-    }
-    int bi = 0;
-#pragma unroll
-    for (int l = 0; l < L; ++l)
-      if (l == bl) { bi = ci[l * 8 + pos[l]]; pos[l] += 1; }
-    v[k] = bv;
-    id[k] = bi;
+  for (int i = 0; i < 8; ++i) {
+    w[i] = __shfl_xor_sync(0xffffffffu, v[7 - i], o);
+    f[i] = __shfl_xor_sync(0xffffffffu, id[7 - i], o);
   }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool tk = ranks_above(w[i], f[i], v[i], id[i]);
+    v[i] = tk ? w[i] : v[i];
+    id[i] = tk ? f[i] : id[i];
+  }
+#pragma unroll
+  for (int h = 4; h > 0; h >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & h) == 0) cas_pair(v[i], id[i], v[i + h], id[i + h]);
 }
 
 __global__ void __launch_bounds__(kRtThreads, 1)
@@ -87,11 +103,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                        const __grid_constant__ CUtensorMap tm_wr, RouterArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  float* cand_v = reinterpret_cast<float*>(smem + kRtStages * kRtStage);  // [128][4][8] leader
-  int* cand_i = reinterpret_cast<int*>(cand_v + kRtCand);
-  float* half_v = reinterpret_cast<float*>(cand_i + kRtCand);             // [128][2][8]
-  int* half_i = reinterpret_cast<int*>(half_v + kRtHalf);
-  uint64_t* full = reinterpret_cast<uint64_t*>(half_i + kRtHalf);
+  float* recv = reinterpret_cast<float*>(smem);  // [src block][32 tokens][kRtRow], after the ring
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtStages * kRtStage);
   uint64_t* empty = full + kRtStages;
   uint64_t* tfull = empty + kRtStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
@@ -101,22 +114,23 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   const uint32_t rank = cluster_rank();
   const int blk = (int)cluster_id_x();  // 128-token block
   const int KB = a.d / kBK;
+  const int nk = KB > (int)rank ? (KB - (int)rank + kRtCluster - 1) / kRtCluster : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRtStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kRtCluster);  // released by the MMA of every block of the cluster
+      mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kRtN);
+    tmem_alloc(tmem_slot, kE);
     tmem_relinquish();
   }
   for (int i = threadIdx.x; i < kE; i += blockDim.x) hist_s[i] = 0;
   tc_fence_before();
-  cluster_sync();  // barriers of every block initialised before any multicast lands
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // x (and the bias) may come from the previous kernel on the stream
@@ -125,125 +139,152 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&tm_x);
       prefetch_tensormap(&tm_wr);
-      const uint64_t keep = policy_evict_last();  // x and the router weights are re-read
+      const uint64_t keep = policy_evict_last();  // x is gathered again by the expert GEMMs
       int stage = 0;
       uint32_t ph = 0;
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int i = 0; i < nk; ++i) {
+        const int kb = (int)rank + kRtCluster * i;
         if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) break;
         uint8_t* st = smem + stage * kRtStage;
         mbar_arrive_expect_tx(&full[stage], kRtStage);
-        tma_load_2d_mc(st + rank * kRtASlice, &tm_x, &full[stage], kb * kBK,
-                       blk * kBlockTokens + (int)rank * (kBlockTokens / kRtCluster),
-                       (uint16_t)((1u << kRtCluster) - 1), keep);
-        tma_load_2d(st + kRtA, &tm_wr, &full[stage], kb * kBK, (int)rank * kRtN, keep);
+        tma_load_2d(st, &tm_x, &full[stage], kb * kBK, blk * kBlockTokens, keep);
+        tma_load_2d(st + kRtA, &tm_wr, &full[stage], kb * kBK, 0, keep);
         if (++stage == kRtStages) { stage = 0; ph ^= 1; }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, kRtN);
+    if (lane == 0 && nk > 0) {
+      const uint32_t idesc = idesc_bf16(128, kE);
       int stage = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int i = 0; i < nk; ++i) {
         if (!mbar_wait(&full[stage], ph, a.err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + stage * kRtStage), sb = sa + kRtA;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
           mma_bf16(tmem, sdesc_k128(sa + kk * 32), sdesc_k128(sb + kk * 32), idesc,
-                   (kb | kk) != 0);
-        mma_commit_mc(&empty[stage], (uint16_t)((1u << kRtCluster) - 1));
+                   (i | kk) != 0);
+        mma_commit(&empty[stage]);
         if (++stage == kRtStages) { stage = 0; ph ^= 1; }
       }
       if (ok) mma_commit(tfull);
     }
-  } else {
-    // epilogue: thread = one token row and one half (32) of this block's 64 experts
-    const int q = warp & 3, half = (warp - 2) >> 2;
-    const int m = q * 32 + lane;
-    const bool have = mbar_wait(tfull, 0, a.err);
-    tc_fence_after();
-    float v[8];
-    int id[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { v[i] = -INFINITY; id[i] = 0; }
-    if (have) {
-#pragma unroll
-      for (int c0 = 0; c0 < kRtN / 2; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * (kRtN / 2) + c0), r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = (int)rank * kRtN + half * (kRtN / 2) + c0 + i;
-          float x = __uint_as_float(r[i]);
-          if (a.bias) x += __ldg(a.bias + e);
-          top8_insert(v, id, x, e);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      half_v[(m * 2 + half) * 8 + j] = v[j];
-      half_i[(m * 2 + half) * 8 + j] = id[j];
-    }
-    named_sync(1, 8 * 32);  // both halves of every token listed
-    if (half == 0) {
-      merge_top8<2>(half_v + m * 16, half_i + m * 16, v, id);
-      const uint32_t dv = map_shared(cand_v + m * (kRtCluster * 8) + rank * 8, 0);
-      const uint32_t di = map_shared(cand_i + m * (kRtCluster * 8) + rank * 8, 0);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        st_cluster_f32(dv + 4 * j, v[j]);
-        st_cluster_s32(di + 4 * j, id[j]);
-      }
-    }
   }
+  // the epilogue warps wait for this block's MMAs: after the cluster barrier every block's
+  // ring is drained and may receive the partials
+  bool have = true;
+  if (warp >= 2 && nk > 0) have = mbar_wait(tfull, 0, a.err);
   tc_fence_before();
-  cluster_sync();  // candidates of all four blocks are in the leader's shared memory
+  cluster_sync();
+  tc_fence_after();
 
-  if (rank == 0 && warp >= 2 && ((warp - 2) >> 2) == 0) {
-    const int q = warp & 3;
-    const int m = q * 32 + lane;
-    const int t = blk * kBlockTokens + m;
+  if (warp >= 2) {
+    // send: TMEM lanes 32q .. 32q + 31 (tokens) x columns [128 half, +128) to block q
+    const int q = warp & 3, half = (warp - 2) >> 2;
+    const uint32_t dst = map_shared(recv + ((int)rank * kRtTok + lane) * kRtRow + half * 128, q);
+    uint32_t r[128];
+    if (nk > 0 && have) {
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 16)
+        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * 128 + c0),
+                  *reinterpret_cast<uint32_t(*)[16]>(r + c0));
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int i = 0; i < 128; ++i) r[i] = 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      st_cluster_v4(dst + (uint32_t)j * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+  }
+  cluster_sync();  // all partials of this block's 32 tokens have arrived
+
+  if (warp >= 2) {
+    // select: thread (token tl, part p) takes experts 4p + 32i + j (i < 8, j < 4).  The sums
+    // go back into partial slot 0 (each thread owns those words).  Any value below
+    // tau = min over the 8 parts of the part's largest value has at least 8 values of the token
+    // above it, so only values >= tau are inserted: a few per thread, taken one at a time.
+    const int tid = threadIdx.x - 64, tl = tid >> 3, p = tid & 7;
+    const int t = blk * kBlockTokens + (int)rank * kRtTok + tl;
+    float* row = recv + tl * kRtRow;
+    float sv[32];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e0 = 4 * p + 32 * i;
+      float4 s = *reinterpret_cast<const float4*>(row + e0);
+#pragma unroll
+      for (int src = 1; src < kRtCluster; ++src) {
+        const float4 u = *reinterpret_cast<const float4*>(recv + (src * kRtTok + tl) * kRtRow + e0);
+        s.x += u.x; s.y += u.y; s.z += u.z; s.w += u.w;
+      }
+      if (a.bias) {
+        const float4 bb = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
+        s.x += bb.x; s.y += bb.y; s.z += bb.z; s.w += bb.w;
+      }
+      *reinterpret_cast<float4*>(row + e0) = s;
+      sv[4 * i] = s.x; sv[4 * i + 1] = s.y; sv[4 * i + 2] = s.z; sv[4 * i + 3] = s.w;
+      mx = fmaxf(mx, fmaxf(fmaxf(s.x, s.y), fmaxf(s.z, s.w)));
+    }
+    float tau = mx;
+    tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, 1));
+    tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, 2));
+    tau = fminf(tau, __shfl_xor_sync(0xffffffffu, tau, 4));
+    uint32_t pass = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) pass |= (sv[j] >= tau ? 1u : 0u) << j;
     float v[8];
     int id[8];
-    merge_top8<kRtCluster>(cand_v + m * (kRtCluster * 8), cand_i + m * (kRtCluster * 8), v, id);
-    // list the kept experts in ascending id
 #pragma unroll
-    for (int i = 0; i < 7; ++i)
+    for (int i = 0; i < 8; ++i) { v[i] = -INFINITY; id[i] = 0x7fffffff; }
+    while (__any_sync(0xffffffffu, pass != 0)) {
+      if (pass) {
+        const int j = __ffs(pass) - 1;  // ascending j: ascending expert id
+        pass &= pass - 1;
+        const int e = 4 * p + 32 * (j >> 2) + (j & 3);
+        top8_insert(v, id, row[e], e);
+      }
+    }
+    top8_merge_xor(v, id, 1);
+    top8_merge_xor(v, id, 2);
+    top8_merge_xor(v, id, 4);
+    if (p == 0 && t < a.T) {
+      // list the kept experts in ascending id; softmax over the kept logits
 #pragma unroll
-      for (int j = 0; j < 7 - i; ++j)
-        if (id[j] > id[j + 1]) {
-          int ti = id[j]; id[j] = id[j + 1]; id[j + 1] = ti;
-          float tv = v[j]; v[j] = v[j + 1]; v[j + 1] = tv;
-        }
-    float mx = v[0];
+      for (int i = 0; i < 7; ++i)
 #pragma unroll
-    for (int j = 1; j < 8; ++j) mx = fmaxf(mx, v[j]);
-    float ex[8], s = 0.f;
+        for (int j = 0; j < 7 - i; ++j)
+          if (id[j] > id[j + 1]) {
+            int ti = id[j]; id[j] = id[j + 1]; id[j + 1] = ti;
+            float tv = v[j]; v[j] = v[j + 1]; v[j + 1] = tv;
+          }
+      float mx = v[0];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) { ex[j] = __expf(v[j] - mx); s += ex[j]; }
-    if (t < a.T) {
+      for (int j = 1; j < 8; ++j) mx = fmaxf(mx, v[j]);
+      float ex[8], sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { ex[j] = __expf(v[j] - mx); sum += ex[j]; }
       int4* pi = reinterpret_cast<int4*>(a.topk_idx + (size_t)t * kTopK);
       float4* pw = reinterpret_cast<float4*>(a.topk_w + (size_t)t * kTopK);
       pi[0] = make_int4(id[0], id[1], id[2], id[3]);
       pi[1] = make_int4(id[4], id[5], id[6], id[7]);
-      pw[0] = make_float4(ex[0] / s, ex[1] / s, ex[2] / s, ex[3] / s);
-      pw[1] = make_float4(ex[4] / s, ex[5] / s, ex[6] / s, ex[7] / s);
+      pw[0] = make_float4(ex[0] / sum, ex[1] / sum, ex[2] / sum, ex[3] / sum);
+      pw[1] = make_float4(ex[4] / sum, ex[5] / sum, ex[6] / sum, ex[7] / sum);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) atomicAdd(&hist_s[id[j]], 1);
+      for (int j = 0; j < 8; ++j) red_cluster_add(map_shared(hist_s + id[j], 0), 1);
     }
-    named_sync(2, 128);  // the four merging warps
-    const int et = threadIdx.x - 64;
-    a.hist[(size_t)blk * kE + et] = hist_s[et];
-    a.hist[(size_t)blk * kE + et + 128] = hist_s[et + 128];
+  }
+  cluster_sync();  // the leader's histogram is complete
+  if (rank == 0 && warp >= 2) {
+    const int e = threadIdx.x - 64;
+    a.hist[(size_t)blk * kE + e] = hist_s[e];
   }
   pdl_trigger();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, kRtN);
+  if (warp == 1) tmem_dealloc(tmem, kE);
 }
 
 // ---------------------------------------------------------------- plan
