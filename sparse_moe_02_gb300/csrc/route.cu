@@ -16,10 +16,11 @@ namespace {
 // A cluster of four blocks per 128 tokens splits the reduction: block r multiplies the
 // k-blocks r, r + 4, r + 8, ... of x and the router matrix (tcgen05, M = 128 tokens, N = 256
 // experts) into a partial logit tile in TMEM, so each block streams a quarter of the tile's
-// inputs.  The partials are summed through distributed shared memory: the warps reading TMEM
-// lane quadrant q send those rows (tokens 32q .. 32q + 31) to block q, which then holds all
-// four partials of its 32 tokens, adds them in block order and selects each token's top 8
-// with eight threads per token.
+// inputs.  The partials are summed in the block that owns the tokens: TMEM lane quadrant q
+// (tokens 32q .. 32q + 31) belongs to block q.  Each block writes its three foreign quadrants
+// to shared memory and sends each to its owner with one bulk copy (distributed shared memory,
+// completing on the owner's mbarrier); the owner adds the four partials in block order and
+// selects each token's top 8 with eight threads per token.
 constexpr int kRtCluster = 4;
 constexpr int kRtStages = 4;
 constexpr int kRtA = kBlockTokens * kBK * 2;          // x tile: 128 tokens x 64 (16 KB)
@@ -27,10 +28,19 @@ constexpr int kRtB = kE * kBK * 2;                    // router tile: 256 expert
 constexpr int kRtStage = kRtA + kRtB;
 constexpr int kRtThreads = 320;                       // producer, MMA, 8 epilogue warps
 constexpr int kRtTok = kBlockTokens / kRtCluster;     // tokens owned per block
-constexpr int kRtRow = kE + 4;                        // floats per received partial row (padded)
-constexpr int kRtRecv = kRtCluster * kRtTok * kRtRow * 4;
-static_assert(kRtRecv <= kRtStages * kRtStage, "received partials reuse the drained ring");
-constexpr int kRtSmem = kRtStages * kRtStage + 1024 + 2048;
+constexpr int kRtSlot = kRtTok * kE * 4;              // one quadrant of partial logits (32 KB)
+// after the ring drains: received partials [4 source blocks] then outgoing quadrants [3]
+constexpr int kRtRecv = 0, kRtSend = kRtCluster * kRtSlot;
+constexpr int kRtArea = kRtSend + (kRtCluster - 1) * kRtSlot;
+constexpr int kRtBody = kRtArea > kRtStages * kRtStage ? kRtArea : kRtStages * kRtStage;
+constexpr int kRtSmem = kRtBody + 1024 + 2048;
+
+// Float e of token row `row` in a quadrant slot: rows of 256 floats whose 16-byte chunks are
+// XOR-swizzled by the row, so that a warp writing one chunk of 32 rows, or reading chunks of a
+// few rows, spreads over all banks.
+__device__ __forceinline__ float* slot_at(float* slot, int row, int e) {
+  return slot + row * kE + ((((e >> 2) ^ (row & 7))) << 2) + (e & 3);
+}
 
 struct RouterArgs {
   const float* bias;
@@ -103,11 +113,13 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                        const __grid_constant__ CUtensorMap tm_wr, RouterArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  float* recv = reinterpret_cast<float*>(smem);  // [src block][32 tokens][kRtRow], after the ring
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtStages * kRtStage);
+  float* recv = reinterpret_cast<float*>(smem + kRtRecv);  // [src block] slots, after the ring
+  float* send = reinterpret_cast<float*>(smem + kRtSend);  // [3] outgoing quadrants
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtBody);
   uint64_t* empty = full + kRtStages;
   uint64_t* tfull = empty + kRtStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  uint64_t* rfull = tfull + 1;  // the three foreign partials of this block's tokens arrived
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rfull + 1);
   int* hist_s = reinterpret_cast<int*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,7 +134,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
+    mbar_init(rfull, 1);
     fence_mbar_init();
+    mbar_arrive_expect_tx(rfull, (kRtCluster - 1) * kRtSlot);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kE);
@@ -172,18 +186,15 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       if (ok) mma_commit(tfull);
     }
   }
-  // the epilogue warps wait for this block's MMAs: after the cluster barrier every block's
-  // ring is drained and may receive the partials
-  bool have = true;
-  if (warp >= 2 && nk > 0) have = mbar_wait(tfull, 0, a.err);
-  tc_fence_before();
-  cluster_sync();
-  tc_fence_after();
-
+  // epilogue: TMEM quadrant q to the local slot of block q's partial (its own quadrant straight
+  // into the receive slot); after the cluster barrier every block's ring has drained, so the
+  // foreign quadrants may be copied into their owners' receive slots
   if (warp >= 2) {
-    // send: TMEM lanes 32q .. 32q + 31 (tokens) x columns [128 half, +128) to block q
     const int q = warp & 3, half = (warp - 2) >> 2;
-    const uint32_t dst = map_shared(recv + ((int)rank * kRtTok + lane) * kRtRow + half * 128, q);
+    const bool have = nk == 0 || mbar_wait(tfull, 0, a.err);
+    tc_fence_after();
+    float* dst = q == (int)rank ? recv + (int)rank * (kRtSlot / 4)
+                                : send + ((q - (int)rank + kRtCluster - 1) & 3) * (kRtSlot / 4);
     uint32_t r[128];
     if (nk > 0 && have) {
 #pragma unroll
@@ -197,34 +208,44 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      st_cluster_v4(dst + (uint32_t)j * 16, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+      *reinterpret_cast<uint4*>(slot_at(dst, lane, half * 128 + 4 * j)) =
+          make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    fence_proxy_async_smem();  // read next by the bulk copies
   }
-  cluster_sync();  // all partials of this block's 32 tokens have arrived
+  tc_fence_before();
+  cluster_sync();
+  if (warp >= 2 && warp < 2 + kRtCluster - 1 && lane == 0) {
+    const int s = warp - 2, q = ((int)rank + 1 + s) & 3;
+    bulk_s2cluster(map_shared(recv + (int)rank * (kRtSlot / 4), q), send + s * (kRtSlot / 4),
+                   kRtSlot, map_shared(rfull, q));
+    bulk_commit();
+  }
 
   if (warp >= 2) {
     // select: thread (token tl, part p) takes experts 4p + 32i + j (i < 8, j < 4).  The sums
-    // go back into partial slot 0 (each thread owns those words).  Any value below
+    // go back into receive slot 0 (each thread owns those words).  Any value below
     // tau = min over the 8 parts of the part's largest value has at least 8 values of the token
     // above it, so only values >= tau are inserted: a few per thread, taken one at a time.
     const int tid = threadIdx.x - 64, tl = tid >> 3, p = tid & 7;
     const int t = blk * kBlockTokens + (int)rank * kRtTok + tl;
-    float* row = recv + tl * kRtRow;
+    mbar_wait(rfull, 0, a.err);
     float sv[32];
     float mx = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e0 = 4 * p + 32 * i;
-      float4 s = *reinterpret_cast<const float4*>(row + e0);
+      float4 s = *reinterpret_cast<const float4*>(slot_at(recv, tl, e0));
 #pragma unroll
       for (int src = 1; src < kRtCluster; ++src) {
-        const float4 u = *reinterpret_cast<const float4*>(recv + (src * kRtTok + tl) * kRtRow + e0);
+        const float4 u =
+            *reinterpret_cast<const float4*>(slot_at(recv + src * (kRtSlot / 4), tl, e0));
         s.x += u.x; s.y += u.y; s.z += u.z; s.w += u.w;
       }
       if (a.bias) {
         const float4 bb = __ldg(reinterpret_cast<const float4*>(a.bias + e0));
         s.x += bb.x; s.y += bb.y; s.z += bb.z; s.w += bb.w;
       }
-      *reinterpret_cast<float4*>(row + e0) = s;
+      *reinterpret_cast<float4*>(slot_at(recv, tl, e0)) = s;
       sv[4 * i] = s.x; sv[4 * i + 1] = s.y; sv[4 * i + 2] = s.z; sv[4 * i + 3] = s.w;
       mx = fmaxf(mx, fmaxf(fmaxf(s.x, s.y), fmaxf(s.z, s.w)));
     }
@@ -244,7 +265,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         const int j = __ffs(pass) - 1;  // ascending j: ascending expert id
         pass &= pass - 1;
         const int e = 4 * p + 32 * (j >> 2) + (j & 3);
-        top8_insert(v, id, row[e], e);
+        top8_insert(v, id, *slot_at(recv, tl, e), e);
       }
     }
     top8_merge_xor(v, id, 1);
@@ -276,6 +297,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       for (int j = 0; j < 8; ++j) red_cluster_add(map_shared(hist_s + id[j], 0), 1);
     }
   }
+  if (warp >= 2 && warp < 2 + kRtCluster - 1 && lane == 0) bulk_wait_read();  // sources free
   cluster_sync();  // the leader's histogram is complete
   if (rank == 0 && warp >= 2) {
     const int e = threadIdx.x - 64;
