@@ -123,6 +123,16 @@ def test_decode_layer(layer, schedule):
     assert_close(got["y"], oracle_outputs(c), f"decode layer {layer}")
 
 
+# Batch-1 decode at other sizes: the largest expert inner dimension (d=4096, f=2048) and a
+# wide hidden size (d=8192, f=512).
+@pytest.mark.parametrize("d,f", [(4096, 2048), (8192, 512)])
+def test_decode_other_shapes(d, f):
+    c = build_case("decode-shapes", d=d, f=f, fs=f, T=1, seed=5, full_host=False)
+    got = _run(c, moe.MOE_SCHEDULE_GEMV)
+    _check_routing(c, got)
+    assert_close(got["y"], oracle_outputs(c), f"decode d={d} f={f}")
+
+
 @pytest.mark.parametrize("skew", [False, True], ids=["balanced", "skewed"])
 def test_prefill_4096(skew):
     c = build_case("prefill", d=2048, f=512, fs=512, T=4096, seed=0, skew=skew)
