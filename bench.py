@@ -12,7 +12,9 @@ Also measured in the same run and reported in the same line:
           its CUDA-event duration, against MEASURED_PEAKS.json;
   e2e: the same tokens/s through moe_forward_host (pinned host x in, host y out, copies
        inside the timed region);
-  cpu_baseline: the CPU oracle on a bounded sample of the same workload (rank 0 only).
+  cpu_baseline: the CPU oracle on a bounded sample of the same workload (rank 0 only);
+  prefill_skewed: the same layer with skewed routing (router bias -2.4 ln(rank_e)), timed
+       and set against the floor of its own bytes and FLOPs; --sweep adds T = 256 .. 131072.
 --impl reference times only the CPU oracle (the reference arm of this benchmark).
 """
 import argparse
@@ -52,6 +54,9 @@ def parse_args():
     p.add_argument("--decode-layers", type=int, default=DECODE_LAYERS,
                    help="layers in the decode graph (40 = the benchmark workload)")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-skew", action="store_true", help="skip the skewed-routing prefill line")
+    p.add_argument("--sweep", action="store_true",
+                   help="also time the prefill layer at T = 256 .. 131072 (balanced)")
     return p.parse_args()
 
 
@@ -332,6 +337,46 @@ def run_prefill(torch, moe, args, rank, world, P_hbm, P_tc, peak_note):
     return dict(ms=ms, e2e_ms=e2e_ms, roofline=roof, layer=stats, launches=len(KERNELS_GEMM))
 
 
+SWEEP_T = (256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)
+
+
+def time_prefill(torch, moe, T, skew, steps, warmup, seed, P_hbm, P_tc):
+    """Layer time (L2 flushed before every step) at T tokens, balanced or skewed routing
+    (router bias -2.4 ln(rank) over a seeded permutation of the experts), with the bytes and
+    FLOPs of that routing and the fraction of the binding floor max(bytes/B, FLOPs/P)."""
+    dims = synth.Dims(d=D, f=F, fs=FS)
+    bias = synth.skew_bias(seed, 0, E) if skew else None
+    W = device_weights(torch, seed, 0, dims, bias)
+    x = torch.from_numpy(synth.x_rows(seed, 0, T, D).view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty_like(x)
+    layer = moe.MoeLayer(W, T)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    counts = np.diff(layer.route(x)["offsets"].cpu().numpy())
+    for _ in range(warmup):
+        layer.forward(x, y)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        layer.forward(x, y)
+        b.record()
+    torch.cuda.synchronize()
+    assert layer.device_error() == moe.MOE_OK
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    layer.close()
+    _, _, byts, flops = algorithmic(counts, T)
+    t = ms / 1e3
+    floor = max(byts / (P_hbm * 1e9), flops / (P_tc * 1e12))
+    return {"T": T, "routing": "skewed" if skew else "balanced", "ms": ms,
+            "tokens_per_s": T / t, "hbm_frac": byts / t / 1e9 / P_hbm,
+            "tensor_frac": flops / t / 1e12 / P_tc, "floor_us": floor * 1e6,
+            "frac_of_floor": floor / t, "bound": "hbm" if byts / (P_hbm * 1e9) >= flops /
+            (P_tc * 1e12) else "tensor", "nonempty_experts": int((counts > 0).sum()),
+            "max_expert_rows": int(counts.max())}
+
+
 def run_decode(torch, moe, args, rank, world, P_hbm):
     dims = synth.Dims(d=D, f=F, fs=FS)
     seed = 1000 + rank
@@ -446,6 +491,12 @@ def main():
             print(json.dumps({"decode": dec, "clocks": clk}), flush=True)
         return
     pre = run_prefill(torch, moe, args, rank, world, P_hbm, P_tc, note)
+    skewed = None if args.no_skew else time_prefill(
+        torch, moe, T_PREFILL, True, min(args.steps, 50), max(3, args.warmup), rank, P_hbm, P_tc)
+    sweep = None
+    if args.sweep:
+        sweep = [time_prefill(torch, moe, t, False, min(args.steps, 20), 3, rank, P_hbm, P_tc)
+                 for t in SWEEP_T]
     dec = None if args.no_decode else run_decode(torch, moe, args, rank, world, P_hbm)
     clk = clocks.stop()
     cpu = None
@@ -468,6 +519,8 @@ def main():
                          "1.62 GB > L2"},
         "roofline": pre["roofline"],
         "layer": pre["layer"],
+        "prefill_skewed": skewed,
+        "prefill_sweep": sweep,
         "decode": dec,
         "cpu_baseline": cpu,
         "e2e": {"value": world * T_PREFILL / (pre["e2e_ms"] / 1e3), "unit": "tokens/s",
