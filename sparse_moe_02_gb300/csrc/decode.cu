@@ -101,66 +101,55 @@ __device__ __forceinline__ uint32_t float_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Warp-level selection from logits[256] (read through L2): the 8 largest (ties: lower id) in
-// ascending expert id and their softmax weights; lanes 0..7 write ids[lane], w[lane].
-// Each lane sorts its 8 logits (ids lane + 32i) by value, keeping ids ascending among equal
-// values; each round takes the warp-wide largest head value (redux max over order-preserving
-// keys), then the lowest id holding it (redux min), and that lane advances its head.
+// Warp-level selection from logits[256] (read through L2): the 8 largest (ties: lower id),
+// listed in ascending expert id with their softmax weights; lanes 0..7 write ids[rank],
+// w[rank].  Lane l holds the logits of ids l + 32 i.  Eight rounds, each taking the warp-wide
+// largest remaining logit (redux max over order-preserving keys, then redux min over the ids
+// holding it); the winners are then ranked by id.  The rounds stay a loop: the code runs
+// once per launch from a cold instruction cache, where straight-line code is slow.
 __device__ __forceinline__ void select_top8(const float* logits, int lane, int* ids, float* w) {
   float v[8];
-  int id[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[i] = __ldcg(logits + lane + 32 * i);
-    id[i] = lane + 32 * i;
-  }
-  // stable insertion sort, value descending (ids ascending within equal values)
-#pragma unroll
-  for (int i = 1; i < 8; ++i)
-#pragma unroll
-    for (int j = i; j > 0; --j)
-      if (v[j] > v[j - 1]) {
-        float tv = v[j]; v[j] = v[j - 1]; v[j - 1] = tv;
-        int ti = id[j]; id[j] = id[j - 1]; id[j - 1] = ti;
-      }
-  float wv[8];
-  int wi[8];
-#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __ldcg(logits + lane + 32 * i);
+  int my_id = 0;
+  float my_v = 0.f;
+  uint32_t taken = 0;  // bit i: id lane + 32 i already selected
+#pragma unroll 1
   for (int r = 0; r < kTopK; ++r) {
-    const uint32_t key = float_key(v[0]);
-    const uint32_t best = __reduce_max_sync(0xffffffffu, key);
-    const uint32_t win = __reduce_min_sync(0xffffffffu, key == best ? (uint32_t)id[0] : 0xffffffffu);
-    wi[r] = (int)win;
-    wv[r] = __shfl_sync(0xffffffffu, v[0], (int)(win & 31u));
-    if ((int)(win & 31u) == lane) {  // advance this lane's head
+    uint32_t bk = 0;
+    int bid = 0x7fffffff;
+    float bv = 0.f;
 #pragma unroll
-      for (int i = 0; i < 7; ++i) { v[i] = v[i + 1]; id[i] = id[i + 1]; }
-      v[7] = -INFINITY;
-      id[7] = 0x7fffffff;
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t k = float_key(v[i]);
+      // ids ascend with i: the first maximum in the lane wins ties
+      if (!((taken >> i) & 1u) && (k > bk || bid == 0x7fffffff)) {
+        bk = k;
+        bid = lane + 32 * i;
+        bv = v[i];
+      }
+    }
+    const uint32_t best = __reduce_max_sync(0xffffffffu, bk);
+    const int win = (int)__reduce_min_sync(0xffffffffu, bk == best ? (uint32_t)bid : 0xffffffffu);
+    if (bid == win) taken |= 1u << (win >> 5);
+    const float val = __shfl_sync(0xffffffffu, bv, win & 31);
+    if (lane == r) {
+      my_id = win;
+      my_v = val;
     }
   }
+  // lanes 0..7: softmax against the largest kept logit (the first winner), rank by id
+  const float mx = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < kTopK ? __expf(my_v - mx) : 0.f;
+  float sum = ex;
 #pragma unroll
-  for (int i = 0; i < 7; ++i)
-#pragma unroll
-    for (int j = 0; j < 7 - i; ++j)
-      if (wi[j] > wi[j + 1]) {
-        int ti = wi[j]; wi[j] = wi[j + 1]; wi[j + 1] = ti;
-        float tv = wv[j]; wv[j] = wv[j + 1]; wv[j + 1] = tv;
-      }
-  float mx = wv[0];
-#pragma unroll
-  for (int j = 1; j < 8; ++j) mx = fmaxf(mx, wv[j]);
-  float ex[8], sum = 0.f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) { ex[j] = __expf(wv[j] - mx); sum += ex[j]; }
+  for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  int rank = 0;
+#pragma unroll 1
+  for (int k = 0; k < kTopK; ++k) rank += __shfl_sync(0xffffffffu, my_id, k) < my_id;
   if (lane < kTopK) {
-    int myi = wi[0];
-    float myw = ex[0];
-#pragma unroll
-    for (int j = 1; j < 8; ++j)
-      if (lane == j) { myi = wi[j]; myw = ex[j]; }
-    ids[lane] = myi;
-    w[lane] = myw / sum;
+    ids[rank] = my_id;
+    w[rank] = ex / sum;
   }
 }
 

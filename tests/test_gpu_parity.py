@@ -133,6 +133,39 @@ def test_decode_other_shapes(d, f):
     assert_close(got["y"], oracle_outputs(c), f"decode d={d} f={f}")
 
 
+# Batch-1 decode where the shared expert's inner dim differs from the routed one and d is not
+# a power of two (rows end in a partial 4 KB chunk, blocks get uneven shares).
+@pytest.mark.parametrize("d,f,fs", [(640, 128, 384), (2176, 384, 128)])
+def test_decode_ragged_shapes(d, f, fs):
+    c = build_case("decode-ragged", d=d, f=f, fs=fs, T=1, seed=d, full_host=False)
+    got = _run(c, moe.MOE_SCHEDULE_GEMV)
+    _check_routing(c, got)
+    assert_close(got["y"], oracle_outputs(c), f"decode d={d} f={f} fs={fs}")
+
+
+def test_decode_repeated_and_interleaved_launches():
+    # the layer launch keeps its grid-barrier counters in the handle and resets them on exit:
+    # back-to-back launches on one handle, and two handles' launches interleaved on one
+    # stream, all give the same bytes
+    import torch
+    cs = [build_case("decode-rep", d=2048, f=512, fs=512, T=1, seed=0, layer=l, full_host=False)
+          for l in (3, 4)]
+    Ls, xs = [], []
+    for c in cs:
+        W, x = to_device(c)
+        Ls.append(moe.MoeLayer(W, 1, schedule=moe.MOE_SCHEDULE_GEMV))
+        xs.append(x)
+    first = [bf16_bits(L.forward(x)) for L, x in zip(Ls, xs)]
+    for _ in range(5):
+        for i, (L, x) in enumerate(zip(Ls, xs)):
+            assert np.array_equal(bf16_bits(L.forward(x)), first[i])
+    torch.cuda.synchronize()
+    for L, c, y in zip(Ls, cs, first):
+        assert L.device_error() == moe.MOE_OK
+        assert_close(y, oracle_outputs(c), "decode repeated")
+        L.close()
+
+
 @pytest.mark.parametrize("skew", [False, True], ids=["balanced", "skewed"])
 def test_prefill_4096(skew):
     c = build_case("prefill", d=2048, f=512, fs=512, T=4096, seed=0, skew=skew)
