@@ -80,6 +80,12 @@ typedef struct {
   int shared_ffn_dim; /* fs, shared expert inner dim: multiple of 128, 128 <= fs <= 2048 */
   int max_tokens;     /* largest T accepted later: 1 <= max_tokens <= 1048576 */
   int schedule;       /* a moe_schedule value */
+  int chunk_tokens;   /* 0, or 1 <= chunk_tokens: moe_forward / moe_forward_host run the layer
+                         over at most this many tokens at a time (§ "Prompt chunking": long
+                         prompts in bounded pieces), so the per-slot expert buffers (about
+                         9 T (2 d + 2 max(f, fs)) bytes) are sized for a chunk, not for
+                         max_tokens.  Tokens are independent: the output is byte-identical to
+                         the unchunked layer.  moe_route is never chunked. */
 } moe_config;
 
 typedef struct {           /* device pointers, borrowed (see above) */

@@ -40,7 +40,8 @@ _c_int, _c_void_p = ctypes.c_int, ctypes.c_void_p
 
 class moe_config(ctypes.Structure):
     _fields_ = [("d", _c_int), ("n_experts", _c_int), ("top_k", _c_int), ("ffn_dim", _c_int),
-                ("shared_ffn_dim", _c_int), ("max_tokens", _c_int), ("schedule", _c_int)]
+                ("shared_ffn_dim", _c_int), ("max_tokens", _c_int), ("schedule", _c_int),
+                ("chunk_tokens", _c_int)]
 
 
 class moe_weights(ctypes.Structure):
@@ -161,13 +162,13 @@ class MoeLayer:
     optionally router_bias [E] (float32).  The tensors are borrowed: keep them alive.
     """
 
-    def __init__(self, weights, max_tokens, schedule=MOE_SCHEDULE_AUTO):
+    def __init__(self, weights, max_tokens, schedule=MOE_SCHEDULE_AUTO, chunk_tokens=0):
         E, f, d = weights["w_gate"].shape
         fs = weights["ws_gate"].shape[0]
         self.d, self.f, self.fs, self.E, self.k = d, f, fs, E, 8
         self.max_tokens = max_tokens
         self._weights = weights  # keep the borrowed tensors alive
-        cfg = moe_config(d, E, 8, f, fs, max_tokens, schedule)
+        cfg = moe_config(d, E, 8, f, fs, max_tokens, schedule, chunk_tokens)
         w = moe_weights(_ptr(weights["w_router"]), _ptr(weights.get("router_bias")),
                         _ptr(weights["w_gate"]), _ptr(weights["w_up"]), _ptr(weights["w_down"]),
                         _ptr(weights["ws_gate"]), _ptr(weights["ws_up"]),

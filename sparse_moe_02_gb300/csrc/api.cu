@@ -65,6 +65,7 @@ struct moe_handle_s {
   Dims D;
   int device = 0, sms = 0;
   int P_max = 0, max_units_gu = 0, max_units_dn = 0, max_chunks = 0;
+  int Tc = 0, P_chunk = 0;  // tokens per forward chunk; rows of h and ys for one chunk
   void* ws = nullptr;
   size_t ws_bytes = 0;
   moe::RouteWs rws{};
@@ -94,6 +95,7 @@ int check_config(const moe_config* c) {
   if (c->ffn_dim % 128 || c->ffn_dim > 2048) return MOE_ERR_UNSUPPORTED;
   if (c->shared_ffn_dim % 128 || c->shared_ffn_dim > 2048) return MOE_ERR_UNSUPPORTED;
   if (c->max_tokens > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+  if (c->chunk_tokens < 0) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -145,10 +147,11 @@ void layout(moe_handle_s* h, char* base, size_t* total) {
   h->dws.logits = c.take<float>(kE);
   h->dws.counter = c.take<int>(1);
   h->dws.hdec = c.take<float>((size_t)9 * h->D.hdim);
-  h->h = c.take<__nv_bfloat16>((size_t)h->P_max * h->D.hdim);
-  h->ys = c.take<__nv_bfloat16>((size_t)h->P_max * h->D.d);
-  h->x_stage = c.take<__nv_bfloat16>((size_t)Tm * h->D.d);
-  h->y_stage = c.take<__nv_bfloat16>((size_t)Tm * h->D.d);
+  // the large per-slot buffers hold one forward chunk (Tc tokens, P_chunk padded rows)
+  h->h = c.take<__nv_bfloat16>((size_t)h->P_chunk * h->D.hdim);
+  h->ys = c.take<__nv_bfloat16>((size_t)h->P_chunk * h->D.d);
+  h->x_stage = c.take<__nv_bfloat16>((size_t)h->Tc * h->D.d);
+  h->y_stage = c.take<__nv_bfloat16>((size_t)h->Tc * h->D.d);
   *total = c.off + 256;
 }
 
@@ -211,6 +214,23 @@ int run_route_gemm(moe_handle h, const void* x, int T, int32_t* topk_idx, float*
   return cuda_status(moe::launch_route_plan_scatter(T, h->D, topk_idx, perm, w, s));
 }
 
+// The tensor-core schedule over T <= Tc tokens: routing chain, grouped GEMMs, combine
+// (profiling marks 0..4 when prof).
+int forward_gemm(moe_handle h, const __nv_bfloat16* xd, int T, __nv_bfloat16* yd,
+                 cudaStream_t s, bool prof) {
+  int st;
+  if ((st = run_route_gemm(h, xd, T, h->rws.topk_idx, h->rws.topk_w, nullptr, h->rws.perm, s,
+                           prof)))
+    return st;
+  if (prof && (st = prof_mark(h, s, 2))) return st;
+  if ((st = cuda_status(moe::launch_experts(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu,
+                                            h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->h,
+                                            h->ys, h->sms, s))))
+    return st;
+  if (prof && (st = prof_mark(h, s, 3))) return st;
+  return cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, h->sms, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -243,6 +263,10 @@ int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
   const int S = Tm * kTopK;
   // every group padded to 16 rows: routed groups add at most 15 rows each
   h->P_max = moe::round_up(S + kE * (moe::kRowAlign - 1) + moe::round_up(Tm, moe::kRowAlign), 256);
+  h->Tc = cfg->chunk_tokens > 0 && cfg->chunk_tokens < Tm ? cfg->chunk_tokens : Tm;
+  h->P_chunk = moe::round_up(h->Tc * kTopK + kE * (moe::kRowAlign - 1) +
+                                 moe::round_up(h->Tc, moe::kRowAlign),
+                             256);
   const int chunks_routed = (S + moe::kChunkRows - 1) / moe::kChunkRows + kE;
   const int chunks_shared = (Tm + moe::kChunkRows - 1) / moe::kChunkRows;
   h->max_units_gu = chunks_routed * (cfg->ffn_dim / moe::kMTile) +
@@ -269,7 +293,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
             encode_2d(&h->tm_wsu, w->ws_up, D.d, D.fs, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wd, w->w_down, D.f, (uint64_t)kE * D.d, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wsd, w->ws_down, D.fs, D.d, moe::kBK, moe::kMTile) &&
-            encode_2d(&h->tm_h, h->h, D.hdim, h->P_max, moe::kBK, 16);
+            encode_2d(&h->tm_h, h->h, D.hdim, h->P_chunk, moe::kBK, 16);
   if (!ok) return fail(MOE_ERR_CUDA);
   if ((st = cuda_status(moe::prepare_route_kernels()))) return fail(st);
   if ((st = cuda_status(moe::prepare_expert_kernels()))) return fail(st);
@@ -326,18 +350,19 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
     return prof_finish_call(h, s, 3);
   }
 
-  if ((st = run_route_gemm(h, x, T, h->rws.topk_idx, h->rws.topk_w, nullptr, h->rws.perm, s,
-                           true)))
-    return st;
-  if ((st = prof_mark(h, s, 2))) return st;
-  if ((st = cuda_status(moe::launch_experts(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu,
-                                            h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->h,
-                                            h->ys, h->sms, s))))
-    return st;
-  if ((st = prof_mark(h, s, 3))) return st;
-  if ((st = cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, h->sms, s))))
-    return st;
-  return prof_finish_call(h, s, 4);
+  if (T <= h->Tc) {
+    if ((st = forward_gemm(h, xd, T, yd, s, true))) return st;
+    return prof_finish_call(h, s, 4);
+  }
+  // longer than a chunk: the layer over consecutive chunks of at most Tc tokens, in order on
+  // the stream (profiled as one entry)
+  if ((st = prof_mark(h, s, 0))) return st;
+  for (int t0 = 0; t0 < T; t0 += h->Tc) {
+    const int n = T - t0 < h->Tc ? T - t0 : h->Tc;
+    const size_t off = (size_t)t0 * h->D.d;
+    if ((st = forward_gemm(h, xd + off, n, yd + off, s, false))) return st;
+  }
+  return prof_finish_call(h, s, 1);
 }
 
 int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void* stream) {
@@ -347,11 +372,19 @@ int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void
   if (T == 0) return MOE_OK;
   if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t bytes = (size_t)T * h->D.d * 2;
-  int st = cuda_status(cudaMemcpyAsync(h->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s));
-  if (st) return st;
-  if ((st = moe_forward(h, h->x_stage, T, h->y_stage, stream))) return st;
-  return cuda_status(cudaMemcpyAsync(y_host, h->y_stage, bytes, cudaMemcpyDeviceToHost, s));
+  // through the staging buffers one chunk at a time (stream order keeps the reuse safe)
+  const char* xb = static_cast<const char*>(x_host);
+  char* yb = static_cast<char*>(y_host);
+  for (int t0 = 0; t0 < T; t0 += h->Tc) {
+    const int n = T - t0 < h->Tc ? T - t0 : h->Tc;
+    const size_t off = (size_t)t0 * h->D.d * 2, bytes = (size_t)n * h->D.d * 2;
+    int st = cuda_status(cudaMemcpyAsync(h->x_stage, xb + off, bytes, cudaMemcpyHostToDevice, s));
+    if (st) return st;
+    if ((st = moe_forward(h, h->x_stage, n, h->y_stage, stream))) return st;
+    if ((st = cuda_status(cudaMemcpyAsync(yb + off, h->y_stage, bytes, cudaMemcpyDeviceToHost, s))))
+      return st;
+  }
+  return MOE_OK;
 }
 
 int moe_get_device_error(moe_handle h, void* stream) {

@@ -28,7 +28,7 @@ def test_library_exports_every_declared_function():
 
 def _cfg(**kw):
     base = dict(d=512, n_experts=256, top_k=8, ffn_dim=128, shared_ffn_dim=128, max_tokens=64,
-                schedule=0)
+                schedule=0, chunk_tokens=0)
     base.update(kw)
     return moe.moe_config(**base)
 
@@ -53,6 +53,7 @@ def _weights(addr=0x10000, **kw):
     (dict(max_tokens=(1 << 20) + 1), moe.MOE_ERR_UNSUPPORTED),
     (dict(d=0), moe.MOE_ERR_INVALID_ARG),
     (dict(schedule=7), moe.MOE_ERR_INVALID_ARG),
+    (dict(chunk_tokens=-1), moe.MOE_ERR_INVALID_ARG),
 ])
 def test_create_rejects_bad_config(kw, status):
     st, h = moe.moe_create(_cfg(**kw), _weights())

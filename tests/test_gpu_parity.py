@@ -201,6 +201,32 @@ def test_prefill_plan_paths(T):
     assert_close(got["y"][toks], oracle_outputs(c, toks), f"plan paths T={T}")
 
 
+# In-layer token chunking: the layer over chunks of at most chunk_tokens tokens (the expert
+# buffers sized for one chunk) gives exactly the bytes of the unchunked layer, through the
+# device and the host entry points; outputs checked against the oracle on sampled tokens.
+@pytest.mark.parametrize("chunk", [1000, 2048])
+def test_chunked_forward_is_byte_identical(chunk):
+    import torch
+    T = 4500
+    c = build_case("chunked", d=512, f=128, fs=256, T=T, seed=31)
+    W, x = to_device(c)
+    L0 = moe.MoeLayer(W, T)
+    L1 = moe.MoeLayer(W, T, chunk_tokens=chunk)
+    y0 = bf16_bits(L0.forward(x))
+    y1 = bf16_bits(L1.forward(x))
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    L1.forward_host(xh, yh)
+    torch.cuda.synchronize()
+    assert L0.device_error() == moe.MOE_OK and L1.device_error() == moe.MOE_OK
+    assert np.array_equal(y0, y1)
+    assert np.array_equal(bf16_bits(yh), y1)
+    toks = sample_tokens(T, n_edge=16, stride=61)
+    assert_close(y1[toks], oracle_outputs(c, toks), f"chunked T={T} chunk={chunk}")
+    L0.close()
+    L1.close()
+
+
 # ---------------------------------------------------------------- API behaviour on the GPU
 
 def test_deterministic_and_host_entry_point():
