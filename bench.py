@@ -55,6 +55,8 @@ def parse_args():
                    help="layers in the decode graph (40 = the benchmark workload)")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-skew", action="store_true", help="skip the skewed-routing prefill line")
+    p.add_argument("--no-small-batch", action="store_true",
+                   help="skip the T = 2..5 decode lines")
     p.add_argument("--sweep", action="store_true",
                    help="also time the prefill layer at T = 256 .. 131072 (balanced)")
     return p.parse_args()
@@ -422,13 +424,68 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
     for L in layers:
         assert L.device_error() == moe.MOE_OK
         L.close()
+    small = None if args.no_small_batch else run_small_batch(torch, moe, args, Ws, seed, P_hbm)
     return {"us_per_layer": us_layer, "GB_per_s": gbs, "layers": nl,
             "bytes_per_layer": DECODE_BYTES_PER_LAYER,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": P_hbm, "unit": "GB/s",
                          "frac": gbs / P_hbm},
             "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in zip(KERNELS_GEMV, kms)},
             "gpu_launches": args.steps * nl * 3,
-            "graph": f"{nl} stream-ordered layer calls, replayed per step"}
+            "graph": f"{nl} stream-ordered layer calls, replayed per step",
+            "small_batch": small}
+
+
+SMALL_BATCH_T = (2, 3, 4, 5)
+
+
+def run_small_batch(torch, moe, args, Ws, seed, P_hbm):
+    """Decode of T = 2..5 tokens per layer (the speculative-verify shape) over the same 40
+    layers' weights, one CUDA graph per T and schedule: us/layer through the matrix-vector
+    path over the union of the tokens' experts (schedule GEMV) and through the default
+    tensor-core path, and the HBM fraction of the bytes this routing needs (gate/up/down of
+    the union of the tokens' experts, router, shared expert, x and y) for the faster one."""
+    out = []
+    for T in SMALL_BATCH_T:
+        x = torch.from_numpy(synth.x_rows(seed, 0, T, D).view(np.int16)).cuda() \
+            .view(torch.bfloat16)
+        row = {"T": T}
+        for name, sched in (("gemv", moe.MOE_SCHEDULE_GEMV), ("tensor_core", moe.MOE_SCHEDULE_AUTO)):
+            layers = [moe.MoeLayer(W, T, schedule=sched) for W in Ws]
+            ys = [torch.empty_like(x) for _ in layers]
+            if name == "gemv":
+                union = [len(np.unique(L.route(x)["topk_idx"].cpu().numpy())) for L in layers]
+            stream = torch.cuda.Stream()
+            with torch.cuda.stream(stream):
+                for L, y in zip(layers, ys):
+                    L.forward(x, y)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for L, y in zip(layers, ys):
+                    L.forward(x, y)
+            for _ in range(3):
+                g.replay()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(min(args.steps, 50))]
+            torch.cuda.synchronize()
+            for a, b in ev:
+                a.record()
+                g.replay()
+                b.record()
+            torch.cuda.synchronize()
+            row[f"{name}_us_per_layer"] = \
+                statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3 / len(layers)
+            for L in layers:
+                assert L.device_error() == moe.MOE_OK
+                L.close()
+            del g
+        nbytes = (statistics.mean(union) * 3 * F * D * 2 + 3 * FS * D * 2 + E * D * 2
+                  + 2 * T * D * 2)
+        best = min(row["gemv_us_per_layer"], row["tensor_core_us_per_layer"])
+        row.update({"union_experts": statistics.mean(union), "bytes_per_layer": nbytes,
+                    "hbm_frac": nbytes / (best * 1e-6) / 1e9 / P_hbm})
+        out.append(row)
+    return out
 
 
 def profiled_traffic(kernel):

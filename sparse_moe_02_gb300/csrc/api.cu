@@ -144,9 +144,9 @@ void layout(moe_handle_s* h, char* base, size_t* total) {
   h->rws.next_unit = c.take<int32_t>(1);
   h->rws.chunk_done = c.take<int32_t>((size_t)h->max_chunks);
   h->rws.err = c.take<int>(1);
-  h->dws.logits = c.take<float>(kE);
+  h->dws.logits = c.take<float>((size_t)moe::kGemvMaxTokens * kE);
   h->dws.counter = c.take<int>(1);
-  h->dws.hdec = c.take<float>((size_t)9 * h->D.hdim);
+  h->dws.hdec = c.take<float>((size_t)moe::kGemvMaxTokens * 9 * h->D.hdim);
   // the large per-slot buffers hold one forward chunk (Tc tokens, P_chunk padded rows)
   h->h = c.take<__nv_bfloat16>((size_t)h->P_chunk * h->D.hdim);
   h->ys = c.take<__nv_bfloat16>((size_t)h->P_chunk * h->D.d);
@@ -174,7 +174,8 @@ int check_call(moe_handle h, const void* x, int T) {
   if (T > h->cfg.max_tokens) return MOE_ERR_UNSUPPORTED;
   if (T > 0 && !x) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x)) return MOE_ERR_ALIGNMENT;
-  if (h->cfg.schedule == MOE_SCHEDULE_GEMV && T > 1) return MOE_ERR_UNSUPPORTED;
+  if (h->cfg.schedule == MOE_SCHEDULE_GEMV && T > 1 && !moe::decode_batch_fits(h->D, T))
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -196,6 +197,13 @@ int prof_finish_call(moe_handle h, cudaStream_t s, int nk) {
 
 bool use_gemv(const moe_handle_s* h, int T) {
   return T == 1 && h->cfg.schedule != MOE_SCHEDULE_GEMM;
+}
+
+// 2..8 tokens whose shapes fit, on request (schedule GEMV): the matrix-vector path over the
+// union of their experts.  AUTO keeps these T on the tensor-core path, measured faster on
+// GB300 at T = 2..5 (bench.py's small-batch lines time both).
+bool use_batch(const moe_handle_s* h, int T) {
+  return h->cfg.schedule == MOE_SCHEDULE_GEMV && moe::decode_batch_fits(h->D, T);
 }
 
 // The routing chain of the tensor-core schedule.
@@ -298,6 +306,7 @@ int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
   if ((st = cuda_status(moe::prepare_route_kernels()))) return fail(st);
   if ((st = cuda_status(moe::prepare_expert_kernels()))) return fail(st);
   if ((st = cuda_status(moe::prepare_decode_kernels(D.hdim)))) return fail(st);
+  if ((st = cuda_status(moe::prepare_decode_batch_kernels()))) return fail(st);
   if ((st = cuda_status(cudaDeviceSynchronize()))) return fail(st);
   *out = h;
   return MOE_OK;
@@ -318,6 +327,10 @@ int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk
     return cuda_status(moe::launch_decode_router_shared(
         static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, idx, wt,
         offsets ? offsets : h->rws.offsets, pm, h->dws, h->rws.err, s, false));
+  if (use_batch(h, T))
+    return cuda_status(moe::launch_decode_batch_router_shared(
+        static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, T, idx, wt,
+        offsets ? offsets : h->rws.offsets, pm, h->dws, s, false));
   return run_route_gemm(h, x, T, idx, wt, offsets, pm, s, false);
 }
 
@@ -347,6 +360,24 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
       return st;
     if ((st = prof_mark(h, s, 2))) return st;
     if ((st = cuda_status(moe::launch_decode_down_combine(W, h->D, h->dws, yd, s)))) return st;
+    return prof_finish_call(h, s, 3);
+  }
+
+  if (use_batch(h, T)) {
+    const moe::DecodeWeights W = decode_weights(h);
+    if ((st = prof_mark(h, s, 0))) return st;
+    if ((st = cuda_status(moe::launch_decode_batch_router_shared(xd, W, h->D, T, nullptr, nullptr,
+                                                                 nullptr, nullptr, h->dws, s,
+                                                                 true))))
+      return st;
+    if ((st = prof_mark(h, s, 1))) return st;
+    if ((st = cuda_status(moe::launch_decode_batch_gateup(xd, W, h->D, T, h->rws.topk_idx,
+                                                          h->rws.topk_w, h->dws, h->sms, s))))
+      return st;
+    if ((st = prof_mark(h, s, 2))) return st;
+    if ((st = cuda_status(moe::launch_decode_batch_down_combine(W, h->D, T, h->dws, yd, h->sms,
+                                                                s))))
+      return st;
     return prof_finish_call(h, s, 3);
   }
 

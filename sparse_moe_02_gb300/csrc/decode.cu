@@ -359,6 +359,304 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_down_combine_kernel(DownAr
   }
 }
 
+// ---------------------------------------------------------------- small batches (2..8 tokens)
+//
+// The speculative-verify shape (§ "Limits of further optimization": verifying a few draft
+// tokens at once): each token keeps its own top 8, and every weight row of the union of the
+// selected experts is read once and applied to every token that chose that expert.  Per token
+// the sum keeps the single-token order: ascending expert id, then the shared expert.
+
+// Lane-partial dot products of one d-element row with the x rows of the tokens in `mask`
+// (bit t: token t, at xs + t * nch), kPre*32 pieces at a time; the first such piece group is
+// already in r.  mask is the same in every lane.
+__device__ __forceinline__ void row_dot_tokens(RowFrag& r, const __nv_bfloat16* row,
+                                               const uint4* xs, int nch, int mask, int lane,
+                                               float (&acc)[kGemvMaxTokens]) {
+  for (int base = 0; base < nch; base += kPre * 32) {
+    if (base) row_load(r, row, nch, lane, base);
+#pragma unroll
+    for (int t = 0; t < kGemvMaxTokens; ++t)
+      if ((mask >> t) & 1) acc[t] += row_dot(r, xs + (size_t)t * nch, nch, lane, base);
+  }
+}
+
+// Per-block view of the batch's routing: each token's top 8 (ascending id) and weights, and
+// the union of the selections in ascending expert id with, per expert, the mask of tokens
+// that chose it.
+struct BatchSel {
+  int ids[kGemvMaxTokens][kTopK];
+  float w[kGemvMaxTokens][kTopK];
+  int tmask[kE];
+  int ulist[kE];
+  int nu;
+};
+
+// Every thread of the block calls this (it holds barriers); logits [T][E] read through L2.
+__device__ void batch_select(const float* logits, int T, BatchSel& S) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < kE; e += blockDim.x) S.tmask[e] = 0;
+  if (warp < T) select_top8(logits + (size_t)warp * kE, lane, S.ids[warp], S.w[warp]);
+  __syncthreads();
+  if ((int)threadIdx.x < T * kTopK)
+    atomicOr(&S.tmask[S.ids[threadIdx.x / kTopK][threadIdx.x % kTopK]], 1 << (threadIdx.x / kTopK));
+  __syncthreads();
+  if (warp == 0) {
+    int n = 0;
+    for (int e0 = 0; e0 < kE; e0 += 32) {
+      const bool used = S.tmask[e0 + lane] != 0;
+      const uint32_t bal = __ballot_sync(0xffffffffu, used);
+      if (used) S.ulist[n + __popc(bal & ((1u << lane) - 1u))] = e0 + lane;
+      n += __popc(bal);
+    }
+    if (lane == 0) S.nu = n;
+  }
+  __syncthreads();
+}
+
+// Position of expert e in token t's top 8 (e was selected by t).
+__device__ __forceinline__ int batch_slot(const BatchSel& S, int t, int e) {
+  int j = 0;
+#pragma unroll
+  for (int i = 0; i < kTopK; ++i) j = S.ids[t][i] == e ? i : j;
+  return j;
+}
+
+struct BatchRouterArgs {
+  const __nv_bfloat16* x;
+  DecodeWeights W;
+  Dims D;
+  int T;
+  int32_t *topk_idx, *offsets, *perm;  // routing outputs (NULL topk_idx: forward)
+  float* topk_w;
+  DecodeWs dw;
+  int router_blocks;
+};
+
+// Blocks [0, router_blocks): one router row per warp for all T tokens; in a routing-only
+// launch the last block to finish selects and writes topk_idx / topk_w / offsets / perm.
+// Blocks after: one shared-expert feature per warp, h_s[t][c] for every token.
+__global__ void __launch_bounds__(kWarps * 32) dec_batch_router_shared_kernel(BatchRouterArgs a) {
+  extern __shared__ uint4 xs[];  // [T][d/8]
+  __shared__ int s_last;
+  __shared__ BatchSel S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.D.d, nch = d / 8, T = a.T;
+  const bool router = (int)blockIdx.x < a.router_blocks;
+  const int c = ((int)blockIdx.x - a.router_blocks) * kWarps + warp;
+  RowFrag r0, r1;
+  if (router) {
+    row_load(r0, a.W.w_r + (size_t)(blockIdx.x * kWarps + warp) * d, nch, lane, 0);
+  } else if (c < a.D.fs) {
+    row_load(r0, a.W.ws_gate + (size_t)c * d, nch, lane, 0);
+    row_load(r1, a.W.ws_up + (size_t)c * d, nch, lane, 0);
+  }
+  pdl_wait();  // x may be written by the previous kernel
+  pdl_trigger();
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    for (int i = threadIdx.x; i < T * nch; i += blockDim.x) xs[i] = __ldcg(src + i);
+  }
+  __syncthreads();
+  if (!router) {
+    if (c < a.D.fs) {
+      float g[kGemvMaxTokens], u[kGemvMaxTokens];
+#pragma unroll
+      for (int t = 0; t < kGemvMaxTokens; ++t) g[t] = u[t] = 0.f;
+      row_dot_tokens(r0, a.W.ws_gate + (size_t)c * d, xs, nch, (1 << T) - 1, lane, g);
+      row_dot_tokens(r1, a.W.ws_up + (size_t)c * d, xs, nch, (1 << T) - 1, lane, u);
+#pragma unroll
+      for (int t = 0; t < kGemvMaxTokens; ++t)
+        if (t < T) {
+          const float gv = warp_sum(g[t]), uv = warp_sum(u[t]);
+          if (lane == 0) a.dw.hdec[((size_t)t * 9 + 8) * a.D.hdim + c] = silu_mul(gv, uv);
+        }
+    }
+    return;
+  }
+  const int e = blockIdx.x * kWarps + warp;
+  float l[kGemvMaxTokens];
+#pragma unroll
+  for (int t = 0; t < kGemvMaxTokens; ++t) l[t] = 0.f;
+  row_dot_tokens(r0, a.W.w_r + (size_t)e * d, xs, nch, (1 << T) - 1, lane, l);
+#pragma unroll
+  for (int t = 0; t < kGemvMaxTokens; ++t)
+    if (t < T) {
+      const float v = warp_sum(l[t]);
+      if (lane == 0) a.dw.logits[(size_t)t * kE + e] = v + (a.W.bias ? a.W.bias[e] : 0.f);
+    }
+  if (!a.topk_idx) return;  // the forward path selects in the next two kernels
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.dw.counter, 1) == a.router_blocks - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  batch_select(a.dw.logits, T, S);
+  if ((int)threadIdx.x < T * kTopK) {
+    const int t = threadIdx.x / kTopK, j = threadIdx.x % kTopK, id = S.ids[t][j];
+    a.topk_idx[t * kTopK + j] = id;
+    a.topk_w[t * kTopK + j] = S.w[t][j];
+    // slot of (t, j): assignments grouped by expert, tokens ascending within a group
+    int rank = 0;
+    for (int t2 = 0; t2 < T; ++t2)
+      for (int j2 = 0; j2 < kTopK; ++j2) {
+        const int id2 = S.ids[t2][j2];
+        rank += id2 < id || (id2 == id && t2 < t);
+      }
+    if (a.perm) a.perm[rank] = t * kTopK + j;
+  }
+  if (a.offsets)
+    for (int e2 = threadIdx.x; e2 <= kE; e2 += blockDim.x) {
+      int n = 0;
+      for (int i = 0; i < T * kTopK; ++i) n += S.ids[i / kTopK][i % kTopK] < e2;
+      a.offsets[e2] = n;
+    }
+  if (threadIdx.x == 0) *a.dw.counter = 0;  // ready for the next launch on the stream
+}
+
+struct BatchGateUpArgs {
+  const __nv_bfloat16* x;
+  DecodeWeights W;
+  Dims D;
+  int T;
+  int32_t* topk_idx;  // written by block 0 (the selection behind this forward)
+  float* topk_w;
+  DecodeWs dw;
+};
+
+// Items (union expert k, feature c), one warp per item over a resident grid: the gate and up
+// rows are read once; h[t][slot][c] = silu(gate . x_t) * (up . x_t) for every token t that
+// chose the expert.
+__global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_gateup_kernel(BatchGateUpArgs a) {
+  extern __shared__ uint4 xs[];  // [T][d/8]
+  __shared__ BatchSel S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.D.d, f = a.D.f, nch = d / 8, T = a.T;
+  pdl_wait();     // the router logits come from the previous kernel
+  pdl_trigger();  // the down kernel may start selecting and streaming its rows now
+  batch_select(a.dw.logits, T, S);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    for (int i = threadIdx.x; i < T * nch; i += blockDim.x) xs[i] = __ldcg(src + i);
+  }
+  if (blockIdx.x == 0 && (int)threadIdx.x < T * kTopK) {
+    a.topk_idx[threadIdx.x] = S.ids[threadIdx.x / kTopK][threadIdx.x % kTopK];
+    a.topk_w[threadIdx.x] = S.w[threadIdx.x / kTopK][threadIdx.x % kTopK];
+  }
+  __syncthreads();
+  const int nwarps = gridDim.x * kWarps, items = S.nu * f;
+  for (int it = blockIdx.x * kWarps + warp; it < items; it += nwarps) {
+    const int k = it / f, c = it % f, e = S.ulist[k], mask = S.tmask[e];
+    const size_t row = ((size_t)e * f + c) * d;
+    RowFrag rg, ru;
+    row_load(rg, a.W.w_gate + row, nch, lane, 0);
+    row_load(ru, a.W.w_up + row, nch, lane, 0);
+    float g[kGemvMaxTokens], u[kGemvMaxTokens];
+#pragma unroll
+    for (int t = 0; t < kGemvMaxTokens; ++t) g[t] = u[t] = 0.f;
+    row_dot_tokens(rg, a.W.w_gate + row, xs, nch, mask, lane, g);
+    row_dot_tokens(ru, a.W.w_up + row, xs, nch, mask, lane, u);
+#pragma unroll
+    for (int t = 0; t < kGemvMaxTokens; ++t)
+      if (t < T && ((mask >> t) & 1)) {
+        const float gv = warp_sum(g[t]), uv = warp_sum(u[t]);
+        if (lane == 0)
+          a.dw.hdec[((size_t)t * 9 + batch_slot(S, t, e)) * a.D.hdim + c] = silu_mul(gv, uv);
+      }
+  }
+}
+
+struct BatchDownArgs {
+  DecodeWeights W;
+  Dims D;
+  int T;
+  DecodeWs dw;
+  __nv_bfloat16* y;
+};
+
+constexpr int kBatchRows = 8;  // union experts whose down rows one warp has in flight at once
+
+// One warp per output n over a resident grid: the down rows of the union experts, eight at a
+// time (the first eight requested before waiting for h), each applied to the tokens that
+// chose it; per lane and token the terms w_tj (down_e[n] . h_tj) add in ascending expert id,
+// then the shared expert's; one warp reduction per token gives y[t][n].
+__global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_down_combine_kernel(BatchDownArgs a) {
+  extern __shared__ float hs[];  // [T][9][hdim]
+  __shared__ BatchSel S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.D.d, f = a.D.f, fs = a.D.fs, hdim = a.D.hdim, T = a.T;
+  const int nc = f / 8;
+  batch_select(a.dw.logits, T, S);  // final: the router finished before this launch started
+  const int nwarps = gridDim.x * kWarps;
+  int n = blockIdx.x * kWarps + warp;
+  uint4 pre[kBatchRows][kPreDown];
+  auto load_group = [&](int k0, int nn) {
+#pragma unroll
+    for (int q = 0; q < kBatchRows; ++q)
+      if (k0 + q < S.nu) {
+        const __nv_bfloat16* row = a.W.w_down + ((size_t)S.ulist[k0 + q] * d + nn) * f;
+#pragma unroll
+        for (int i = 0; i < kPreDown; ++i)
+          if (lane + 32 * i < nc) pre[q][i] = ld_stream_u4(row + (size_t)(lane + 32 * i) * 8);
+      }
+  };
+  if (n < d) load_group(0, n);
+  pdl_wait();  // h comes from the gate/up kernel
+  pdl_trigger();
+  {
+    const float4* src = reinterpret_cast<const float4*>(a.dw.hdec);
+    float4* dst = reinterpret_cast<float4*>(hs);
+    for (int i = threadIdx.x; i < T * 9 * hdim / 4; i += blockDim.x) dst[i] = __ldcg(src + i);
+  }
+  __syncthreads();
+  for (; n < d; n += nwarps) {
+    float acc[kGemvMaxTokens];
+#pragma unroll
+    for (int t = 0; t < kGemvMaxTokens; ++t) acc[t] = 0.f;
+    for (int k0 = 0; k0 < S.nu; k0 += kBatchRows) {
+      if (k0) load_group(k0, n);
+#pragma unroll
+      for (int q = 0; q < kBatchRows; ++q) {
+        if (k0 + q >= S.nu) break;
+        const int e = S.ulist[k0 + q], mask = S.tmask[e];
+        const __nv_bfloat16* row = a.W.w_down + ((size_t)e * d + n) * f;
+#pragma unroll
+        for (int t = 0; t < kGemvMaxTokens; ++t)
+          if (t < T && ((mask >> t) & 1)) {
+            const int j = batch_slot(S, t, e);
+            const float* ht = hs + ((size_t)t * 9 + j) * hdim;
+            float sj = 0.f;
+#pragma unroll
+            for (int i = 0; i < kPreDown; ++i) {
+              const int cc = lane + 32 * i;
+              if (cc < nc) sj += dot8_f32(pre[q][i], ht + cc * 8);
+            }
+            for (int cc = lane + 32 * kPreDown; cc < nc; cc += 32)
+              sj += dot8_f32(ld_stream_u4(row + (size_t)cc * 8), ht + cc * 8);
+            acc[t] = fmaf(S.w[t][j], sj, acc[t]);
+          }
+      }
+    }
+    // the shared expert, weight 1
+    const __nv_bfloat16* srow = a.W.ws_down + (size_t)n * fs;
+    for (int cc = lane; cc < fs / 8; cc += 32) {
+      const uint4 wv = ld_stream_u4(srow + (size_t)cc * 8);
+#pragma unroll
+      for (int t = 0; t < kGemvMaxTokens; ++t)
+        if (t < T) acc[t] += dot8_f32(wv, hs + ((size_t)t * 9 + 8) * hdim + cc * 8);
+    }
+#pragma unroll
+    for (int t = 0; t < kGemvMaxTokens; ++t)
+      if (t < T) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) a.y[(size_t)t * d + n] = __float2bfloat16_rn(v);
+      }
+    if (n + nwarps < d) load_group(0, n + nwarps);
+  }
+}
+
 }  // namespace
 
 namespace {
@@ -412,6 +710,54 @@ cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D, co
   const int grid = std::min(g_down_grid, (D.d + kWarps - 1) / kWarps);
   return launch_pdl(dec_down_combine_kernel, dim3(grid), dim3(kWarps * 32),
                     (size_t)9 * D.hdim * sizeof(float), s, a);
+}
+
+// ---- small batches
+
+bool decode_batch_fits(const Dims& D, int T) {
+  return T >= 2 && T <= kGemvMaxTokens && T * D.hdim <= kBatchMaxTHdim &&
+         T * D.d <= kBatchMaxTD;
+}
+
+cudaError_t prepare_decode_batch_kernels() {
+  cudaError_t e;
+  const int xs = kBatchMaxTD * 2, hs = kBatchMaxTHdim * 9 * 4;
+  if ((e = cudaFuncSetAttribute(dec_batch_router_shared_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, xs)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(dec_batch_gateup_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, xs)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(dec_batch_down_combine_kernel,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, hs);
+}
+
+cudaError_t launch_decode_batch_router_shared(const __nv_bfloat16* x, const DecodeWeights& W,
+                                              const Dims& D, int T, int32_t* topk_idx,
+                                              float* topk_w, int32_t* offsets, int32_t* perm,
+                                              const DecodeWs& dw, cudaStream_t s,
+                                              bool with_shared) {
+  BatchRouterArgs a{x, W, D, T, topk_idx, offsets, perm, topk_w, dw, kE / kWarps};
+  const int blocks = a.router_blocks + (with_shared ? (D.fs + kWarps - 1) / kWarps : 0);
+  return launch_pdl(dec_batch_router_shared_kernel, dim3(blocks), dim3(kWarps * 32),
+                    (size_t)T * D.d * 2, s, a);
+}
+
+cudaError_t launch_decode_batch_gateup(const __nv_bfloat16* x, const DecodeWeights& W,
+                                       const Dims& D, int T, int32_t* topk_idx, float* topk_w,
+                                       const DecodeWs& dw, int sms, cudaStream_t s) {
+  BatchGateUpArgs a{x, W, D, T, topk_idx, topk_w, dw};
+  return launch_pdl(dec_batch_gateup_kernel, dim3(2 * sms), dim3(kWarps * 32),
+                    (size_t)T * D.d * 2, s, a);
+}
+
+cudaError_t launch_decode_batch_down_combine(const DecodeWeights& W, const Dims& D, int T,
+                                             const DecodeWs& dw, __nv_bfloat16* y, int sms,
+                                             cudaStream_t s) {
+  BatchDownArgs a{W, D, T, dw, y};
+  const int grid = std::min(2 * sms, (D.d + kWarps - 1) / kWarps);
+  return launch_pdl(dec_batch_down_combine_kernel, dim3(grid), dim3(kWarps * 32),
+                    (size_t)T * 9 * D.hdim * sizeof(float), s, a);
 }
 
 }  // namespace moe

@@ -104,10 +104,16 @@ cudaError_t launch_combine(int T, const Dims& D, const float* topk_w, const Rout
 
 // ---------------------------------------------------------------- batch-1 decode path
 
+// Small-batch decode (2..kGemvMaxTokens tokens): shapes whose per-block copies of x
+// (T d bf16) and h (T 9 hdim fp32) fit in shared memory.
+constexpr int kGemvMaxTokens = 8;
+constexpr int kBatchMaxTHdim = 4096;  // T * max(f, fs)
+constexpr int kBatchMaxTD = 65536;    // T * d
+
 struct DecodeWs {
-  float* logits;   // [E]
+  float* logits;   // [kGemvMaxTokens][E]
   int* counter;    // last-block detection of the router
-  float* hdec;     // [9][hdim] fp32: routed experts j = 0..7, shared = 8
+  float* hdec;     // [kGemvMaxTokens][9][hdim] fp32: routed experts j = 0..7, shared = 8
 };
 
 struct DecodeWeights {
@@ -131,5 +137,23 @@ cudaError_t launch_decode_gateup(const __nv_bfloat16* x, const DecodeWeights& W,
 // Down GEMV of the 8 experts and the shared expert, weighted and combined in fixed order.
 cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D, const DecodeWs& dw,
                                        __nv_bfloat16* y, cudaStream_t s);
+
+// Small-batch decode of T = 2..kGemvMaxTokens tokens (decode_batch_fits): the same three
+// launches as the single-token path, over the union of the tokens' experts (each weight row
+// read once, applied to every token that chose it).  With topk_idx not NULL the router launch
+// is routing only (its last block writes topk_idx, topk_w, offsets, perm).
+bool decode_batch_fits(const Dims& D, int T);
+cudaError_t prepare_decode_batch_kernels();
+cudaError_t launch_decode_batch_router_shared(const __nv_bfloat16* x, const DecodeWeights& W,
+                                              const Dims& D, int T, int32_t* topk_idx,
+                                              float* topk_w, int32_t* offsets, int32_t* perm,
+                                              const DecodeWs& dw, cudaStream_t s,
+                                              bool with_shared);
+cudaError_t launch_decode_batch_gateup(const __nv_bfloat16* x, const DecodeWeights& W,
+                                       const Dims& D, int T, int32_t* topk_idx, float* topk_w,
+                                       const DecodeWs& dw, int sms, cudaStream_t s);
+cudaError_t launch_decode_batch_down_combine(const DecodeWeights& W, const Dims& D, int T,
+                                             const DecodeWs& dw, __nv_bfloat16* y, int sms,
+                                             cudaStream_t s);
 
 }  // namespace moe

@@ -255,12 +255,45 @@ def test_deterministic_and_host_entry_point():
     L.close()
 
 
-def test_gemv_schedule_rejects_more_than_one_token():
-    c = build_case("gemv-t2", d=512, f=128, fs=128, T=2, seed=4)
-    W, x = to_device(c)
-    L = moe.MoeLayer(W, 4, schedule=moe.MOE_SCHEDULE_GEMV)
+def test_gemv_schedule_rejects_shapes_it_does_not_fit():
     import torch
+    c = build_case("gemv-t9", d=512, f=128, fs=128, T=9, seed=4)
+    W, x = to_device(c)
+    L = moe.MoeLayer(W, 16, schedule=moe.MOE_SCHEDULE_GEMV)
     y = torch.empty_like(x)
-    assert moe.moe_forward(L.handle, x.data_ptr(), 2, y.data_ptr(), None) == \
+    assert moe.moe_forward(L.handle, x.data_ptr(), 9, y.data_ptr(), None) == \
         moe.MOE_ERR_UNSUPPORTED
     L.close()
+    # 3 tokens x max(f, fs) = 2048 is past the per-block h copy: GEMV rejects, AUTO falls back
+    c = build_case("gemv-wide", d=512, f=2048, fs=128, T=3, seed=4, full_host=False)
+    W, x = to_device(c)
+    L = moe.MoeLayer(W, 3, schedule=moe.MOE_SCHEDULE_GEMV)
+    y = torch.empty_like(x)
+    assert moe.moe_forward(L.handle, x.data_ptr(), 3, y.data_ptr(), None) == \
+        moe.MOE_ERR_UNSUPPORTED
+    L.close()
+    got = _run(c, moe.MOE_SCHEDULE_AUTO)
+    _check_routing(c, got)
+    assert_close(got["y"], oracle_outputs(c), "wide T=3 through the tensor-core path")
+
+
+# Small batches (2..8 tokens, the speculative-verify shape): the matrix-vector path over the
+# union of the tokens' experts, routing bit-exact and outputs within tolerance, against the
+# oracle; the same tokens through the tensor-core path agree too.
+@pytest.mark.parametrize("T", [2, 3, 5, 8])
+def test_small_batch_decode(T):
+    c = build_case("small-batch", d=512, f=128, fs=256, T=T, seed=40 + T)
+    for sched in (moe.MOE_SCHEDULE_GEMV, moe.MOE_SCHEDULE_AUTO, moe.MOE_SCHEDULE_GEMM):
+        got = _run(c, sched)
+        _check_routing(c, got)
+        assert_close(got["y"], oracle_outputs(c), f"small batch T={T} schedule {sched}")
+
+
+@pytest.mark.parametrize("T", [2, 5])
+def test_small_batch_decode_shape(T):
+    # the benchmark's decode dimensions, d=2048, f=fs=512
+    c = build_case("small-batch-decode", d=2048, f=512, fs=512, T=T, seed=7, layer=T,
+                   full_host=False)
+    got = _run(c, moe.MOE_SCHEDULE_GEMV)
+    _check_routing(c, got)
+    assert_close(got["y"], oracle_outputs(c), f"small batch decode T={T}")
