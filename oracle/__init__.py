@@ -28,6 +28,10 @@ class _Dims(ctypes.Structure):
     _fields_ = [("d", _I), ("E", _I), ("k", _I), ("f", _I), ("fs", _I)]
 
 
+class _Q4(ctypes.Structure):
+    _fields_ = [("codes", _P), ("scales", _P), ("biases", _P)]
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -44,8 +48,13 @@ def lib():
         L.oracle_expert_ffn.argtypes = [_P, _I, _P, _P, _P, _I, _P, _P]
         L.oracle_forward.argtypes = [ctypes.POINTER(_Dims), _P, _I64, _P, _P, _P, _P, _P, _P, _P,
                                      _P, _P, _I64, _P, _P, _P, _I]
+        L.oracle_dequant_q4.argtypes = [ctypes.POINTER(_Q4), _I64, _I, _P]
+        L.oracle_forward_q4.argtypes = [ctypes.POINTER(_Dims), _P, _I64, _P, _P, _P, _P, _P,
+                                        ctypes.POINTER(_Q4), ctypes.POINTER(_Q4),
+                                        ctypes.POINTER(_Q4), _P, _I64, _P, _P, _P, _I]
         for fn in ("oracle_router_logits_f64", "oracle_router_logits_f32", "oracle_select",
-                   "oracle_route_structure", "oracle_expert_ffn", "oracle_forward"):
+                   "oracle_route_structure", "oracle_expert_ffn", "oracle_forward",
+                   "oracle_dequant_q4", "oracle_forward_q4"):
             getattr(L, fn).restype = _I
         _lib = L
     return _lib
@@ -175,6 +184,61 @@ def forward(x, w_r, bias, experts, shared, k, tokens=None, nthreads=None):
                               ptrs[2], _ptr(sg), _ptr(su), _ptr(sd), _ptr(tok), n, _ptr(y),
                               _ptr(idx), _ptr(w), _threads(nthreads))
     _check(rc, "forward")
+    return y, idx, w
+
+
+def _q4(m, keep):
+    """(codes, scales, biases) arrays -> the C struct (arrays kept alive in `keep`)."""
+    c = np.ascontiguousarray(m[0], dtype=np.uint8)
+    sc, b = _u16(m[1]), _u16(m[2])
+    keep += [c, sc, b]
+    return _Q4(c.ctypes.data, sc.ctypes.data, b.ctypes.data)
+
+
+def dequant_q4(codes, scales, biases):
+    """fp32 weights [rows][K] of a 4-bit group-affine matrix (codes [rows][K/2] uint8,
+    scales/biases [rows][K/64] bf16 bits)."""
+    keep = []
+    m = _q4((codes, scales, biases), keep)
+    rows, K = int(np.prod(codes.shape[:-1])), codes.shape[-1] * 2
+    out = np.empty((rows, K), dtype=np.float32)
+    _check(lib().oracle_dequant_q4(ctypes.byref(m), rows, K, _ptr(out)), "dequant_q4")
+    return out.reshape(codes.shape[:-1] + (K,))
+
+
+def forward_q4(x, w_r, bias, experts, shared, k, tokens=None, nthreads=None):
+    """forward() with 4-bit experts.  experts: {e: (gate, up, down)} holding at least every
+    expert the listed tokens select, each matrix a (codes, scales, biases) triple; shared: the
+    shared expert's three triples.  Returns (y [n][d] uint16, topk_idx, topk_w)."""
+    x, w_r = _u16(x), _u16(w_r)
+    T, d = x.shape
+    E = w_r.shape[0]
+    keep = []
+    arrs = [(_Q4 * E)(), (_Q4 * E)(), (_Q4 * E)()]
+    f = None
+    for e, mats in experts.items():
+        for q in range(3):
+            arrs[q][int(e)] = _q4(mats[q], keep)
+        f = np.asarray(mats[0][0]).shape[-2]
+    sg, su, sd = (_q4(m, keep) for m in shared)
+    fs = np.asarray(shared[0][0]).shape[-2]
+    if f is None:
+        f = fs
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    if tokens is None:
+        tok, n = None, T
+    else:
+        tok = np.ascontiguousarray(tokens, dtype=np.int64)
+        n = tok.shape[0]
+    y = np.empty((n, d), dtype=np.uint16)
+    idx = np.empty((n, k), dtype=np.int32)
+    w = np.empty((n, k), dtype=np.float32)
+    dims = _Dims(d, E, k, f, fs)
+    rc = lib().oracle_forward_q4(ctypes.byref(dims), _ptr(x), T, _ptr(w_r), _ptr(b), arrs[0],
+                                 arrs[1], arrs[2], ctypes.byref(sg), ctypes.byref(su),
+                                 ctypes.byref(sd), _ptr(tok), n, _ptr(y), _ptr(idx), _ptr(w),
+                                 _threads(nthreads))
+    _check(rc, "forward_q4")
     return y, idx, w
 
 

@@ -83,22 +83,91 @@ void logits_row_f32(const uint16_t* xr, int d, const uint16_t* w_r, int E, const
   }
 }
 
-void expert_row(const uint16_t* xr, int d, const uint16_t* wg, const uint16_t* wu,
-                const uint16_t* wd, int f, float* h, float* o) {
+// Weight (r, i) of a bf16 matrix with rows of K elements: the bf16 value widened exactly.
+struct Bf16Mat {
+  const uint16_t* p;
+  int K;
+  float operator()(int64_t r, int i) const { return widen(p[r * K + i]); }
+};
+
+// Weight (r, i) of a 4-bit group-affine matrix with rows of K elements: code q = nibble i of
+// the row (two per byte, the lower nibble first), group g = i / 64; weight = scale_g * q +
+// bias_g, one fp32 multiply and one fp32 add.
+struct Q4Mat {
+  oracle_q4 m;
+  int K;
+  float operator()(int64_t r, int i) const {
+    const uint8_t b = m.codes[r * (K / 2) + i / 2];
+    const int q = (i & 1) ? (b >> 4) : (b & 15);
+    const int64_t g = r * (K / 64) + i / 64;
+    return widen(m.scales[g]) * (float)q + widen(m.biases[g]);
+  }
+};
+
+// One SwiGLU expert on one row: h[c] = silu(gate_c . x) * (up_c . x) over the d inputs in
+// ascending order, then o[n] = down_n . h over the f features in ascending order.
+template <class W>
+void expert_row_t(const uint16_t* xr, int d, const W& wg, const W& wu, const W& wd, int f,
+                  float* h, float* o) {
   for (int c = 0; c < f; ++c) {
     float g = 0.0f, u = 0.0f;
-    const uint16_t* gr = wg + (int64_t)c * d;
-    const uint16_t* ur = wu + (int64_t)c * d;
-    for (int i = 0; i < d; ++i) g += widen(xr[i]) * widen(gr[i]);
-    for (int i = 0; i < d; ++i) u += widen(xr[i]) * widen(ur[i]);
+    for (int i = 0; i < d; ++i) g += widen(xr[i]) * wg(c, i);
+    for (int i = 0; i < d; ++i) u += widen(xr[i]) * wu(c, i);
     h[c] = swiglu(g, u);
   }
   for (int n = 0; n < d; ++n) {
-    const uint16_t* dr = wd + (int64_t)n * f;
     float acc = 0.0f;
-    for (int c = 0; c < f; ++c) acc += h[c] * widen(dr[c]);
+    for (int c = 0; c < f; ++c) acc += h[c] * wd(n, c);
     o[n] = acc;
   }
+}
+
+void expert_row(const uint16_t* xr, int d, const uint16_t* wg, const uint16_t* wu,
+                const uint16_t* wd, int f, float* h, float* o) {
+  expert_row_t(xr, d, Bf16Mat{wg, d}, Bf16Mat{wu, d}, Bf16Mat{wd, f}, f, h, o);
+}
+
+// The layer's output rows for the listed tokens; expert(e, &g, &u, &dn) gives expert e's
+// weights (false: not supplied); shared() the shared expert's.
+template <class GetExpert, class W>
+int forward_t(const oracle_dims* D, const uint16_t* x, int64_t T, const uint16_t* w_r,
+              const float* bias, GetExpert expert, const W& sg, const W& su, const W& sd,
+              const int64_t* tokens, int64_t n_tokens, uint16_t* y, int32_t* topk_idx,
+              float* topk_w, int nthreads) {
+  const int d = D->d, E = D->E, k = D->k, f = D->f, fs = D->fs;
+  if (!tokens) n_tokens = T;
+  for (int64_t r = 0; r < n_tokens; ++r) {
+    int64_t t = tokens ? tokens[r] : r;
+    if (t < 0 || t >= T) return -1;
+  }
+  std::vector<int> bad(n_tokens, 0);
+  parallel_for(n_tokens, nthreads, [&](int64_t r) {
+    int64_t t = tokens ? tokens[r] : r;
+    const uint16_t* xr = x + t * d;
+    std::vector<float> logits(E), w(k), h(std::max(f, fs)), o(d), acc(d, 0.0f);
+    std::vector<int32_t> idx(k);
+    logits_row_f32(xr, d, w_r, E, bias, logits.data());
+    select_row(logits.data(), E, k, idx.data(), w.data());
+    for (int j = 0; j < k; ++j) {  // routed experts in ascending id, weighted
+      W g, u, dn;
+      if (!expert(idx[j], &g, &u, &dn)) {
+        bad[r] = 1;
+        return;
+      }
+      expert_row_t(xr, d, g, u, dn, f, h.data(), o.data());
+      for (int n = 0; n < d; ++n) acc[n] += w[j] * o[n];
+    }
+    expert_row_t(xr, d, sg, su, sd, fs, h.data(), o.data());  // shared, weight 1
+    for (int n = 0; n < d; ++n) acc[n] += o[n];
+    for (int n = 0; n < d; ++n) y[r * d + n] = round_bf16(acc[n]);
+    if (topk_idx)
+      for (int j = 0; j < k; ++j) topk_idx[r * k + j] = idx[j];
+    if (topk_w)
+      for (int j = 0; j < k; ++j) topk_w[r * k + j] = w[j];
+  });
+  for (int64_t r = 0; r < n_tokens; ++r)
+    if (bad[r]) return -3;  // a selected expert's weights were not supplied
+  return 0;
 }
 
 }  // namespace
@@ -177,40 +246,48 @@ int oracle_forward(const oracle_dims* D, const uint16_t* x, int64_t T, const uin
     return -1;
   if (T < 0 || !x || !w_r || !w_gate || !w_up || !w_down || !ws_gate || !ws_up || !ws_down || !y)
     return -1;
-  const int d = D->d, E = D->E, k = D->k, f = D->f, fs = D->fs;
-  if (!tokens) n_tokens = T;
-  for (int64_t r = 0; r < n_tokens; ++r) {
-    int64_t t = tokens ? tokens[r] : r;
-    if (t < 0 || t >= T) return -1;
-  }
-  std::vector<int> bad(n_tokens, 0);
-  parallel_for(n_tokens, nthreads, [&](int64_t r) {
-    int64_t t = tokens ? tokens[r] : r;
-    const uint16_t* xr = x + t * d;
-    std::vector<float> logits(E), w(k), h(std::max(f, fs)), o(d), acc(d, 0.0f);
-    std::vector<int32_t> idx(k);
-    logits_row_f32(xr, d, w_r, E, bias, logits.data());
-    select_row(logits.data(), E, k, idx.data(), w.data());
-    for (int j = 0; j < k; ++j) {  // routed experts in ascending id, weighted
-      int e = idx[j];
-      if (!w_gate[e] || !w_up[e] || !w_down[e]) {
-        bad[r] = 1;
-        return;
-      }
-      expert_row(xr, d, w_gate[e], w_up[e], w_down[e], f, h.data(), o.data());
-      for (int n = 0; n < d; ++n) acc[n] += w[j] * o[n];
-    }
-    expert_row(xr, d, ws_gate, ws_up, ws_down, fs, h.data(), o.data());  // shared, weight 1
-    for (int n = 0; n < d; ++n) acc[n] += o[n];
-    for (int n = 0; n < d; ++n) y[r * d + n] = round_bf16(acc[n]);
-    if (topk_idx)
-      for (int j = 0; j < k; ++j) topk_idx[r * k + j] = idx[j];
-    if (topk_w)
-      for (int j = 0; j < k; ++j) topk_w[r * k + j] = w[j];
-  });
-  for (int64_t r = 0; r < n_tokens; ++r)
-    if (bad[r]) return -3;  // a selected expert's weights were not supplied
+  const int d = D->d, f = D->f, fs = D->fs;
+  auto expert = [&](int e, Bf16Mat* g, Bf16Mat* u, Bf16Mat* dn) {
+    if (!w_gate[e] || !w_up[e] || !w_down[e]) return false;
+    *g = Bf16Mat{w_gate[e], d};
+    *u = Bf16Mat{w_up[e], d};
+    *dn = Bf16Mat{w_down[e], f};
+    return true;
+  };
+  return forward_t(D, x, T, w_r, bias, expert, Bf16Mat{ws_gate, d}, Bf16Mat{ws_up, d},
+                   Bf16Mat{ws_down, fs}, tokens, n_tokens, y, topk_idx, topk_w, nthreads);
+}
+
+int oracle_dequant_q4(const oracle_q4* m, int64_t rows, int K, float* out) {
+  if (!m || !m->codes || !m->scales || !m->biases || !out || rows < 0 || K <= 0 || K % 64)
+    return -1;
+  const Q4Mat w{*m, K};
+  for (int64_t r = 0; r < rows; ++r)
+    for (int i = 0; i < K; ++i) out[r * K + i] = w(r, i);
   return 0;
+}
+
+int oracle_forward_q4(const oracle_dims* D, const uint16_t* x, int64_t T, const uint16_t* w_r,
+                      const float* bias, const oracle_q4* w_gate, const oracle_q4* w_up,
+                      const oracle_q4* w_down, const oracle_q4* ws_gate, const oracle_q4* ws_up,
+                      const oracle_q4* ws_down, const int64_t* tokens, int64_t n_tokens,
+                      uint16_t* y, int32_t* topk_idx, float* topk_w, int nthreads) {
+  if (!D || D->d <= 0 || D->E <= 0 || D->k <= 0 || D->k > D->E || D->f <= 0 || D->fs <= 0)
+    return -1;
+  if (D->d % 64 || D->f % 64 || D->fs % 64) return -1;
+  if (T < 0 || !x || !w_r || !w_gate || !w_up || !w_down || !ws_gate || !ws_up || !ws_down || !y)
+    return -1;
+  if (!ws_gate->codes || !ws_up->codes || !ws_down->codes) return -1;
+  const int d = D->d, f = D->f, fs = D->fs;
+  auto expert = [&](int e, Q4Mat* g, Q4Mat* u, Q4Mat* dn) {
+    if (!w_gate[e].codes || !w_up[e].codes || !w_down[e].codes) return false;
+    *g = Q4Mat{w_gate[e], d};
+    *u = Q4Mat{w_up[e], d};
+    *dn = Q4Mat{w_down[e], f};
+    return true;
+  };
+  return forward_t(D, x, T, w_r, bias, expert, Q4Mat{*ws_gate, d}, Q4Mat{*ws_up, d},
+                   Q4Mat{*ws_down, fs}, tokens, n_tokens, y, topk_idx, topk_w, nthreads);
 }
 
 }  // extern "C"

@@ -69,6 +69,28 @@ int oracle_forward(const oracle_dims* D, const uint16_t* x, int64_t T, const uin
                    const uint16_t* ws_down, const int64_t* tokens, int64_t n_tokens, uint16_t* y,
                    int32_t* topk_idx, float* topk_w, int nthreads);
 
+/* 4-bit group-affine matrix with rows of K inputs (K a multiple of 64): codes [rows][K/2]
+ * (two 4-bit codes per byte, the lower nibble first), scales and biases [rows][K/64] bf16.
+ * Weight (r, i) = scales[r][i/64] * q + biases[r][i/64] in fp32 (one multiply, one add), q the
+ * code of input i (§ "Dequantize weights during matrix multiplication": 4-bit weights in
+ * groups with a scale and a bias). */
+typedef struct {
+  const uint8_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+} oracle_q4;
+
+/* The dequantized fp32 weights of a 4-bit matrix, out [rows][K]. */
+int oracle_dequant_q4(const oracle_q4* m, int64_t rows, int K, float* out);
+
+/* oracle_forward with 4-bit experts: w_gate/w_up/w_down are arrays of E matrices (codes NULL
+ * for an expert no listed token selects); the router stays bf16. */
+int oracle_forward_q4(const oracle_dims* D, const uint16_t* x, int64_t T, const uint16_t* w_r,
+                      const float* bias, const oracle_q4* w_gate, const oracle_q4* w_up,
+                      const oracle_q4* w_down, const oracle_q4* ws_gate, const oracle_q4* ws_up,
+                      const oracle_q4* ws_down, const int64_t* tokens, int64_t n_tokens,
+                      uint16_t* y, int32_t* topk_idx, float* topk_w, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,6 +15,11 @@ dimension contiguous, like a linear layer's weight matrix):
   ws_gate, ws_up [fs][d], ws_down [d][fs]   sigma 0.02 (the shared expert)
 Element (r, c) of a tensor is element r*cols + c of its stream, so any expert or row range
 can be produced on its own.
+
+4-bit group-affine experts (the same names, one group per 64 inputs of a row): codes
+[rows][K/2] uint8 (two codes per byte, the lower nibble first), scales and biases
+[rows][K/64] bf16, with K the row length (d for gate/up, f or fs for down); the dequantized
+weight is scale*q + bias (see synth.h for how they are drawn).
 """
 import ctypes
 import os
@@ -57,6 +62,20 @@ def lib():
         L.synth_permutation.restype = None
         L.synth_permutation.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_int32,
                                         ctypes.c_void_p]
+        L.synth_bytes.restype = None
+        L.synth_bytes.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                  ctypes.c_uint64, ctypes.c_void_p]
+        L.synth_q4_affine.restype = None
+        L.synth_q4_affine.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                      ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p,
+                                      ctypes.c_void_p]
+        L.synth_bytes_device.restype = ctypes.c_int
+        L.synth_bytes_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                         ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
+        L.synth_q4_affine_device.restype = ctypes.c_int
+        L.synth_q4_affine_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                             ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p]
         L.synth_normal_bf16_device.restype = ctypes.c_int
         L.synth_normal_bf16_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
                                                ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p,
@@ -164,6 +183,53 @@ def skew_bias(seed, layer, E):
     return (-2.4 * np.log(rank)).astype(np.float32)
 
 
+# 4-bit weights: stream ids of the codes and of the scales/biases of tensor t
+Q4_CODES, Q4_AFFINE = 16, 32
+Q4_GROUP = 64
+Q4_BASE = 0.02 / 4.61  # spread of s*(q - 8), q uniform on 0..15: 4.61 s
+Q4_NAMES = tuple(n for n in WEIGHT_NAMES if n != "w_r")
+
+
+def q4_shapes(name, dims):
+    """(codes shape, scales/biases shape) of 4-bit tensor `name`."""
+    shape = weight_shape(name, dims)
+    K = shape[-1]
+    return shape[:-1] + (K // 2,), shape[:-1] + (K // Q4_GROUP,)
+
+
+def q4_host(seed, layer, name, dims, expert=None):
+    """(codes uint8, scales bf16 bits, biases bf16 bits) of 4-bit tensor `name` of `layer`,
+    or only expert `expert`'s slice of a routed tensor."""
+    tid = _SPEC[name][0]
+    cs, gs = q4_shapes(name, dims)
+    if expert is not None:
+        cs, gs = cs[1:], gs[1:]
+    nc, ng = int(np.prod(cs)), int(np.prod(gs))
+    oc = 0 if expert is None else int(expert) * nc
+    og = 0 if expert is None else int(expert) * ng
+    codes = np.empty(nc, dtype=np.uint8)
+    scales = np.empty(ng, dtype=np.uint16)
+    biases = np.empty(ng, dtype=np.uint16)
+    lib().synth_bytes(seed, stream_id(Q4_CODES + tid, layer), oc, nc, codes.ctypes.data)
+    lib().synth_q4_affine(seed, stream_id(Q4_AFFINE + tid, layer), og, ng, Q4_BASE,
+                          scales.ctypes.data, biases.ctypes.data)
+    return codes.reshape(cs), scales.reshape(gs), biases.reshape(gs)
+
+
+def q4_device(seed, layer, name, dims, codes_ptr, scales_ptr, biases_ptr, cuda_stream=0):
+    """Device fill of the whole 4-bit tensor `name` (the bits of q4_host)."""
+    tid = _SPEC[name][0]
+    cs, gs = q4_shapes(name, dims)
+    rc = lib().synth_bytes_device(seed, stream_id(Q4_CODES + tid, layer), 0, int(np.prod(cs)),
+                                  codes_ptr, cuda_stream)
+    if rc == 0:
+        rc = lib().synth_q4_affine_device(seed, stream_id(Q4_AFFINE + tid, layer), 0,
+                                          int(np.prod(gs)), Q4_BASE, scales_ptr, biases_ptr,
+                                          cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"synth device fill failed: cudaError {rc}")
+
+
 def bf16_to_f32(a):
     """Widen bf16 bits (uint16) to float32 exactly."""
     return (np.asarray(a, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
@@ -178,4 +244,4 @@ def f32_to_bf16(a):
 
 __all__ = ["Dims", "stream_id", "normal_bf16", "normal_bf16_device", "permutation",
            "host_weight", "device_weight", "x_rows", "skew_bias", "bf16_to_f32", "f32_to_bf16",
-           "weight_shape", "WEIGHT_NAMES"]
+           "weight_shape", "WEIGHT_NAMES", "q4_shapes", "q4_host", "q4_device", "Q4_NAMES"]

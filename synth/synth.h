@@ -48,6 +48,23 @@ void synth_permutation(uint64_t seed, uint64_t stream, int32_t n, int32_t* out);
 int synth_normal_bf16_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n,
                              float sigma, void* dst, void* cuda_stream);
 
+/* 4-bit group-affine weights (groups of 64 along a row's input dimension).
+ * Codes: byte j of a stream is byte (j mod 8) of word j/8 (little-endian), two 4-bit codes per
+ * byte, the lower nibble first.
+ * Scale and bias of group j: u = the top 23 bits of word j, v = 0.75f + float(u) * 2^-24 (one
+ * IEEE fp32 add), s = bf16_rne(v * base) (one fp32 multiply, then round to nearest even),
+ * bias = -8 s (exact in bf16).  The dequantized weight s*q + bias = s*(q - 8) is centred;
+ * base = 0.02 / 4.61 gives it the spread of the bf16 experts' N(0, 0.02). */
+void synth_bytes(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, uint8_t* out);
+void synth_q4_affine(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, float base,
+                     uint16_t* scales, uint16_t* biases);
+
+/* Device fills of the same (returns 0 or the cudaError_t of the launch). */
+int synth_bytes_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, void* dst,
+                       void* cuda_stream);
+int synth_q4_affine_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n,
+                           float base, void* scales, void* biases, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

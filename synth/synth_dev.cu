@@ -36,6 +36,33 @@ __global__ void fill_kernel(uint64_t key, uint64_t offset, uint64_t n, float sig
     dst[j] = element(key, offset + j, sigma);
 }
 
+__global__ void bytes_kernel(uint64_t key, uint64_t offset, uint64_t n, uint8_t* dst) {
+  uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride) {
+    uint64_t b = offset + j;
+    dst[j] = (uint8_t)(fin(key + ((b >> 3) + 1) * kGamma) >> (8 * (b & 7)));
+  }
+}
+
+__global__ void affine_kernel(uint64_t key, uint64_t offset, uint64_t n, float base,
+                              uint16_t* scales, uint16_t* biases) {
+  uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride) {
+    uint32_t u = (uint32_t)(fin(key + (offset + j + 1) * kGamma) >> 41);
+    float v = __fadd_rn(0.75f, __fmul_rn((float)u, 0x1p-24f));
+    uint32_t w = __float_as_uint(__fmul_rn(v, base));
+    w += 0x7FFFu + ((w >> 16) & 1u);
+    uint16_t sb = (uint16_t)(w >> 16);
+    scales[j] = sb;
+    biases[j] = (uint16_t)((uint16_t)(sb ^ 0x8000u) + (uint16_t)(3u << 7));
+  }
+}
+
+unsigned grid_for(uint64_t n) {
+  uint64_t blocks = (n + 255) / 256;
+  return (unsigned)(blocks > 152ull * 32 ? 152ull * 32 : blocks);
+}
+
 }  // namespace
 
 extern "C" int synth_normal_bf16_device(uint64_t seed, uint64_t stream, uint64_t offset,
@@ -46,5 +73,21 @@ extern "C" int synth_normal_bf16_device(uint64_t seed, uint64_t stream, uint64_t
   if (blocks > 152ull * 32) blocks = 152ull * 32;
   fill_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)cuda_stream>>>(key, offset, n, sigma,
                                                                       (uint16_t*)dst);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int synth_bytes_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n,
+                                  void* dst, void* cuda_stream) {
+  if (n == 0) return 0;
+  bytes_kernel<<<grid_for(n), 256, 0, (cudaStream_t)cuda_stream>>>(synth_key(seed, stream),
+                                                                    offset, n, (uint8_t*)dst);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int synth_q4_affine_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n,
+                                      float base, void* scales, void* biases, void* cuda_stream) {
+  if (n == 0) return 0;
+  affine_kernel<<<grid_for(n), 256, 0, (cudaStream_t)cuda_stream>>>(
+      synth_key(seed, stream), offset, n, base, (uint16_t*)scales, (uint16_t*)biases);
   return (int)cudaGetLastError();
 }

@@ -91,3 +91,23 @@ void synth_permutation(uint64_t seed, uint64_t stream, int32_t n, int32_t* out) 
     out[j] = t;
   }
 }
+
+void synth_bytes(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, uint8_t* out) {
+  uint64_t key = synth_key(seed, stream);
+  for (uint64_t j = 0; j < n; ++j) {
+    uint64_t b = offset + j;
+    out[j] = (uint8_t)(synth_word(key, b >> 3) >> (8 * (b & 7)));
+  }
+}
+
+void synth_q4_affine(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, float base,
+                     uint16_t* scales, uint16_t* biases) {
+  uint64_t key = synth_key(seed, stream);
+  for (uint64_t j = 0; j < n; ++j) {
+    uint32_t u = (uint32_t)(synth_word(key, offset + j) >> 41);
+    float v = 0.75f + (float)u * 0x1p-24f;
+    uint16_t sb = f32_to_bf16_rne(v * base);
+    scales[j] = sb;
+    biases[j] = (uint16_t)(sb ^ 0x8000u) + (uint16_t)(3u << 7); /* -8 s: sign flip, exponent + 3 */
+  }
+}

@@ -24,7 +24,15 @@ MUTANTS = [
     ("bias_dropped", "out[e] = acc + (bias ? bias[e] : 0.0f);", "out[e] = acc;"),
     ("router_transposed", "const uint16_t* wr = w_r + (int64_t)e * d;\n    float acc = 0.0f;\n    for (int i = 0; i < d; ++i) acc += widen(xr[i]) * widen(wr[i]);",
      "float acc = 0.0f;\n    for (int i = 0; i < d; ++i) acc += widen(xr[i]) * widen(w_r[(int64_t)i * E + e]);"),
-    ("down_transposed", "acc += h[c] * widen(dr[c]);", "acc += h[c] * widen(wd[(int64_t)c * d + n]);"),
+    ("down_transposed", "for (int c = 0; c < f; ++c) acc += h[c] * wd(n, c);",
+     "for (int c = 0; c < f; ++c) acc += h[c] * wd(c, n);"),
+    # 4-bit weights: nibble order, group index, the bias term
+    ("q4_nibbles_swapped", "const int q = (i & 1) ? (b >> 4) : (b & 15);",
+     "const int q = (i & 1) ? (b & 15) : (b >> 4);"),
+    ("q4_group_of_32", "const int64_t g = r * (K / 64) + i / 64;",
+     "const int64_t g = r * (K / 64) + (i / 32) % (K / 64);"),
+    ("q4_bias_dropped", "return widen(m.scales[g]) * (float)q + widen(m.biases[g]);",
+     "return widen(m.scales[g]) * (float)q;"),
     ("shared_dropped", "for (int n = 0; n < d; ++n) acc[n] += o[n];", "for (int n = 0; n < d; ++n) acc[n] += 0.0f * o[n];"),
     ("weight_misaligned", "acc[n] += w[j] * o[n];", "acc[n] += w[(j + 1) % k] * o[n];"),
     ("round_truncates", "u += 0x7FFFu + lsb;", "(void)lsb;"),

@@ -297,3 +297,68 @@ def test_gap_rule_redraws_and_is_reproducible():
     assert np.all(oracle.kth_gap(oracle.router_logits_f64(x, w_r), k) >= 1e-3)
     assert redraws == int(rounds.sum())
     assert np.array_equal(x, synth.x_rows(0, 0, 64, d, rounds))
+
+
+# ---------------------------------------------------------------- 4-bit group-affine weights
+# Pinned through the encoding direction: integer weights v in [-8, 7] and per-group scales
+# are packed here into codes (v + 8, two per byte, the lower nibble first) and bf16 scales and
+# biases (bias = -8 * scale); dequantizing must give v * scale back, and with power-of-two
+# scales (v * scale exact in bf16) the whole 4-bit layer must equal, bit for bit, the bf16
+# layer on those weights -- whose own pins are above.
+
+def _encode_q4(v, scales_f32, biases_f32=None):
+    """v int [rows][K] in [-8, 7]; scales [rows][K/64] -> (codes, scale bits, bias bits)."""
+    q = (np.asarray(v, dtype=np.int64) + 8).astype(np.uint8)
+    codes = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+    s = synth.f32_to_bf16(np.asarray(scales_f32, dtype=np.float32))
+    if biases_f32 is None:
+        b = synth.f32_to_bf16(-8.0 * synth.bf16_to_f32(s))
+    else:
+        b = synth.f32_to_bf16(np.asarray(biases_f32, dtype=np.float32))
+    return codes, s, b
+
+
+def _pow2_scales(rng, shape):
+    return np.ldexp(1.0, -rng.integers(6, 10, size=shape)).astype(np.float32)
+
+
+def test_q4_dequant_roundtrip():
+    rng = np.random.default_rng(11)
+    v = rng.integers(-8, 8, size=(5, 256))
+    s = _pow2_scales(rng, (5, 4))
+    got = oracle.dequant_q4(*_encode_q4(v, s))
+    assert np.array_equal(got, (v * np.repeat(s, 64, axis=1)).astype(np.float32))
+    # general biases: scale*q + bias within one fp32 rounding of the exact value
+    sc = rng.uniform(0.003, 0.006, size=(5, 4)).astype(np.float32)
+    bi = rng.uniform(-0.05, 0.05, size=(5, 4)).astype(np.float32)
+    codes, sb, bb = _encode_q4(v, sc, bi)
+    exact = (np.repeat(synth.bf16_to_f32(sb), 64, 1).astype(np.float64) * (v + 8) +
+             np.repeat(synth.bf16_to_f32(bb), 64, 1).astype(np.float64))
+    got = oracle.dequant_q4(codes, sb, bb).astype(np.float64)
+    assert np.max(np.abs(got - exact)) <= 2.0 ** -22 * np.max(np.abs(exact))
+
+
+def test_q4_layer_equals_bf16_layer_on_its_weights():
+    rng = np.random.default_rng(12)
+    d, E, f, fs, k, T = 128, 16, 64, 128, 4, 7
+    x = synth.f32_to_bf16(rng.standard_normal((T, d)).astype(np.float32))
+    w_r = synth.f32_to_bf16((0.2 * rng.standard_normal((E, d))).astype(np.float32))
+
+    def mat(rows, K):
+        v = rng.integers(-8, 8, size=(rows, K))
+        s = _pow2_scales(rng, (rows, K // 64))
+        w = synth.f32_to_bf16((v * np.repeat(s, 64, axis=1)).astype(np.float32))
+        return _encode_q4(v, s), w
+
+    experts_q4, experts_bf = {}, ([], [], [])
+    for e in range(E):
+        g, u, dn = mat(f, d), mat(f, d), mat(d, f)
+        experts_q4[e] = (g[0], u[0], dn[0])
+        for i, m in enumerate((g, u, dn)):
+            experts_bf[i].append(m[1])
+    sg, su, sd = mat(fs, d), mat(fs, d), mat(d, fs)
+    yq, iq, wq = oracle.forward_q4(x, w_r, None, experts_q4, (sg[0], su[0], sd[0]), k)
+    yb, ib, wb = oracle.forward(x, w_r, None, tuple(np.stack(a) for a in experts_bf),
+                                (sg[1], su[1], sd[1]), k)
+    assert np.array_equal(iq, ib) and np.array_equal(wq, wb)
+    assert np.array_equal(yq, yb)
