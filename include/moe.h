@@ -108,6 +108,33 @@ typedef struct {           /* device pointers, borrowed (see above) */
  * NULL and nothing stays allocated. */
 int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out);
 
+/* 4-bit group-affine matrix (§ "Dequantize weights during matrix multiplication": weights in
+ * 4 bits, in groups of 64 inputs with a scale and a bias, dequantized inside the matrix
+ * kernel).  Rows of K inputs (K a multiple of 128); weight (r, i) = scales[r][i/64] * q +
+ * biases[r][i/64], q = the 4-bit code of input i.  Device pointers, borrowed like the bf16
+ * weights, each 16-byte aligned. */
+typedef struct {
+  const void* codes;  /* uint8 [rows][K/2]: two codes per byte, input 2i in the lower nibble */
+  const void* scales; /* bf16 [rows][K/64] */
+  const void* biases; /* bf16 [rows][K/64] */
+} moe_q4_matrix;
+
+typedef struct {
+  const void* w_router;     /* bf16 [E][d]: the router stays bf16 */
+  const float* router_bias; /* fp32 [E], or NULL */
+  moe_q4_matrix w_gate;     /* E*f rows of d inputs */
+  moe_q4_matrix w_up;       /* E*f rows of d inputs */
+  moe_q4_matrix w_down;     /* E*d rows of f inputs */
+  moe_q4_matrix ws_gate;    /* fs rows of d inputs */
+  moe_q4_matrix ws_up;      /* fs rows of d inputs */
+  moe_q4_matrix ws_down;    /* d rows of fs inputs */
+} moe_weights_q4;
+
+/* moe_create for 4-bit experts.  Such a handle runs batch-1 decode (moe_forward and
+ * moe_forward_host with T == 1; the schedule must be AUTO or GEMV) and moe_route for any T;
+ * moe_forward with T > 1 returns MOE_ERR_UNSUPPORTED (the tensor-core path reads bf16). */
+int moe_create_q4(const moe_config* cfg, const moe_weights_q4* w, moe_handle* out);
+
 /* Routing only (§ "Keep expert routing on the GPU"): the same kernels moe_forward runs for
  * this T, so moe_forward's routing equals what this returns.  Device outputs, each may be
  * NULL if not wanted:

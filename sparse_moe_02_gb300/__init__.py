@@ -29,7 +29,7 @@ MOE_SCHEDULE_GEMV = 2
 
 EXPORTS = ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_get_device_error",
            "moe_destroy", "moe_status_string", "moe_last_cuda_error", "moe_profile_begin",
-           "moe_profile_end", "moe_route_one_noalloc")
+           "moe_profile_end", "moe_route_one_noalloc", "moe_create_q4")
 
 # kernel order reported by moe_profile_end
 KERNELS_GEMM = ("router_topk", "route_plan_scatter", "experts", "combine")
@@ -50,6 +50,17 @@ class moe_weights(ctypes.Structure):
                 ("ws_up", _c_void_p), ("ws_down", _c_void_p)]
 
 
+class moe_q4_matrix(ctypes.Structure):
+    _fields_ = [("codes", _c_void_p), ("scales", _c_void_p), ("biases", _c_void_p)]
+
+
+class moe_weights_q4(ctypes.Structure):
+    _fields_ = [("w_router", _c_void_p), ("router_bias", _c_void_p),
+                ("w_gate", moe_q4_matrix), ("w_up", moe_q4_matrix), ("w_down", moe_q4_matrix),
+                ("ws_gate", moe_q4_matrix), ("ws_up", moe_q4_matrix),
+                ("ws_down", moe_q4_matrix)]
+
+
 _lib = None
 
 
@@ -62,6 +73,8 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         L.moe_create.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights),
                                  ctypes.POINTER(_c_void_p)]
+        L.moe_create_q4.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights_q4),
+                                    ctypes.POINTER(_c_void_p)]
         L.moe_route.argtypes = [_c_void_p, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                 _c_void_p, _c_void_p]
         L.moe_forward.argtypes = [_c_void_p, _c_void_p, _c_int, _c_void_p, _c_void_p]
@@ -76,7 +89,7 @@ def lib():
                                       ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]
         L.moe_route_one_noalloc.argtypes = [_c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                             _c_void_p, _c_void_p]
-        for fn in ("moe_create", "moe_route", "moe_forward", "moe_forward_host",
+        for fn in ("moe_create", "moe_create_q4", "moe_route", "moe_forward", "moe_forward_host",
                    "moe_get_device_error", "moe_destroy", "moe_last_cuda_error",
                    "moe_profile_begin", "moe_profile_end", "moe_route_one_noalloc"):
             getattr(L, fn).restype = _c_int
@@ -88,6 +101,13 @@ def moe_create(cfg, weights):
     """Returns (status, handle)."""
     h = _c_void_p()
     st = lib().moe_create(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(h))
+    return st, h
+
+
+def moe_create_q4(cfg, weights_q4):
+    """Returns (status, handle) for 4-bit experts (moe_weights_q4)."""
+    h = _c_void_p()
+    st = lib().moe_create_q4(ctypes.byref(cfg), ctypes.byref(weights_q4), ctypes.byref(h))
     return st, h
 
 
@@ -163,6 +183,9 @@ class MoeLayer:
     """
 
     def __init__(self, weights, max_tokens, schedule=MOE_SCHEDULE_AUTO, chunk_tokens=0):
+        if isinstance(weights["w_gate"], tuple):
+            self._init_q4(weights, max_tokens, schedule, chunk_tokens)
+            return
         E, f, d = weights["w_gate"].shape
         fs = weights["ws_gate"].shape[0]
         self.d, self.f, self.fs, self.E, self.k = d, f, fs, E, 8
@@ -175,6 +198,27 @@ class MoeLayer:
                         _ptr(weights["ws_down"]))
         st, self.handle = moe_create(cfg, w)
         _check(st, "moe_create")
+
+    def _init_q4(self, weights, max_tokens, schedule, chunk_tokens):
+        """4-bit experts: each expert tensor is a (codes uint8, scales bf16, biases bf16)
+        triple of torch tensors, shapes as in synth.q4_shapes; w_router stays bf16."""
+        codes = weights["w_gate"][0]
+        E, f, d = codes.shape[0], codes.shape[1], codes.shape[2] * 2
+        fs = weights["ws_gate"][0].shape[0]
+        self.d, self.f, self.fs, self.E, self.k = d, f, fs, E, 8
+        self.max_tokens = max_tokens
+        self._weights = weights
+
+        def m(name):
+            c, sc, b = weights[name]
+            return moe_q4_matrix(_ptr(c), _ptr(sc), _ptr(b))
+
+        cfg = moe_config(d, E, 8, f, fs, max_tokens, schedule, chunk_tokens)
+        w = moe_weights_q4(_ptr(weights["w_router"]), _ptr(weights.get("router_bias")),
+                           m("w_gate"), m("w_up"), m("w_down"), m("ws_gate"), m("ws_up"),
+                           m("ws_down"))
+        st, self.handle = moe_create_q4(cfg, w)
+        _check(st, "moe_create_q4")
 
     @staticmethod
     def _stream(stream):

@@ -61,7 +61,9 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 struct moe_handle_s {
   moe_config cfg;
-  moe_weights w;
+  moe_weights w;       // bf16 handle: the weights; 4-bit handle: only w_router, router_bias
+  bool q4 = false;     // 4-bit experts (batch-1 decode only)
+  moe::Q4Weights wq{};
   Dims D;
   int device = 0, sms = 0;
   int P_max = 0, max_units_gu = 0, max_units_dn = 0, max_chunks = 0;
@@ -109,6 +111,26 @@ int check_weights(const moe_weights* w) {
   }
   if (w->router_bias && !aligned4(w->router_bias)) return MOE_ERR_ALIGNMENT;
   return MOE_OK;
+}
+
+int check_q4(const moe_weights_q4* w) {
+  if (!w || !w->w_router) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w->w_router)) return MOE_ERR_ALIGNMENT;
+  if (w->router_bias && !aligned4(w->router_bias)) return MOE_ERR_ALIGNMENT;
+  const moe_q4_matrix* ms[] = {&w->w_gate, &w->w_up, &w->w_down, &w->ws_gate, &w->ws_up,
+                               &w->ws_down};
+  for (const moe_q4_matrix* m : ms) {
+    if (!m->codes || !m->scales || !m->biases) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(m->codes) || !aligned16(m->scales) || !aligned16(m->biases))
+      return MOE_ERR_ALIGNMENT;
+  }
+  return MOE_OK;
+}
+
+moe::Q4Matrix q4_matrix(const moe_q4_matrix& m) {
+  return moe::Q4Matrix{static_cast<const uint8_t*>(m.codes),
+                       static_cast<const __nv_bfloat16*>(m.scales),
+                       static_cast<const __nv_bfloat16*>(m.biases)};
 }
 
 // Bump allocator over the single workspace allocation (256-byte aligned pieces).
@@ -243,17 +265,35 @@ int forward_gemm(moe_handle h, const __nv_bfloat16* xd, int T, __nv_bfloat16* yd
 
 extern "C" {
 
-int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
+}  // extern "C"
+
+namespace {
+
+// moe_create and moe_create_q4: exactly one of w (bf16 experts) and wq (4-bit experts).
+int create_handle(const moe_config* cfg, const moe_weights* w, const moe_weights_q4* wq,
+                  moe_handle* out) {
   if (!out) return MOE_ERR_INVALID_ARG;
   *out = nullptr;
   int st = check_config(cfg);
   if (st) return st;
-  if ((st = check_weights(w))) return st;
+  if ((st = w ? check_weights(w) : check_q4(wq))) return st;
+  if (wq && cfg->schedule == MOE_SCHEDULE_GEMM) return MOE_ERR_UNSUPPORTED;
 
   moe_handle_s* h = new (std::nothrow) moe_handle_s();
   if (!h) return MOE_ERR_NO_MEMORY;
   h->cfg = *cfg;
-  h->w = *w;
+  if (w) {
+    h->w = *w;
+  } else {
+    h->q4 = true;
+    h->w = moe_weights{};
+    h->w.w_router = wq->w_router;
+    h->w.router_bias = wq->router_bias;
+    h->wq = moe::Q4Weights{static_cast<const __nv_bfloat16*>(wq->w_router), wq->router_bias,
+                           q4_matrix(wq->w_gate), q4_matrix(wq->w_up), q4_matrix(wq->w_down),
+                           q4_matrix(wq->ws_gate), q4_matrix(wq->ws_up),
+                           q4_matrix(wq->ws_down)};
+  }
   h->D = Dims{cfg->d, cfg->ffn_dim, cfg->shared_ffn_dim,
               cfg->ffn_dim > cfg->shared_ffn_dim ? cfg->ffn_dim : cfg->shared_ffn_dim};
   auto fail = [&](int status) {
@@ -294,22 +334,45 @@ int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
   if ((st = cuda_status(cudaMemset(h->ws, 0, total)))) return fail(st);
 
   const Dims& D = h->D;
-  bool ok = encode_2d(&h->tm_wr, w->w_router, D.d, kE, moe::kBK, kE) &&
-            encode_2d(&h->tm_wg, w->w_gate, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
+  bool ok = encode_2d(&h->tm_wr, h->w.w_router, D.d, kE, moe::kBK, kE) &&
+            encode_2d(&h->tm_h, h->h, D.hdim, h->P_chunk, moe::kBK, 16);
+  // the tensor-core path's maps of the bf16 experts
+  ok = ok && (h->q4 ||
+             (encode_2d(&h->tm_wg, w->w_gate, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wu, w->w_up, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wsg, w->ws_gate, D.d, D.fs, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wsu, w->ws_up, D.d, D.fs, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wd, w->w_down, D.f, (uint64_t)kE * D.d, moe::kBK, moe::kMTile) &&
-            encode_2d(&h->tm_wsd, w->ws_down, D.fs, D.d, moe::kBK, moe::kMTile) &&
-            encode_2d(&h->tm_h, h->h, D.hdim, h->P_chunk, moe::kBK, 16);
+            encode_2d(&h->tm_wsd, w->ws_down, D.fs, D.d, moe::kBK, moe::kMTile)));
   if (!ok) return fail(MOE_ERR_CUDA);
   if ((st = cuda_status(moe::prepare_route_kernels()))) return fail(st);
   if ((st = cuda_status(moe::prepare_expert_kernels()))) return fail(st);
   if ((st = cuda_status(moe::prepare_decode_kernels(D.hdim)))) return fail(st);
   if ((st = cuda_status(moe::prepare_decode_batch_kernels()))) return fail(st);
+  if ((st = cuda_status(moe::prepare_decode_q4_kernels()))) return fail(st);
   if ((st = cuda_status(cudaDeviceSynchronize()))) return fail(st);
   *out = h;
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_create(const moe_config* cfg, const moe_weights* w, moe_handle* out) {
+  if (!w) {
+    if (out) *out = nullptr;
+    return MOE_ERR_INVALID_ARG;
+  }
+  return create_handle(cfg, w, nullptr, out);
+}
+
+int moe_create_q4(const moe_config* cfg, const moe_weights_q4* w, moe_handle* out) {
+  if (!w) {
+    if (out) *out = nullptr;
+    return MOE_ERR_INVALID_ARG;
+  }
+  return create_handle(cfg, nullptr, w, out);
 }
 
 int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w,
@@ -346,6 +409,22 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* xd = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* yd = static_cast<__nv_bfloat16*>(y);
+
+  if (h->q4) {  // 4-bit experts: batch-1 decode only
+    if (T != 1) return MOE_ERR_UNSUPPORTED;
+    if ((st = prof_mark(h, s, 0))) return st;
+    if ((st = cuda_status(moe::launch_decode_q4_router_shared(xd, h->wq, h->D, h->dws, s))))
+      return st;
+    if ((st = prof_mark(h, s, 1))) return st;
+    if ((st = cuda_status(moe::launch_decode_q4_gateup(xd, h->wq, h->D, h->rws.topk_idx,
+                                                       h->rws.topk_w, h->dws, h->sms, s))))
+      return st;
+    if ((st = prof_mark(h, s, 2))) return st;
+    if ((st = cuda_status(moe::launch_decode_q4_down_combine(h->wq, h->D, h->dws, yd, h->sms,
+                                                             s))))
+      return st;
+    return prof_finish_call(h, s, 3);
+  }
 
   if (use_gemv(h, T)) {
     const moe::DecodeWeights W = decode_weights(h);

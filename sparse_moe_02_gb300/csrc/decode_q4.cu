@@ -1,0 +1,355 @@
+// Batch-1 decode with 4-bit group-affine expert weights ("Optimizing on-device inference for
+// Apple Silicon", § "Dequantize weights during matrix multiplication": 4-bit weights in groups
+// of 64 with a scale and a bias, dequantized inside the matrix kernel; § "Optimize the
+// one-row weight path"; § "Reduce intermediate and state traffic").
+//
+// Same three launches as the bf16 decode path (router + shared gate/up; the 8 selected
+// experts' gate/up with SwiGLU; down rows weighted and combined in fixed order), but every
+// expert row is 4-bit: one 16-byte load carries 32 codes, i.e. half a group, and the piece's
+// contribution is scale * sum_i q_i v_i + bias * sum_i v_i over its 32 inputs v (the sums of v
+// per 32 inputs are formed once per block).  The router stays bf16.  Codes are turned into
+// floats exactly: 0x4B000000 | q is the float 2^23 + q.
+#include <algorithm>
+
+#include "layer.cuh"
+#include "ptx.cuh"
+#include "select.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kQWarps = 8;  // warps per block in every 4-bit decode kernel
+constexpr int kQB = 2;      // 16-byte code pieces per lane and row held in flight
+
+__device__ __forceinline__ float nib(uint32_t u, int n) {
+  return __uint_as_float(0x4B000000u | ((u >> (4 * n)) & 15u)) - 8388608.0f;
+}
+
+// 32 consecutive codes (the lower nibble of a byte first) times v[0..32): sum_i q_i v_i.
+__device__ __forceinline__ float q4_dot32(uint4 c, const float* v) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float4 a = *reinterpret_cast<const float4*>(v + 8 * k);
+    const float4 b = *reinterpret_cast<const float4*>(v + 8 * k + 4);
+    s = fmaf(nib(w[k], 0), a.x, s);
+    s = fmaf(nib(w[k], 1), a.y, s);
+    s = fmaf(nib(w[k], 2), a.z, s);
+    s = fmaf(nib(w[k], 3), a.w, s);
+    s = fmaf(nib(w[k], 4), b.x, s);
+    s = fmaf(nib(w[k], 5), b.y, s);
+    s = fmaf(nib(w[k], 6), b.z, s);
+    s = fmaf(nib(w[k], 7), b.w, s);
+  }
+  return s;
+}
+
+__device__ __forceinline__ float ld_bf16(const __nv_bfloat16* p) {
+  unsigned short u;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(u) : "l"(p));
+  return __uint_as_float((uint32_t)u << 16);
+}
+
+__device__ __forceinline__ float warp_sum_q(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Up to kQB pieces per lane of one 4-bit row of np pieces: piece p = p0 + lane + 32 i, with
+// its group's scale and bias.
+struct Q4Frag {
+  uint4 c[kQB];
+  float s[kQB], b[kQB];
+};
+
+__device__ __forceinline__ void q4_load(Q4Frag& r, const Q4Row& row, int np, int lane, int p0) {
+#pragma unroll
+  for (int i = 0; i < kQB; ++i) {
+    const int p = p0 + lane + 32 * i;
+    if (p < np) {
+      r.c[i] = ld_stream_u4(row.codes + (size_t)p * 16);
+      r.s[i] = ld_bf16(row.scales + p / 2);
+      r.b[i] = ld_bf16(row.biases + p / 2);
+    }
+  }
+}
+
+// Lane-partial of row . v for the pieces in r (v and its per-32 sums vs in shared memory).
+__device__ __forceinline__ float q4_dot(const Q4Frag& r, const float* v, const float* vs, int np,
+                                        int lane, int p0) {
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kQB; ++i) {
+    const int p = p0 + lane + 32 * i;
+    if (p < np) acc += r.s[i] * q4_dot32(r.c[i], v + 32 * p) + r.b[i] * vs[p];
+  }
+  return acc;
+}
+
+// Lane-partial of row . v over the whole row; the first kQB*32 pieces already in r.
+__device__ __forceinline__ float q4_dot_rest(Q4Frag& r, const Q4Row& row, const float* v,
+                                             const float* vs, int np, int lane) {
+  float acc = q4_dot(r, v, vs, np, lane, 0);
+  for (int p0 = kQB * 32; p0 < np; p0 += kQB * 32) {
+    q4_load(r, row, np, lane, p0);
+    acc += q4_dot(r, v, vs, np, lane, p0);
+  }
+  return acc;
+}
+
+// Stages v (n bf16 values, n a multiple of 32) as fp32 in vf[n] and the sums of each 32 in
+// vs[n / 32]; every thread of the block calls this (it holds barriers).
+__device__ __forceinline__ void stage_f32(const __nv_bfloat16* src, float* vf, float* vs, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) vf[i] = __bfloat162float(src[i]);
+  __syncthreads();
+  for (int p = threadIdx.x; p < n / 32; p += blockDim.x) {
+    float s = 0.f;
+    for (int i = 0; i < 32; ++i) s += vf[32 * p + i];
+    vs[p] = s;
+  }
+  __syncthreads();
+}
+
+// 8 bf16 weights times 8 fp32 values (router rows).
+__device__ __forceinline__ float dot8_bf16_f32(uint4 w, const float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(v);
+  const float4 b = *reinterpret_cast<const float4*>(v + 4);
+  float s = 0.f;
+  s = fmaf(bf16_lo(w.x), a.x, s);
+  s = fmaf(bf16_hi(w.x), a.y, s);
+  s = fmaf(bf16_lo(w.y), a.z, s);
+  s = fmaf(bf16_hi(w.y), a.w, s);
+  s = fmaf(bf16_lo(w.z), b.x, s);
+  s = fmaf(bf16_hi(w.z), b.y, s);
+  s = fmaf(bf16_lo(w.w), b.z, s);
+  return fmaf(bf16_hi(w.w), b.w, s);
+}
+
+constexpr int kRPre = 8;  // 16-byte pieces per lane of a bf16 router row held in registers
+
+struct Q4RouterSharedArgs {
+  const __nv_bfloat16* x;
+  Q4Weights W;
+  Dims D;
+  DecodeWs dw;
+};
+
+// Blocks [0, E / kQWarps): one bf16 router row per warp -> logits; blocks after: one
+// shared-expert feature per warp (its 4-bit gate and up rows) -> h_s.  Weight rows are
+// requested before waiting on the previous kernel (they do not depend on it).
+__global__ void __launch_bounds__(kQWarps * 32) dec_q4_router_shared_kernel(Q4RouterSharedArgs a) {
+  extern __shared__ float qsm[];  // x as fp32 [d], then its sums per 32 [d / 32]
+  float* xf = qsm;
+  float* xs = qsm + a.D.d;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.D.d, nch = d / 8, np = d / 32;
+  const int router_blocks = kE / kQWarps;
+  const bool router = (int)blockIdx.x < router_blocks;
+  const int e = blockIdx.x * kQWarps + warp;
+  const int c = ((int)blockIdx.x - router_blocks) * kQWarps + warp;  // shared feature
+  const __nv_bfloat16* rrow = a.W.w_r + (size_t)e * d;
+  uint4 rr[kRPre];
+  Q4Frag g, u;
+  if (router) {
+#pragma unroll
+    for (int i = 0; i < kRPre; ++i)
+      if (lane + 32 * i < nch) rr[i] = ld_stream_u4(rrow + (size_t)(lane + 32 * i) * 8);
+  } else if (c < a.D.fs) {
+    q4_load(g, a.W.s_gate.row(c, d), np, lane, 0);
+    q4_load(u, a.W.s_up.row(c, d), np, lane, 0);
+  }
+  pdl_wait();  // x may be written by the previous kernel
+  pdl_trigger();
+  stage_f32(a.x, xf, xs, d);
+  if (router) {
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRPre; ++i) {
+      const int cc = lane + 32 * i;
+      if (cc < nch) acc += dot8_bf16_f32(rr[i], xf + cc * 8);
+    }
+    for (int cc = lane + 32 * kRPre; cc < nch; cc += 32)
+      acc += dot8_bf16_f32(ld_stream_u4(rrow + (size_t)cc * 8), xf + cc * 8);
+    acc = warp_sum_q(acc);
+    if (lane == 0) a.dw.logits[e] = acc + (a.W.bias ? a.W.bias[e] : 0.f);
+  } else if (c < a.D.fs) {
+    const float gv = warp_sum_q(q4_dot_rest(g, a.W.s_gate.row(c, d), xf, xs, np, lane));
+    const float uv = warp_sum_q(q4_dot_rest(u, a.W.s_up.row(c, d), xf, xs, np, lane));
+    if (lane == 0) a.dw.hdec[(size_t)8 * a.D.hdim + c] = silu_mul(gv, uv);
+  }
+}
+
+struct Q4GateUpArgs {
+  const __nv_bfloat16* x;
+  Q4Weights W;
+  Dims D;
+  int32_t* topk_idx;  // written by block 0 (the selection behind this forward)
+  float* topk_w;
+  DecodeWs dw;
+};
+
+// Items (selected expert j, feature c), one warp per item over a resident grid:
+// h[j][c] = silu(gate . x) * (up . x) from the 4-bit gate and up rows.  Warp 0 of every
+// block selects the top 8 from the router logits first.
+__global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_gateup_kernel(Q4GateUpArgs a) {
+  extern __shared__ float qsm[];
+  float* xf = qsm;
+  float* xs = qsm + a.D.d;
+  __shared__ int s_ids[kTopK];
+  __shared__ float s_w[kTopK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.D.d, f = a.D.f, np = d / 32;
+  pdl_wait();     // the router logits come from the previous kernel
+  pdl_trigger();  // the down kernel may start selecting and streaming its rows now
+  if (warp == 0) select_top8(a.dw.logits, lane, s_ids, s_w);
+  stage_f32(a.x, xf, xs, d);
+  if (blockIdx.x == 0 && threadIdx.x < kTopK) {
+    a.topk_idx[threadIdx.x] = s_ids[threadIdx.x];
+    a.topk_w[threadIdx.x] = s_w[threadIdx.x];
+  }
+  const int nwarps = gridDim.x * kQWarps;
+  for (int it = blockIdx.x * kQWarps + warp; it < kTopK * f; it += nwarps) {
+    const int j = it / f, c = it % f;
+    const size_t r = (size_t)s_ids[j] * f + c;
+    const Q4Row rg = a.W.gate.row(r, d), ru = a.W.up.row(r, d);
+    Q4Frag g, u;
+    q4_load(g, rg, np, lane, 0);
+    q4_load(u, ru, np, lane, 0);
+    const float gv = warp_sum_q(q4_dot_rest(g, rg, xf, xs, np, lane));
+    const float uv = warp_sum_q(q4_dot_rest(u, ru, xf, xs, np, lane));
+    if (lane == 0) a.dw.hdec[(size_t)j * a.D.hdim + c] = silu_mul(gv, uv);
+  }
+}
+
+struct Q4DownArgs {
+  Q4Weights W;
+  Dims D;
+  DecodeWs dw;
+  __nv_bfloat16* y;
+};
+
+constexpr int kQDPre = 6;  // pieces per lane of one output's nine down rows held in flight
+
+// One warp per output n over a resident grid.  The nine 4-bit down rows of n (experts
+// j = 0..7 in ascending id, then the shared expert) are taken as one run of pieces, piece P of
+// routed row j = P / (f/32) or of the shared row past 8 f/32; lane l takes P = l, l+32, ...
+// and sums w_j (scale * codes . h_j + bias * sum h_j) over its pieces in that order; one warp
+// reduction gives y[n].  The top 8 is selected again from the router logits (final: the router
+// kernel completed before the gate/up kernel let this one start), so the first output's rows
+// are requested before waiting for h.
+__global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4DownArgs a) {
+  extern __shared__ float qsm[];  // h [9][hdim] fp32, then its sums per 32 [9][hdim / 32]
+  const int d = a.D.d, f = a.D.f, fs = a.D.fs, hdim = a.D.hdim;
+  float* hf = qsm;
+  float* hsum = qsm + 9 * hdim;
+  __shared__ int s_ids[kTopK];
+  __shared__ float s_w[kTopK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) select_top8(a.dw.logits, lane, s_ids, s_w);
+  __syncthreads();
+  const int npr = f / 32, nps = fs / 32, npt = 8 * npr + nps;
+  // the row of piece P of output nn: routed row j or the shared row (j = 8), piece p in it
+  auto row_of = [&](int P, int nn, int& j, int& p) {
+    if (P < 8 * npr) {
+      j = P / npr;
+      p = P - j * npr;
+      return a.W.down.row((size_t)s_ids[j] * d + nn, f);
+    }
+    j = 8;
+    p = P - 8 * npr;
+    return a.W.s_down.row((size_t)nn, fs);
+  };
+  uint4 pc[kQDPre];
+  float ps[kQDPre], pb[kQDPre];
+  auto load = [&](int P0, int nn) {
+#pragma unroll
+    for (int i = 0; i < kQDPre; ++i) {
+      const int P = P0 + lane + 32 * i;
+      if (P < npt) {
+        int j, p;
+        const Q4Row r = row_of(P, nn, j, p);
+        pc[i] = ld_stream_u4(r.codes + (size_t)p * 16);
+        ps[i] = ld_bf16(r.scales + p / 2);
+        pb[i] = ld_bf16(r.biases + p / 2);
+      }
+    }
+  };
+  const int nwarps = gridDim.x * kQWarps;
+  int n = blockIdx.x * kQWarps + warp;
+  if (n < d) load(0, n);
+  pdl_wait();  // h comes from the gate/up kernel
+  pdl_trigger();
+  for (int i = threadIdx.x; i < 9 * hdim; i += blockDim.x) hf[i] = __ldcg(a.dw.hdec + i);
+  __syncthreads();
+  for (int q = threadIdx.x; q < 9 * (hdim / 32); q += blockDim.x) {
+    float sum = 0.f;
+    for (int i = 0; i < 32; ++i) sum += hf[32 * q + i];
+    hsum[q] = sum;
+  }
+  __syncthreads();
+  for (; n < d; n += nwarps) {
+    float yv = 0.f;
+    for (int P0 = 0; P0 < npt; P0 += 32 * kQDPre) {
+      if (P0) load(P0, n);
+#pragma unroll
+      for (int i = 0; i < kQDPre; ++i) {
+        const int P = P0 + lane + 32 * i;
+        if (P < npt) {
+          int j, p;
+          row_of(P, n, j, p);
+          const float part = ps[i] * q4_dot32(pc[i], hf + (size_t)j * hdim + 32 * p) +
+                             pb[i] * hsum[j * (hdim / 32) + p];
+          yv = fmaf(j < 8 ? s_w[j] : 1.0f, part, yv);
+        }
+      }
+    }
+    yv = warp_sum_q(yv);
+    if (lane == 0) a.y[n] = __float2bfloat16_rn(yv);
+    if (n + nwarps < d) load(0, n + nwarps);
+  }
+}
+
+}  // namespace
+
+cudaError_t prepare_decode_q4_kernels() {
+  // dynamic shared memory at the largest supported shape (d = 8192, hdim = 2048)
+  cudaError_t e = cudaFuncSetAttribute(dec_q4_router_shared_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       8192 * 4 + 256 * 4);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(dec_q4_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                8192 * 4 + 256 * 4)) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(dec_q4_down_combine_kernel,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              9 * 2048 * 4 + 9 * 64 * 4);
+}
+
+cudaError_t launch_decode_q4_router_shared(const __nv_bfloat16* x, const Q4Weights& W,
+                                           const Dims& D, const DecodeWs& dw, cudaStream_t s) {
+  Q4RouterSharedArgs a{x, W, D, dw};
+  const int blocks = kE / kQWarps + (D.fs + kQWarps - 1) / kQWarps;
+  return launch_pdl(dec_q4_router_shared_kernel, dim3(blocks), dim3(kQWarps * 32),
+                    (size_t)D.d * 4 + (size_t)D.d / 32 * 4, s, a);
+}
+
+cudaError_t launch_decode_q4_gateup(const __nv_bfloat16* x, const Q4Weights& W, const Dims& D,
+                                    int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
+                                    int sms, cudaStream_t s) {
+  Q4GateUpArgs a{x, W, D, topk_idx, topk_w, dw};
+  const int grid = std::min(2 * sms, kTopK * D.f / kQWarps);
+  return launch_pdl(dec_q4_gateup_kernel, dim3(grid), dim3(kQWarps * 32),
+                    (size_t)D.d * 4 + (size_t)D.d / 32 * 4, s, a);
+}
+
+cudaError_t launch_decode_q4_down_combine(const Q4Weights& W, const Dims& D, const DecodeWs& dw,
+                                          __nv_bfloat16* y, int sms, cudaStream_t s) {
+  Q4DownArgs a{W, D, dw, y};
+  const int grid = std::min(2 * sms, (D.d + kQWarps - 1) / kQWarps);
+  return launch_pdl(dec_q4_down_combine_kernel, dim3(grid), dim3(kQWarps * 32),
+                    (size_t)9 * D.hdim * 4 + (size_t)9 * (D.hdim / 32) * 4, s, a);
+}
+
+}  // namespace moe

@@ -104,6 +104,33 @@ cudaError_t launch_combine(int T, const Dims& D, const float* topk_w, const Rout
 
 // ---------------------------------------------------------------- batch-1 decode path
 
+// ---------------------------------------------------------------- 4-bit weights
+
+// One row of a 4-bit group-affine matrix: codes (K/2 bytes, two codes per byte, the lower
+// nibble first), scales and biases (K/64 bf16, one per group of 64 inputs).
+struct Q4Row {
+  const uint8_t* codes;
+  const __nv_bfloat16* scales;
+  const __nv_bfloat16* biases;
+};
+
+// A whole matrix of rows of K inputs (row r at codes + r K/2, scales/biases + r K/64).
+struct Q4Matrix {
+  const uint8_t* codes;
+  const __nv_bfloat16* scales;
+  const __nv_bfloat16* biases;
+  __host__ __device__ Q4Row row(size_t r, int K) const {
+    return Q4Row{codes + r * (size_t)(K / 2), scales + r * (size_t)(K / 64),
+                 biases + r * (size_t)(K / 64)};
+  }
+};
+
+struct Q4Weights {
+  const __nv_bfloat16* w_r;  // the router stays bf16
+  const float* bias;
+  Q4Matrix gate, up, down, s_gate, s_up, s_down;
+};
+
 // Small-batch decode (2..kGemvMaxTokens tokens): shapes whose per-block copies of x
 // (T d bf16) and h (T 9 hdim fp32) fit in shared memory.
 constexpr int kGemvMaxTokens = 8;
@@ -155,5 +182,16 @@ cudaError_t launch_decode_batch_gateup(const __nv_bfloat16* x, const DecodeWeigh
 cudaError_t launch_decode_batch_down_combine(const DecodeWeights& W, const Dims& D, int T,
                                              const DecodeWs& dw, __nv_bfloat16* y, int sms,
                                              cudaStream_t s);
+
+// Batch-1 decode with 4-bit experts: router + shared gate/up, the 8 selected experts' gate/up,
+// down rows weighted and combined in fixed order (three launches, as the bf16 path).
+cudaError_t prepare_decode_q4_kernels();
+cudaError_t launch_decode_q4_router_shared(const __nv_bfloat16* x, const Q4Weights& W,
+                                           const Dims& D, const DecodeWs& dw, cudaStream_t s);
+cudaError_t launch_decode_q4_gateup(const __nv_bfloat16* x, const Q4Weights& W, const Dims& D,
+                                    int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
+                                    int sms, cudaStream_t s);
+cudaError_t launch_decode_q4_down_combine(const Q4Weights& W, const Dims& D, const DecodeWs& dw,
+                                          __nv_bfloat16* y, int sms, cudaStream_t s);
 
 }  // namespace moe

@@ -132,3 +132,37 @@ def assert_close(y_gpu_bits, y_ref_bits, what=""):
     bound = TOL_REL * (np.max(np.abs(r)) if r.size else 0.0) + TOL_ABS
     assert err <= bound, f"{what}: max|gpu-ref| = {err:.3e} > {bound:.3e}"
     return err, bound
+
+
+# ---------------------------------------------------------------- 4-bit experts
+
+def q4_to_device(c):
+    """Device tensors of the case's 4-bit experts (generated on the device) and bf16 router."""
+    import torch
+    dev = torch.device("cuda")
+    W = {"w_router": torch.from_numpy(c.w_r.view(np.int16)).to(dev).view(torch.bfloat16)}
+    s = torch.cuda.current_stream().cuda_stream
+    for nm in synth.Q4_NAMES:
+        cs, gs = synth.q4_shapes(nm, c.dims)
+        codes = torch.empty(cs, dtype=torch.uint8, device=dev)
+        sc = torch.empty(gs, dtype=torch.bfloat16, device=dev)
+        b = torch.empty(gs, dtype=torch.bfloat16, device=dev)
+        synth.q4_device(c.seed, c.layer, nm, c.dims, codes.data_ptr(), sc.data_ptr(),
+                        b.data_ptr(), s)
+        W[nm] = (codes, sc, b)
+    if c.bias is not None:
+        W["router_bias"] = torch.from_numpy(c.bias).to(dev)
+    return W
+
+
+def oracle_outputs_q4(c, tokens=None):
+    """Oracle y rows (bf16 bits) of the case with 4-bit experts (only the selected experts'
+    weights are generated on the host)."""
+    toks = np.arange(c.T) if tokens is None else np.asarray(tokens)
+    idx, _ = oracle.select(oracle.router_logits_f32(c.x[toks], c.w_r, c.bias), c.dims.k)
+    experts = {int(e): tuple(synth.q4_host(c.seed, c.layer, nm, c.dims, expert=int(e))
+                             for nm in ("w_gate", "w_up", "w_down")) for e in np.unique(idx)}
+    shared = tuple(synth.q4_host(c.seed, c.layer, nm, c.dims)
+                   for nm in ("ws_gate", "ws_up", "ws_down"))
+    y, _, _ = oracle.forward_q4(c.x, c.w_r, c.bias, experts, shared, c.dims.k, tokens=toks)
+    return y
