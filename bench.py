@@ -55,6 +55,7 @@ def parse_args():
                    help="layers in the decode graph (40 = the benchmark workload)")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-skew", action="store_true", help="skip the skewed-routing prefill line")
+    p.add_argument("--no-q4", action="store_true", help="skip the 4-bit decode line")
     p.add_argument("--no-small-batch", action="store_true",
                    help="skip the T = 2..5 decode lines")
     p.add_argument("--sweep", action="store_true",
@@ -101,6 +102,8 @@ def algorithmic(counts, T):
 
 
 DECODE_BYTES_PER_LAYER = 9 * 3 * F * D * 2 + E * D * 2 + 2 * D * 2  # 9 experts + router + x + y
+# 4-bit experts: half a byte per weight plus a bf16 scale and bias per 64; the router stays bf16
+DECODE_Q4_BYTES_PER_LAYER = 9 * 3 * F * D * 9 // 16 + E * D * 2 + 2 * D * 2  # 0.5625 B/weight
 
 
 # ---------------------------------------------------------------- clocks
@@ -425,6 +428,8 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
         assert L.device_error() == moe.MOE_OK
         L.close()
     small = None if args.no_small_batch else run_small_batch(torch, moe, args, Ws, seed, P_hbm)
+    del Ws
+    q4 = None if args.no_q4 else run_decode_q4(torch, moe, args, seed, P_hbm)
     return {"us_per_layer": us_layer, "GB_per_s": gbs, "layers": nl,
             "bytes_per_layer": DECODE_BYTES_PER_LAYER,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": P_hbm, "unit": "GB/s",
@@ -432,7 +437,65 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
             "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in zip(KERNELS_GEMV, kms)},
             "gpu_launches": args.steps * nl * 3,
             "graph": f"{nl} stream-ordered layer calls, replayed per step",
-            "small_batch": small}
+            "small_batch": small,
+            "q4": q4}
+
+
+def run_decode_q4(torch, moe, args, seed, P_hbm):
+    """Batch-1 decode with 4-bit group-affine experts (group 64, bf16 scale and bias; the
+    router bf16) over 40 layers' weights, one CUDA graph: us/layer and HBM GB/s of the
+    bytes this routing needs."""
+    dims = synth.Dims(d=D, f=F, fs=FS)
+    s = torch.cuda.current_stream().cuda_stream
+    layers, Ws = [], []
+    for l in range(args.decode_layers):
+        W = {"w_router": torch.empty((E, D), dtype=torch.bfloat16, device="cuda")}
+        synth.device_weight(seed, l, "w_r", dims, W["w_router"].data_ptr(), s)
+        for nm in synth.Q4_NAMES:
+            cs, gs = synth.q4_shapes(nm, dims)
+            t = (torch.empty(cs, dtype=torch.uint8, device="cuda"),
+                 torch.empty(gs, dtype=torch.bfloat16, device="cuda"),
+                 torch.empty(gs, dtype=torch.bfloat16, device="cuda"))
+            synth.q4_device(seed, l, nm, dims, *(a.data_ptr() for a in t), s)
+            W[nm] = t
+        Ws.append(W)
+        layers.append(moe.MoeLayer(W, 1))
+    x = torch.from_numpy(synth.x_rows(seed, 0, 1, D).view(np.int16)).cuda().view(torch.bfloat16)
+    ys = [torch.empty_like(x) for _ in layers]
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for L, y in zip(layers, ys):
+            L.forward(x, y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for L, y in zip(layers, ys):
+            L.forward(x, y)
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        g.replay()
+        b.record()
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3 / len(layers)
+    L0 = layers[0]
+    assert moe.moe_profile_begin(L0.handle, 50) == moe.MOE_OK
+    for _ in range(50):
+        L0.forward(x, ys[0])
+    st, kms, nc = moe.moe_profile_end(L0.handle)
+    for L in layers:
+        assert L.device_error() == moe.MOE_OK
+        L.close()
+    gbs = DECODE_Q4_BYTES_PER_LAYER / (us * 1e-6) / 1e9
+    return {"us_per_layer": us, "GB_per_s": gbs, "bytes_per_layer": DECODE_Q4_BYTES_PER_LAYER,
+            "hbm_frac": gbs / P_hbm, "layers": len(layers),
+            "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in
+                                zip(("q4_router_shared", "q4_gateup", "q4_down_combine"), kms)},
+            "weights": "4-bit codes, group 64, bf16 scale and bias; router bf16"}
 
 
 SMALL_BATCH_T = (2, 3, 4, 5)

@@ -25,22 +25,32 @@ __device__ __forceinline__ float nib(uint32_t u, int n) {
   return __uint_as_float(0x4B000000u | ((u >> (4 * n)) & 15u)) - 8388608.0f;
 }
 
-// 32 consecutive codes (the lower nibble of a byte first) times v[0..32): sum_i q_i v_i.
-__device__ __forceinline__ float q4_dot32(uint4 c, const float* v) {
+// Vectors in shared memory are stored swizzled: float4 k (k = 0..7) of 32-element piece p sits
+// in slot (k + p) mod 8 of the piece, so that eight lanes reading float4 k of eight
+// consecutive pieces touch all 32 banks.  Element i -> position:
+__host__ __device__ __forceinline__ int swz(int i) {
+  return (i & ~31) | ((((i >> 2) + (i >> 5)) & 7) << 2) | (i & 3);
+}
+
+// float4 k of piece p of a swizzled vector
+__device__ __forceinline__ float4 piece_f4(const float* v, int p, int k) {
+  return *reinterpret_cast<const float4*>(v + 32 * p + 4 * ((k + p) & 7));
+}
+
+// 32 consecutive codes (the lower nibble of a byte first) times piece p of the swizzled
+// vector v: sum_i q_i v_i in ascending i.
+__device__ __forceinline__ float q4_dot32(uint4 c, const float* v, int p) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
   float s = 0.f;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float4 a = *reinterpret_cast<const float4*>(v + 8 * k);
-    const float4 b = *reinterpret_cast<const float4*>(v + 8 * k + 4);
-    s = fmaf(nib(w[k], 0), a.x, s);
-    s = fmaf(nib(w[k], 1), a.y, s);
-    s = fmaf(nib(w[k], 2), a.z, s);
-    s = fmaf(nib(w[k], 3), a.w, s);
-    s = fmaf(nib(w[k], 4), b.x, s);
-    s = fmaf(nib(w[k], 5), b.y, s);
-    s = fmaf(nib(w[k], 6), b.z, s);
-    s = fmaf(nib(w[k], 7), b.w, s);
+  for (int k = 0; k < 8; ++k) {
+    const float4 a = piece_f4(v, p, k);
+    const uint32_t u = w[k >> 1];
+    const int n0 = 4 * (k & 1);
+    s = fmaf(nib(u, n0), a.x, s);
+    s = fmaf(nib(u, n0 + 1), a.y, s);
+    s = fmaf(nib(u, n0 + 2), a.z, s);
+    s = fmaf(nib(u, n0 + 3), a.w, s);
   }
   return s;
 }
@@ -83,7 +93,7 @@ __device__ __forceinline__ float q4_dot(const Q4Frag& r, const float* v, const f
 #pragma unroll
   for (int i = 0; i < kQB; ++i) {
     const int p = p0 + lane + 32 * i;
-    if (p < np) acc += r.s[i] * q4_dot32(r.c[i], v + 32 * p) + r.b[i] * vs[p];
+    if (p < np) acc += r.s[i] * q4_dot32(r.c[i], v, p) + r.b[i] * vs[p];
   }
   return acc;
 }
@@ -99,23 +109,23 @@ __device__ __forceinline__ float q4_dot_rest(Q4Frag& r, const Q4Row& row, const 
   return acc;
 }
 
-// Stages v (n bf16 values, n a multiple of 32) as fp32 in vf[n] and the sums of each 32 in
-// vs[n / 32]; every thread of the block calls this (it holds barriers).
+// Stages v (n bf16 values, n a multiple of 32) as fp32, swizzled, in vf[n] and the sums of
+// each 32 (ascending) in vs[n / 32]; every thread of the block calls this (it holds barriers).
 __device__ __forceinline__ void stage_f32(const __nv_bfloat16* src, float* vf, float* vs, int n) {
-  for (int i = threadIdx.x; i < n; i += blockDim.x) vf[i] = __bfloat162float(src[i]);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) vf[swz(i)] = __bfloat162float(src[i]);
   __syncthreads();
   for (int p = threadIdx.x; p < n / 32; p += blockDim.x) {
     float s = 0.f;
-    for (int i = 0; i < 32; ++i) s += vf[32 * p + i];
+    for (int i = 0; i < 32; ++i) s += vf[swz(32 * p + i)];
     vs[p] = s;
   }
   __syncthreads();
 }
 
-// 8 bf16 weights times 8 fp32 values (router rows).
-__device__ __forceinline__ float dot8_bf16_f32(uint4 w, const float* v) {
-  const float4 a = *reinterpret_cast<const float4*>(v);
-  const float4 b = *reinterpret_cast<const float4*>(v + 4);
+// 8 bf16 weights times elements 8 cc .. 8 cc + 7 of the swizzled vector v (router rows).
+__device__ __forceinline__ float dot8_bf16_f32(uint4 w, const float* v, int cc) {
+  const float4 a = piece_f4(v, cc >> 2, 2 * (cc & 3));
+  const float4 b = piece_f4(v, cc >> 2, 2 * (cc & 3) + 1);
   float s = 0.f;
   s = fmaf(bf16_lo(w.x), a.x, s);
   s = fmaf(bf16_hi(w.x), a.y, s);
@@ -168,10 +178,10 @@ __global__ void __launch_bounds__(kQWarps * 32) dec_q4_router_shared_kernel(Q4Ro
 #pragma unroll
     for (int i = 0; i < kRPre; ++i) {
       const int cc = lane + 32 * i;
-      if (cc < nch) acc += dot8_bf16_f32(rr[i], xf + cc * 8);
+      if (cc < nch) acc += dot8_bf16_f32(rr[i], xf, cc);
     }
     for (int cc = lane + 32 * kRPre; cc < nch; cc += 32)
-      acc += dot8_bf16_f32(ld_stream_u4(rrow + (size_t)cc * 8), xf + cc * 8);
+      acc += dot8_bf16_f32(ld_stream_u4(rrow + (size_t)cc * 8), xf, cc);
     acc = warp_sum_q(acc);
     if (lane == 0) a.dw.logits[e] = acc + (a.W.bias ? a.W.bias[e] : 0.f);
   } else if (c < a.D.fs) {
@@ -281,11 +291,14 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
   if (n < d) load(0, n);
   pdl_wait();  // h comes from the gate/up kernel
   pdl_trigger();
-  for (int i = threadIdx.x; i < 9 * hdim; i += blockDim.x) hf[i] = __ldcg(a.dw.hdec + i);
+  // each row h_j swizzled on its own (pieces counted from the row's start)
+  for (int i = threadIdx.x; i < 9 * hdim; i += blockDim.x)
+    hf[(i / hdim) * hdim + swz(i % hdim)] = __ldcg(a.dw.hdec + i);
   __syncthreads();
   for (int q = threadIdx.x; q < 9 * (hdim / 32); q += blockDim.x) {
+    const int j = q / (hdim / 32), p = q % (hdim / 32);
     float sum = 0.f;
-    for (int i = 0; i < 32; ++i) sum += hf[32 * q + i];
+    for (int i = 0; i < 32; ++i) sum += hf[j * hdim + swz(32 * p + i)];
     hsum[q] = sum;
   }
   __syncthreads();
@@ -299,7 +312,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
         if (P < npt) {
           int j, p;
           row_of(P, n, j, p);
-          const float part = ps[i] * q4_dot32(pc[i], hf + (size_t)j * hdim + 32 * p) +
+          const float part = ps[i] * q4_dot32(pc[i], hf + (size_t)j * hdim, p) +
                              pb[i] * hsum[j * (hdim / 32) + p];
           yv = fmaf(j < 8 ? s_w[j] : 1.0f, part, yv);
         }
