@@ -38,21 +38,36 @@ __device__ __forceinline__ float4 piece_f4(const float* v, int p, int k) {
 }
 
 // 32 consecutive codes (the lower nibble of a byte first) times piece p of the swizzled
-// vector v: sum_i q_i v_i in ascending i.
+// vector v: sum_i q_i v_i, in two interleaved fp32 partial sums (even and odd i) that are
+// added at the end.  Packed fp32 pairs: prmt builds the float 2^23 + q of a code byte, one
+// packed add takes 2^23 off (exact), one packed fma accumulates two products.
 __device__ __forceinline__ float q4_dot32(uint4 c, const float* v, int p) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-  float s = 0.f;
+  unsigned long long acc = 0ull;  // two fp32 zeros
+  const unsigned long long neg_magic = 0xCB000000CB000000ull;  // (-2^23, -2^23)
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float4 a = piece_f4(v, p, k);
-    const uint32_t u = w[k >> 1];
-    const int n0 = 4 * (k & 1);
-    s = fmaf(nib(u, n0), a.x, s);
-    s = fmaf(nib(u, n0 + 1), a.y, s);
-    s = fmaf(nib(u, n0 + 2), a.z, s);
-    s = fmaf(nib(u, n0 + 3), a.w, s);
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t t0 = w[k] & 0x0F0F0F0Fu;         // codes of inputs 8k, 8k+2, 8k+4, 8k+6
+    const uint32_t t1 = (w[k] >> 4) & 0x0F0F0F0Fu;  // codes of inputs 8k+1, 8k+3, ...
+    const float4 a = piece_f4(v, p, 2 * k);
+    const float4 b = piece_f4(v, p, 2 * k + 1);
+    const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t sel = (uint32_t)m | (4u << 4) | (5u << 8) | (7u << 12);
+      uint32_t lo, hi;
+      asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(t0), "r"(0x4B000000u), "r"(sel));
+      asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(t1), "r"(0x4B000000u), "r"(sel));
+      asm("{\n\t.reg .b64 q, x;\n\t"
+          "mov.b64 q, {%1, %2};\n\t"
+          "mov.b64 x, {%3, %4};\n\t"
+          "add.rn.f32x2 q, q, %5;\n\t"
+          "fma.rn.f32x2 %0, q, x, %0;\n\t}"
+          : "+l"(acc)
+          : "r"(lo), "r"(hi), "f"(xv[2 * m]), "f"(xv[2 * m + 1]), "l"(neg_magic));
+    }
   }
-  return s;
+  return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
 }
 
 __device__ __forceinline__ float ld_bf16(const __nv_bfloat16* p) {
@@ -260,17 +275,19 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
   if (warp == 0) select_top8(a.dw.logits, lane, s_ids, s_w);
   __syncthreads();
   const int npr = f / 32, nps = fs / 32, npt = 8 * npr + nps;
-  // the row of piece P of output nn: routed row j or the shared row (j = 8), piece p in it
-  auto row_of = [&](int P, int nn, int& j, int& p) {
-    if (P < 8 * npr) {
-      j = P / npr;
-      p = P - j * npr;
-      return a.W.down.row((size_t)s_ids[j] * d + nn, f);
-    }
-    j = 8;
-    p = P - 8 * npr;
-    return a.W.s_down.row((size_t)nn, fs);
+  // the row and piece of run position P: routed row j = P / npr or the shared row (j = 8)
+  auto split = [&](int P, int& j, int& p) {
+    j = P < 8 * npr ? P / npr : 8;
+    p = P - j * npr;
   };
+  auto row_of = [&](int j, int nn) {
+    return j < 8 ? a.W.down.row((size_t)s_ids[j] * d + nn, f) : a.W.s_down.row((size_t)nn, fs);
+  };
+  // the first kQDPre run positions of this lane are the same for every output: their rows
+  // and pieces are worked out once
+  int pj[kQDPre], pp[kQDPre];
+#pragma unroll
+  for (int i = 0; i < kQDPre; ++i) split(lane + 32 * i, pj[i], pp[i]);
   uint4 pc[kQDPre];
   float ps[kQDPre], pb[kQDPre];
   auto load = [&](int P0, int nn) {
@@ -278,8 +295,9 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
     for (int i = 0; i < kQDPre; ++i) {
       const int P = P0 + lane + 32 * i;
       if (P < npt) {
-        int j, p;
-        const Q4Row r = row_of(P, nn, j, p);
+        int j = pj[i], p = pp[i];
+        if (P0) split(P, j, p);
+        const Q4Row r = row_of(j, nn);
         pc[i] = ld_stream_u4(r.codes + (size_t)p * 16);
         ps[i] = ld_bf16(r.scales + p / 2);
         pb[i] = ld_bf16(r.biases + p / 2);
@@ -291,7 +309,8 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
   if (n < d) load(0, n);
   pdl_wait();  // h comes from the gate/up kernel
   pdl_trigger();
-  // each row h_j swizzled on its own (pieces counted from the row's start)
+  // each row h_j swizzled on its own (pieces counted from the row's start): all loads in
+  // flight at once, then the sums per 32 from shared memory
   for (int i = threadIdx.x; i < 9 * hdim; i += blockDim.x)
     hf[(i / hdim) * hdim + swz(i % hdim)] = __ldcg(a.dw.hdec + i);
   __syncthreads();
@@ -302,6 +321,7 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
     hsum[q] = sum;
   }
   __syncthreads();
+  const float wj[9] = {s_w[0], s_w[1], s_w[2], s_w[3], s_w[4], s_w[5], s_w[6], s_w[7], 1.0f};
   for (; n < d; n += nwarps) {
     float yv = 0.f;
     for (int P0 = 0; P0 < npt; P0 += 32 * kQDPre) {
@@ -310,11 +330,14 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
       for (int i = 0; i < kQDPre; ++i) {
         const int P = P0 + lane + 32 * i;
         if (P < npt) {
-          int j, p;
-          row_of(P, n, j, p);
+          int j = pj[i], p = pp[i];
+          if (P0) split(P, j, p);
           const float part = ps[i] * q4_dot32(pc[i], hf + (size_t)j * hdim, p) +
                              pb[i] * hsum[j * (hdim / 32) + p];
-          yv = fmaf(j < 8 ? s_w[j] : 1.0f, part, yv);
+          float w = wj[0];
+#pragma unroll
+          for (int q = 1; q < 9; ++q) w = j == q ? wj[q] : w;
+          yv = fmaf(w, part, yv);
         }
       }
     }
