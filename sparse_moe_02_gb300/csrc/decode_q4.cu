@@ -129,9 +129,18 @@ __device__ __forceinline__ float q4_dot_rest(Q4Frag& r, const Q4Row& row, const 
 __device__ __forceinline__ void stage_f32(const __nv_bfloat16* src, float* vf, float* vs, int n) {
   for (int i = threadIdx.x; i < n; i += blockDim.x) vf[swz(i)] = __bfloat162float(src[i]);
   __syncthreads();
+  // a piece's 32 values are its 32 slots in some order: summed in slot order
   for (int p = threadIdx.x; p < n / 32; p += blockDim.x) {
+    const float4* q = reinterpret_cast<const float4*>(vf + 32 * p);
     float s = 0.f;
-    for (int i = 0; i < 32; ++i) s += vf[swz(32 * p + i)];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 t = q[i];
+      s += t.x;
+      s += t.y;
+      s += t.z;
+      s += t.w;
+    }
     vs[p] = s;
   }
   __syncthreads();
@@ -311,13 +320,22 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
   pdl_trigger();
   // each row h_j swizzled on its own (pieces counted from the row's start): all loads in
   // flight at once, then the sums per 32 from shared memory
-  for (int i = threadIdx.x; i < 9 * hdim; i += blockDim.x)
-    hf[(i / hdim) * hdim + swz(i % hdim)] = __ldcg(a.dw.hdec + i);
+  for (int j = 0; j < 9; ++j)
+    for (int c = threadIdx.x; c < hdim; c += blockDim.x)
+      hf[j * hdim + swz(c)] = __ldcg(a.dw.hdec + (size_t)j * hdim + c);
   __syncthreads();
+  // a piece's 32 values are its 32 slots in some order: summed in slot order
   for (int q = threadIdx.x; q < 9 * (hdim / 32); q += blockDim.x) {
-    const int j = q / (hdim / 32), p = q % (hdim / 32);
+    const float4* t4 = reinterpret_cast<const float4*>(hf + 32 * q);
     float sum = 0.f;
-    for (int i = 0; i < 32; ++i) sum += hf[j * hdim + swz(32 * p + i)];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 t = t4[i];
+      sum += t.x;
+      sum += t.y;
+      sum += t.z;
+      sum += t.w;
+    }
     hsum[q] = sum;
   }
   __syncthreads();
