@@ -577,13 +577,20 @@ def barrier(world):
         dist.barrier()
 
 
-def reduce_max(torch, world, v):
+def reduce_max(torch, world, v, device="cuda"):
+    """The largest v over the ranks (the step time of the slowest rank)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(world, tokens_per_rank, ms):
+    """Whole-job tokens/s: every rank runs its own batch of tokens_per_rank tokens (weak
+    scaling); ms is the slowest rank's step time."""
+    return world * tokens_per_rank / (ms / 1e3)
 
 
 def main():
@@ -626,7 +633,7 @@ def main():
                "sample": sample}
     if rank != 0:
         return
-    value = world * T_PREFILL / (pre["ms"] / 1e3)
+    value = job_value(world, T_PREFILL, pre["ms"])
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"],
@@ -643,7 +650,7 @@ def main():
         "prefill_sweep": sweep,
         "decode": dec,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * T_PREFILL / (pre["e2e_ms"] / 1e3), "unit": "tokens/s",
+        "e2e": {"value": job_value(world, T_PREFILL, pre["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": T_PREFILL * D * 2, "d2h_bytes_per_step": T_PREFILL * D * 2},
         "gpu_launches": args.steps * pre["launches"],
         "clocks": clk,
