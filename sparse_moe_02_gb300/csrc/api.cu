@@ -429,9 +429,10 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
   if (use_gemv(h, T)) {
     const moe::DecodeWeights W = decode_weights(h);
     if ((st = prof_mark(h, s, 0))) return st;
+    // the router alone: the shared expert's gate/up runs in the gate/up launch
     if ((st = cuda_status(moe::launch_decode_router_shared(xd, W, h->D, nullptr, nullptr,
                                                            nullptr, nullptr, h->dws, h->rws.err,
-                                                           s, true))))
+                                                           s, false))))
       return st;
     if ((st = prof_mark(h, s, 1))) return st;
     if ((st = cuda_status(moe::launch_decode_gateup(xd, W, h->D, h->rws.topk_idx, h->rws.topk_w,

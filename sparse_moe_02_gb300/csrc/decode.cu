@@ -184,15 +184,25 @@ struct GateUpArgs {
   DecodeWs dw;
 };
 
-// Items (selected expert j, feature c), one warp per item in a grid-stride loop over a grid
-// that is fully resident: h[j][c] = silu(gate . x) * (up . x).  Warp 0 of every block
-// selects the top 8 from the router logits first.
+// Items, one warp per item in a grid-stride loop over a grid that is fully resident: first
+// the shared expert's features c < fs, then the selected experts' (j, c):
+// h[j][c] = silu(gate . x) * (up . x).  A warp whose first item is a shared feature requests
+// its rows before waiting on the router kernel (they do not depend on it).  Warp 0 of every
+// block selects the top 8 from the router logits first.
 __global__ void __launch_bounds__(kWarps * 32, 2) dec_gateup_kernel(GateUpArgs a) {
   extern __shared__ uint4 xs[];
   __shared__ int s_ids[kTopK];
   __shared__ float s_w[kTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = a.D.d, f = a.D.f, nch = d / 8;
+  const int d = a.D.d, f = a.D.f, fs = a.D.fs, nch = d / 8;
+  const int total = fs + kTopK * f;
+  const int nwarps = gridDim.x * kWarps;
+  int it = blockIdx.x * kWarps + warp;
+  RowFrag rg, ru;
+  if (it < fs) {
+    row_load(rg, a.W.ws_gate + (size_t)it * d, nch, lane, 0);
+    row_load(ru, a.W.ws_up + (size_t)it * d, nch, lane, 0);
+  }
   pdl_wait();     // the router logits come from the previous kernel
   pdl_trigger();  // the down kernel may start selecting and streaming its rows now
   if (warp == 0) select_top8(a.dw.logits, lane, s_ids, s_w);
@@ -203,18 +213,27 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_gateup_kernel(GateUpArgs a
     a.topk_idx[threadIdx.x] = s_ids[threadIdx.x];
     a.topk_w[threadIdx.x] = s_w[threadIdx.x];
   }
-  const int nwarps = gridDim.x * kWarps;
-  for (int it = blockIdx.x * kWarps + warp; it < kTopK * f; it += nwarps) {
-    const int j = it / f, c = it % f;
-    const size_t row = ((size_t)s_ids[j] * f + c) * d;
-    const __nv_bfloat16* gr = a.W.w_gate + row;
-    const __nv_bfloat16* ur = a.W.w_up + row;
-    RowFrag rg, ru;
-    row_load(rg, gr, nch, lane, 0);
-    row_load(ru, ur, nch, lane, 0);
+  for (bool first = true; it < total; it += nwarps, first = false) {
+    const __nv_bfloat16 *gr, *ur;
+    size_t slot;
+    if (it < fs) {  // the shared expert's feature it
+      gr = a.W.ws_gate + (size_t)it * d;
+      ur = a.W.ws_up + (size_t)it * d;
+      slot = (size_t)8 * a.D.hdim + it;
+    } else {
+      const int j = (it - fs) / f, c = (it - fs) % f;
+      const size_t row = ((size_t)s_ids[j] * f + c) * d;
+      gr = a.W.w_gate + row;
+      ur = a.W.w_up + row;
+      slot = (size_t)j * a.D.hdim + c;
+    }
+    if (!(first && it < fs)) {  // the first shared item's rows are already in registers
+      row_load(rg, gr, nch, lane, 0);
+      row_load(ru, ur, nch, lane, 0);
+    }
     const float g = warp_sum(row_dot_rest(rg, gr, xs, nch, lane));
     const float u = warp_sum(row_dot_rest(ru, ur, xs, nch, lane));
-    if (lane == 0) a.dw.hdec[(size_t)j * a.D.hdim + c] = silu_mul(g, u);
+    if (lane == 0) a.dw.hdec[slot] = silu_mul(g, u);
   }
 }
 
@@ -643,7 +662,7 @@ cudaError_t launch_decode_gateup(const __nv_bfloat16* x, const DecodeWeights& W,
                                  int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
                                  cudaStream_t s) {
   GateUpArgs a{x, W, D, topk_idx, topk_w, dw};
-  const int grid = std::min(g_gateup_grid, kTopK * D.f / kWarps);
+  const int grid = std::min(g_gateup_grid, (D.fs + kTopK * D.f) / kWarps);
   return launch_pdl(dec_gateup_kernel, dim3(grid), dim3(kWarps * 32), (size_t)D.d * 2, s, a);
 }
 
