@@ -224,9 +224,10 @@ struct Q4GateUpArgs {
   DecodeWs dw;
 };
 
-// Items (selected expert j, feature c), one warp per item over a resident grid:
-// h[j][c] = silu(gate . x) * (up . x) from the 4-bit gate and up rows.  Warp 0 of every
-// block selects the top 8 from the router logits first.
+// Items, one warp per item over a resident grid: first the shared expert's features c < fs,
+// then the selected experts' (j, c): h[j][c] = silu(gate . x) * (up . x) from the 4-bit gate
+// and up rows.  A warp whose first item is a shared feature requests its rows before waiting
+// on the router kernel.  Warp 0 of every block selects the top 8 from the router logits first.
 __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_gateup_kernel(Q4GateUpArgs a) {
   extern __shared__ float qsm[];
   float* xf = qsm;
@@ -234,7 +235,15 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_gateup_kernel(Q4GateUp
   __shared__ int s_ids[kTopK];
   __shared__ float s_w[kTopK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = a.D.d, f = a.D.f, np = d / 32;
+  const int d = a.D.d, f = a.D.f, fs = a.D.fs, np = d / 32;
+  const int total = fs + kTopK * f;
+  const int nwarps = gridDim.x * kQWarps;
+  int it = blockIdx.x * kQWarps + warp;
+  Q4Frag g, u;
+  if (it < fs) {
+    q4_load(g, a.W.s_gate.row(it, d), np, lane, 0);
+    q4_load(u, a.W.s_up.row(it, d), np, lane, 0);
+  }
   pdl_wait();     // the router logits come from the previous kernel
   pdl_trigger();  // the down kernel may start selecting and streaming its rows now
   if (warp == 0) select_top8(a.dw.logits, lane, s_ids, s_w);
@@ -243,17 +252,27 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_gateup_kernel(Q4GateUp
     a.topk_idx[threadIdx.x] = s_ids[threadIdx.x];
     a.topk_w[threadIdx.x] = s_w[threadIdx.x];
   }
-  const int nwarps = gridDim.x * kQWarps;
-  for (int it = blockIdx.x * kQWarps + warp; it < kTopK * f; it += nwarps) {
-    const int j = it / f, c = it % f;
-    const size_t r = (size_t)s_ids[j] * f + c;
-    const Q4Row rg = a.W.gate.row(r, d), ru = a.W.up.row(r, d);
-    Q4Frag g, u;
-    q4_load(g, rg, np, lane, 0);
-    q4_load(u, ru, np, lane, 0);
+  for (bool first = true; it < total; it += nwarps, first = false) {
+    Q4Row rg, ru;
+    size_t slot;
+    if (it < fs) {
+      rg = a.W.s_gate.row(it, d);
+      ru = a.W.s_up.row(it, d);
+      slot = (size_t)8 * a.D.hdim + it;
+    } else {
+      const int j = (it - fs) / f, c = (it - fs) % f;
+      const size_t r = (size_t)s_ids[j] * f + c;
+      rg = a.W.gate.row(r, d);
+      ru = a.W.up.row(r, d);
+      slot = (size_t)j * a.D.hdim + c;
+    }
+    if (!(first && it < fs)) {  // the first shared item's pieces are already in registers
+      q4_load(g, rg, np, lane, 0);
+      q4_load(u, ru, np, lane, 0);
+    }
     const float gv = warp_sum_q(q4_dot_rest(g, rg, xf, xs, np, lane));
     const float uv = warp_sum_q(q4_dot_rest(u, ru, xf, xs, np, lane));
-    if (lane == 0) a.dw.hdec[(size_t)j * a.D.hdim + c] = silu_mul(gv, uv);
+    if (lane == 0) a.dw.hdec[slot] = silu_mul(gv, uv);
   }
 }
 
@@ -384,7 +403,7 @@ cudaError_t prepare_decode_q4_kernels() {
 cudaError_t launch_decode_q4_router_shared(const __nv_bfloat16* x, const Q4Weights& W,
                                            const Dims& D, const DecodeWs& dw, cudaStream_t s) {
   Q4RouterSharedArgs a{x, W, D, dw};
-  const int blocks = kE / kQWarps + (D.fs + kQWarps - 1) / kQWarps;
+  const int blocks = kE / kQWarps;  // router rows only: the shared gate/up is in the next launch
   return launch_pdl(dec_q4_router_shared_kernel, dim3(blocks), dim3(kQWarps * 32),
                     (size_t)D.d * 4 + (size_t)D.d / 32 * 4, s, a);
 }
@@ -393,7 +412,7 @@ cudaError_t launch_decode_q4_gateup(const __nv_bfloat16* x, const Q4Weights& W, 
                                     int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
                                     int sms, cudaStream_t s) {
   Q4GateUpArgs a{x, W, D, topk_idx, topk_w, dw};
-  const int grid = std::min(2 * sms, kTopK * D.f / kQWarps);
+  const int grid = std::min(2 * sms, (D.fs + kTopK * D.f) / kQWarps);
   return launch_pdl(dec_q4_gateup_kernel, dim3(grid), dim3(kQWarps * 32),
                     (size_t)D.d * 4 + (size_t)D.d / 32 * 4, s, a);
 }
