@@ -427,6 +427,7 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
     for L in layers:
         assert L.device_error() == moe.MOE_OK
         L.close()
+    read_gbs = read_probe(torch, moe)
     small = None if args.no_small_batch else run_small_batch(torch, moe, args, Ws, seed, P_hbm)
     del Ws
     q4 = None if args.no_q4 else run_decode_q4(torch, moe, args, seed, P_hbm)
@@ -435,6 +436,9 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": P_hbm, "unit": "GB/s",
                          "frac": gbs / P_hbm},
             "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in zip(KERNELS_GEMV, kms)},
+            "read_probe": {"GB_per_s": read_gbs, "frac_of_read_probe": gbs / read_gbs,
+                           "how": "moe_read_probe over 4 GiB, best of 10 (a read-only stream; "
+                                  "the roofline peak above stays the measured copy rate)"},
             "gpu_launches": args.steps * nl * 3,
             "graph": f"{nl} stream-ordered layer calls, replayed per step",
             "small_batch": small,
@@ -496,6 +500,28 @@ def run_decode_q4(torch, moe, args, seed, P_hbm):
             "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in
                                 zip(("q4_router_shared", "q4_gateup", "q4_down_combine"), kms)},
             "weights": "4-bit codes, group 64, bf16 scale and bias; router bf16"}
+
+
+def read_probe(torch, moe):
+    """GB/s of a read-only stream over 4 GiB (moe_read_probe; a pure read can run faster than
+    the copy the measured peak comes from): the best of 10, CUDA events."""
+    nbytes = 4 << 30
+    buf = torch.ones(nbytes // 2, dtype=torch.bfloat16, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        assert moe.moe_read_probe(buf.data_ptr(), nbytes, sink.data_ptr(), s) == moe.MOE_OK
+    best = None
+    for _ in range(10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        moe.moe_read_probe(buf.data_ptr(), nbytes, sink.data_ptr(), s)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    del buf
+    return nbytes / (best / 1e3) / 1e9
 
 
 SMALL_BATCH_T = (2, 3, 4, 5)

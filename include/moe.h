@@ -48,6 +48,7 @@
 #ifndef MOE_H
 #define MOE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -161,6 +162,12 @@ int moe_get_device_error(moe_handle h, void* stream);
 
 /* Frees the workspace and the handle (synchronises the device).  NULL is accepted. */
 int moe_destroy(moe_handle h);
+
+/* Measurement hook: enqueues a read-only stream over bytes (a multiple of 16) of device memory
+ * at buf (16-byte aligned) on `stream`; sink is a device word the kernel may write (4-byte
+ * aligned).  Time it with events on the stream: a pure read stream can exceed the copy rate
+ * of the measured HBM peak, and the benchmark reports it beside the decode roofline. */
+int moe_read_probe(const void* buf, size_t bytes, void* sink, void* stream);
 
 /* Static description of a status code. */
 const char* moe_status_string(int status);

@@ -29,7 +29,7 @@ MOE_SCHEDULE_GEMV = 2
 
 EXPORTS = ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_get_device_error",
            "moe_destroy", "moe_status_string", "moe_last_cuda_error", "moe_profile_begin",
-           "moe_profile_end", "moe_route_one_noalloc", "moe_create_q4")
+           "moe_profile_end", "moe_route_one_noalloc", "moe_create_q4", "moe_read_probe")
 
 # kernel order reported by moe_profile_end
 KERNELS_GEMM = ("router_topk", "route_plan_scatter", "experts", "combine")
@@ -73,6 +73,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         L.moe_create.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights),
                                  ctypes.POINTER(_c_void_p)]
+        L.moe_read_probe.argtypes = [_c_void_p, ctypes.c_size_t, _c_void_p, _c_void_p]
         L.moe_create_q4.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights_q4),
                                     ctypes.POINTER(_c_void_p)]
         L.moe_route.argtypes = [_c_void_p, _c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
@@ -89,7 +90,7 @@ def lib():
                                       ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]
         L.moe_route_one_noalloc.argtypes = [_c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                             _c_void_p, _c_void_p]
-        for fn in ("moe_create", "moe_create_q4", "moe_route", "moe_forward", "moe_forward_host",
+        for fn in ("moe_create", "moe_create_q4", "moe_read_probe", "moe_route", "moe_forward", "moe_forward_host",
                    "moe_get_device_error", "moe_destroy", "moe_last_cuda_error",
                    "moe_profile_begin", "moe_profile_end", "moe_route_one_noalloc"):
             getattr(L, fn).restype = _c_int
@@ -109,6 +110,10 @@ def moe_create_q4(cfg, weights_q4):
     h = _c_void_p()
     st = lib().moe_create_q4(ctypes.byref(cfg), ctypes.byref(weights_q4), ctypes.byref(h))
     return st, h
+
+
+def moe_read_probe(buf, nbytes, sink, stream):
+    return lib().moe_read_probe(buf, nbytes, sink, stream)
 
 
 def moe_route(h, x, T, topk_idx, topk_w, offsets, perm, stream):

@@ -297,3 +297,15 @@ def test_small_batch_decode_shape(T):
     got = _run(c, moe.MOE_SCHEDULE_GEMV)
     _check_routing(c, got)
     assert_close(got["y"], oracle_outputs(c), f"small batch decode T={T}")
+
+
+def test_read_probe_hook():
+    import torch
+    buf = torch.ones(1 << 20, dtype=torch.bfloat16, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert moe.moe_read_probe(buf.data_ptr(), 2 << 20, sink.data_ptr(), s) == moe.MOE_OK
+    assert moe.moe_read_probe(buf.data_ptr() + 8, 1024, sink.data_ptr(), s) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_read_probe(buf.data_ptr(), 1000, sink.data_ptr(), s) == moe.MOE_ERR_INVALID_ARG
+    torch.cuda.synchronize()
