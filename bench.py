@@ -55,7 +55,7 @@ def parse_args():
                    help="layers in the decode graph (40 = the benchmark workload)")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-skew", action="store_true", help="skip the skewed-routing prefill line")
-    p.add_argument("--no-q4", action="store_true", help="skip the 4-bit decode line")
+    p.add_argument("--no-q4", action="store_true", help="skip the 4-bit prefill and decode lines")
     p.add_argument("--no-small-batch", action="store_true",
                    help="skip the T = 2..5 decode lines")
     p.add_argument("--sweep", action="store_true",
@@ -445,23 +445,80 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
             "q4": q4}
 
 
+def q4_device_weights(torch, seed, layer, dims, bias=None):
+    """Device 4-bit experts (codes, scales, biases per tensor) and the bf16 router."""
+    s = torch.cuda.current_stream().cuda_stream
+    W = {"w_router": torch.empty((E, dims.d), dtype=torch.bfloat16, device="cuda")}
+    synth.device_weight(seed, layer, "w_r", dims, W["w_router"].data_ptr(), s)
+    for nm in synth.Q4_NAMES:
+        cs, gs = synth.q4_shapes(nm, dims)
+        t = (torch.empty(cs, dtype=torch.uint8, device="cuda"),
+             torch.empty(gs, dtype=torch.bfloat16, device="cuda"),
+             torch.empty(gs, dtype=torch.bfloat16, device="cuda"))
+        synth.q4_device(seed, layer, nm, dims, *(a.data_ptr() for a in t), s)
+        W[nm] = t
+    if bias is not None:
+        W["router_bias"] = torch.from_numpy(bias).cuda()
+    return W
+
+
+def run_prefill_q4(torch, moe, args, seed, P_hbm, P_tc):
+    """Prefill T=4096 (balanced routing) with 4-bit experts on the tensor-core path: the
+    grouped GEMM dequantizes each weight tile into tensor memory.  Layer time with L2 flushed
+    before each step, the per-kernel split, and the expert kernel against the bf16 tensor
+    peak (its FLOPs are those of the bf16 layer)."""
+    dims = synth.Dims(d=D, f=F, fs=FS)
+    W = q4_device_weights(torch, seed, 0, dims)
+    x = torch.from_numpy(synth.x_rows(seed, 0, T_PREFILL, D).view(np.int16)).cuda() \
+        .view(torch.bfloat16)
+    y = torch.empty_like(x)
+    layer = moe.MoeLayer(W, T_PREFILL)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    counts = np.diff(layer.route(x)["offsets"].cpu().numpy())
+    for _ in range(max(3, args.warmup)):
+        layer.forward(x, y)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        layer.forward(x, y)
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nprof = min(args.steps, 50)
+    assert moe.moe_profile_begin(layer.handle, nprof) == moe.MOE_OK
+    for _ in range(nprof):
+        flush.zero_()
+        layer.forward(x, y)
+    st, kms, nc = moe.moe_profile_end(layer.handle)
+    assert st == moe.MOE_OK and layer.device_error() == moe.MOE_OK
+    layer.close()
+    kt = {k: v / nc for k, v in zip(KERNELS_GEMM, kms)}
+    ne = int((counts > 0).sum())
+    wbytes = (ne * 3 * F * D + 3 * FS * D) * 9 // 16  # 4.5 bits per weight
+    layer_bytes = E * D * 2 + wbytes + 2 * T_PREFILL * D * 2
+    _, fl, _, layer_flops = algorithmic(counts, T_PREFILL)
+    t = ms / 1e3
+    t_x = kt["experts"] / 1e3
+    return {"ms": ms, "tokens_per_s": T_PREFILL / t, "algorithmic_bytes": layer_bytes,
+            "hbm_frac": layer_bytes / t / 1e9 / P_hbm,
+            "tensor_frac": layer_flops / t / 1e12 / P_tc,
+            "experts_tensor_frac": fl["experts"] / t_x / 1e12 / P_tc,
+            "kernel_ms": {k: round(v, 5) for k, v in kt.items()},
+            "weights": "4-bit codes, group 64, bf16 scale and bias; router bf16; dequantized "
+                       "to bf16 in tensor memory inside the grouped GEMM"}
+
+
 def run_decode_q4(torch, moe, args, seed, P_hbm):
     """Batch-1 decode with 4-bit group-affine experts (group 64, bf16 scale and bias; the
     router bf16) over 40 layers' weights, one CUDA graph: us/layer and HBM GB/s of the
     bytes this routing needs."""
     dims = synth.Dims(d=D, f=F, fs=FS)
-    s = torch.cuda.current_stream().cuda_stream
     layers, Ws = [], []
     for l in range(args.decode_layers):
-        W = {"w_router": torch.empty((E, D), dtype=torch.bfloat16, device="cuda")}
-        synth.device_weight(seed, l, "w_r", dims, W["w_router"].data_ptr(), s)
-        for nm in synth.Q4_NAMES:
-            cs, gs = synth.q4_shapes(nm, dims)
-            t = (torch.empty(cs, dtype=torch.uint8, device="cuda"),
-                 torch.empty(gs, dtype=torch.bfloat16, device="cuda"),
-                 torch.empty(gs, dtype=torch.bfloat16, device="cuda"))
-            synth.q4_device(seed, l, nm, dims, *(a.data_ptr() for a in t), s)
-            W[nm] = t
+        W = q4_device_weights(torch, seed, l, dims)
         Ws.append(W)
         layers.append(moe.MoeLayer(W, 1))
     x = torch.from_numpy(synth.x_rows(seed, 0, 1, D).view(np.int16)).cuda().view(torch.bfloat16)
@@ -650,6 +707,7 @@ def main():
     if args.sweep:
         sweep = [time_prefill(torch, moe, t, False, min(args.steps, 20), 3, rank, P_hbm, P_tc)
                  for t in SWEEP_T]
+    pre_q4 = None if args.no_q4 else run_prefill_q4(torch, moe, args, rank, P_hbm, P_tc)
     dec = None if args.no_decode else run_decode(torch, moe, args, rank, world, P_hbm)
     clk = clocks.stop()
     cpu = None
@@ -674,6 +732,7 @@ def main():
         "layer": pre["layer"],
         "prefill_skewed": skewed,
         "prefill_sweep": sweep,
+        "prefill_q4": pre_q4,
         "decode": dec,
         "cpu_baseline": cpu,
         "e2e": {"value": job_value(world, T_PREFILL, pre["e2e_ms"]), "unit": "tokens/s",

@@ -131,9 +131,11 @@ typedef struct {
   moe_q4_matrix ws_down;    /* d rows of fs inputs */
 } moe_weights_q4;
 
-/* moe_create for 4-bit experts.  Such a handle runs batch-1 decode (moe_forward and
- * moe_forward_host with T == 1; the schedule must be AUTO or GEMV) and moe_route for any T;
- * moe_forward with T > 1 returns MOE_ERR_UNSUPPORTED (the tensor-core path reads bf16). */
+/* moe_create for 4-bit experts.  T == 1 under AUTO or GEMV runs the batch-1 matrix-vector
+ * path on the codes; every other T (and T == 1 under GEMM) runs the tensor-core path, whose
+ * grouped GEMM dequantizes each 64-input step of a weight tile to bf16 (scale * q + bias,
+ * rounded once) inside the kernel.  The small-batch matrix-vector path reads bf16 experts
+ * only: under GEMV, moe_forward and moe_route with T > 1 return MOE_ERR_UNSUPPORTED. */
 int moe_create_q4(const moe_config* cfg, const moe_weights_q4* w, moe_handle* out);
 
 /* Routing only (§ "Keep expert routing on the GPU"): the same kernels moe_forward runs for

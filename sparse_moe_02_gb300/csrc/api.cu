@@ -54,6 +54,21 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+// 2-D byte tensor [rows][inner] of 4-bit codes (row pitch inner bytes), box [128 rows][32
+// bytes] = one 64-input step of a 128-row tile, no swizzle.
+bool encode_codes(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {moe::kBK / 2, moe::kMTile};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -62,7 +77,7 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 struct moe_handle_s {
   moe_config cfg;
   moe_weights w;       // bf16 handle: the weights; 4-bit handle: only w_router, router_bias
-  bool q4 = false;     // 4-bit experts (batch-1 decode only)
+  bool q4 = false;     // 4-bit experts
   moe::Q4Weights wq{};
   Dims D;
   int device = 0, sms = 0;
@@ -196,7 +211,9 @@ int check_call(moe_handle h, const void* x, int T) {
   if (T > h->cfg.max_tokens) return MOE_ERR_UNSUPPORTED;
   if (T > 0 && !x) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x)) return MOE_ERR_ALIGNMENT;
-  if (h->cfg.schedule == MOE_SCHEDULE_GEMV && T > 1 && !moe::decode_batch_fits(h->D, T))
+  // the small-batch matrix-vector path reads bf16 experts only
+  if (h->cfg.schedule == MOE_SCHEDULE_GEMV && T > 1 &&
+      (h->q4 || !moe::decode_batch_fits(h->D, T)))
     return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -255,7 +272,7 @@ int forward_gemm(moe_handle h, const __nv_bfloat16* xd, int T, __nv_bfloat16* yd
   if (prof && (st = prof_mark(h, s, 2))) return st;
   if ((st = cuda_status(moe::launch_experts(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu,
                                             h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->h,
-                                            h->ys, h->sms, s))))
+                                            h->ys, h->sms, s, h->q4 ? &h->wq : nullptr))))
     return st;
   if (prof && (st = prof_mark(h, s, 3))) return st;
   return cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, h->sms, s));
@@ -277,7 +294,6 @@ int create_handle(const moe_config* cfg, const moe_weights* w, const moe_weights
   int st = check_config(cfg);
   if (st) return st;
   if ((st = w ? check_weights(w) : check_q4(wq))) return st;
-  if (wq && cfg->schedule == MOE_SCHEDULE_GEMM) return MOE_ERR_UNSUPPORTED;
 
   moe_handle_s* h = new (std::nothrow) moe_handle_s();
   if (!h) return MOE_ERR_NO_MEMORY;
@@ -336,7 +352,16 @@ int create_handle(const moe_config* cfg, const moe_weights* w, const moe_weights
   const Dims& D = h->D;
   bool ok = encode_2d(&h->tm_wr, h->w.w_router, D.d, kE, moe::kBK, kE) &&
             encode_2d(&h->tm_h, h->h, D.hdim, h->P_chunk, moe::kBK, 16);
-  // the tensor-core path's maps of the bf16 experts
+  // the tensor-core path's maps of the experts: 4-bit code bytes, or bf16 tiles
+  if (h->q4) {
+    const moe::Q4Weights& q = h->wq;
+    ok = ok && encode_codes(&h->tm_wg, q.gate.codes, D.d / 2, (uint64_t)kE * D.f) &&
+         encode_codes(&h->tm_wu, q.up.codes, D.d / 2, (uint64_t)kE * D.f) &&
+         encode_codes(&h->tm_wsg, q.s_gate.codes, D.d / 2, D.fs) &&
+         encode_codes(&h->tm_wsu, q.s_up.codes, D.d / 2, D.fs) &&
+         encode_codes(&h->tm_wd, q.down.codes, D.f / 2, (uint64_t)kE * D.d) &&
+         encode_codes(&h->tm_wsd, q.s_down.codes, D.fs / 2, D.d);
+  }
   ok = ok && (h->q4 ||
              (encode_2d(&h->tm_wg, w->w_gate, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
             encode_2d(&h->tm_wu, w->w_up, D.d, (uint64_t)kE * D.f, moe::kBK, moe::kMTile) &&
@@ -390,7 +415,7 @@ int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk
     return cuda_status(moe::launch_decode_router_shared(
         static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, idx, wt,
         offsets ? offsets : h->rws.offsets, pm, h->dws, h->rws.err, s, false));
-  if (use_batch(h, T))
+  if (!h->q4 && use_batch(h, T))
     return cuda_status(moe::launch_decode_batch_router_shared(
         static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, T, idx, wt,
         offsets ? offsets : h->rws.offsets, pm, h->dws, s, false));
@@ -410,8 +435,7 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
   const __nv_bfloat16* xd = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* yd = static_cast<__nv_bfloat16*>(y);
 
-  if (h->q4) {  // 4-bit experts: batch-1 decode only
-    if (T != 1) return MOE_ERR_UNSUPPORTED;
+  if (h->q4 && use_gemv(h, T)) {  // 4-bit experts, batch-1 decode
     if ((st = prof_mark(h, s, 0))) return st;
     if ((st = cuda_status(moe::launch_decode_q4_router_shared(xd, h->wq, h->D, h->dws, s))))
       return st;
@@ -443,7 +467,7 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
     return prof_finish_call(h, s, 3);
   }
 
-  if (use_batch(h, T)) {
+  if (!h->q4 && use_batch(h, T)) {  // the small-batch matrix-vector path reads bf16
     const moe::DecodeWeights W = decode_weights(h);
     if ((st = prof_mark(h, s, 0))) return st;
     if ((st = cuda_status(moe::launch_decode_batch_router_shared(xd, W, h->D, T, nullptr, nullptr,

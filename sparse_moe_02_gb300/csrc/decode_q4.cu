@@ -21,10 +21,6 @@ namespace {
 constexpr int kQWarps = 8;  // warps per block in every 4-bit decode kernel
 constexpr int kQB = 2;      // 16-byte code pieces per lane and row held in flight
 
-__device__ __forceinline__ float nib(uint32_t u, int n) {
-  return __uint_as_float(0x4B000000u | ((u >> (4 * n)) & 15u)) - 8388608.0f;
-}
-
 // Vectors in shared memory are stored swizzled: float4 k (k = 0..7) of 32-element piece p sits
 // in slot (k + p) mod 8 of the piece, so that eight lanes reading float4 k of eight
 // consecutive pieces touch all 32 banks.  Element i -> position:

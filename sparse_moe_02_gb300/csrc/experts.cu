@@ -24,14 +24,33 @@ constexpr int kTileB = kChunkRows * kBK * 2; // up to 192 token rows x 64 (24 KB
 
 // ---------------------------------------------------------------- gate/up + down, one launch
 
-constexpr int kXStages = 4;
-constexpr int kXStage = 2 * kTileA + kTileB;  // weight tile(s) | token rows
-constexpr int kXSmem = kXStages * kXStage + 1024 + 1024;
-constexpr int kXThreads = 384;                 // 12 warps, roles below
+// Ring of pipeline stages.  bf16 weights: 4 stages of (weight tile(s) | token rows).  4-bit
+// weights: 6 stages of (the two tiles' codes, 128 rows x 32 bytes each | token rows); the
+// dequantizing warps turn a stage's codes into bf16 tiles in tensor memory, from where the
+// MMA reads its A operand.
+template <bool Q4>
+struct XCfg {
+  static constexpr int kStages = Q4 ? 6 : 4;
+  static constexpr int kBOff = Q4 ? 2 * kMTile * (kBK / 2) : 2 * kTileA;  // token rows
+  static constexpr int kStage = kBOff + kTileB;
+  static constexpr int kSmem = kStages * kStage + 1024 + 1024;
+  static constexpr int kDqWarps = Q4 ? 8 : 0;                 // warps 12-19 (4-bit only)
+  static constexpr int kThreads = 384 + 32 * kDqWarps;
+};
 constexpr int kXRowThreads = 64;               // warps 2-3: token-row copies (gate/up units)
 constexpr int kXEpiWarps = 8;                  // warps 4-11: two per TMEM lane quadrant
 constexpr int kXQueue = 4;                     // unit indices handed out ahead
-constexpr int kXQueueReaders = 2 + 1 + kXEpiWarps;  // row-producer warps, MMA, epilogue warps
+constexpr int kQTile = kMTile * (kBK / 2);     // one stage's codes of one 128-row tile (4 KB)
+// TMEM columns: accumulators [0, N) and [256, 256 + N) with N <= 192; the 4-bit path's two
+// dequantized A buffers (two 32-column tiles each) sit in the columns above them
+__device__ __forceinline__ uint32_t abuf_col(int b) { return b ? 448u : 192u; }
+
+// 4-bit scales and biases of the six expert matrices (gate, up, down, shared gate, shared up,
+// shared down): group (r, kb) of a matrix with K inputs per row at r * (K / 64) + kb
+struct XQ4 {
+  const __nv_bfloat16* s[6];
+  const __nv_bfloat16* b[6];
+};
 
 struct XArgs {
   const Unit* units_gu;
@@ -45,12 +64,32 @@ struct XArgs {
   __nv_bfloat16* ys;
   int d, f, fs, hdim;
   int* err;
+  XQ4 q4;
 };
 
 struct XUnit {
   Unit u;
   bool down;
 };
+
+// Eight 4-bit codes (one 32-bit word: input 2i in the lower nibble of byte i) to four bf16
+// pairs scale * q + bias, input 2i in the low half of pair i.  0x4300 | q is the bf16 value
+// 128 + q exactly, so (128 + q) - 128 is q exactly, and the fused multiply-add rounds
+// scale * q + bias once to bf16.
+__device__ __forceinline__ void dequant_q4x8(uint32_t c, uint32_t s2, uint32_t b2, uint32_t* o) {
+  const uint32_t lo = c & 0x0F0F0F0Fu;         // inputs 0, 2, 4, 6
+  const uint32_t hi = (c >> 4) & 0x0F0F0F0Fu;  // inputs 1, 3, 5, 7
+  const uint32_t p0 = __byte_perm(lo, hi, 0x5140);  // bytes: inputs 0 1 2 3
+  const uint32_t p1 = __byte_perm(lo, hi, 0x7362);  // inputs 4 5 6 7
+  const uint32_t m[4] = {__byte_perm(p0, 0x43434343u, 0x4140), __byte_perm(p0, 0x43434343u, 0x4342),
+                         __byte_perm(p1, 0x43434343u, 0x4140), __byte_perm(p1, 0x43434343u, 0x4342)};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t qv;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(qv) : "r"(m[i]), "r"(0x3F803F80u), "r"(0xC300C300u));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(o[i]) : "r"(qv), "r"(s2), "r"(b2));
+  }
+}
 
 __device__ __forceinline__ XUnit unit_at(const XArgs& a, int i, int n_gu) {
   XUnit r;
@@ -69,8 +108,13 @@ __device__ __forceinline__ XUnit unit_at(const XArgs& a, int i, int n_gu) {
 // number of gate/up tiles before loading h rows.
 // Warp roles: 0 = TMA producer (weight tiles; h rows of down units); 1 = MMA issuer (TMEM
 // owner); 2-3 = token-row producers of gate/up units (16-byte cp.async gathers from x into
-// the 128-byte swizzle; for down units they only arrive); 4-11 = epilogue.
-__global__ void __launch_bounds__(kXThreads, 1)
+// the 128-byte swizzle; for down units they only arrive); 4-11 = epilogue; with 4-bit weights
+// 12-19 = dequantization (thread = one row of one of the stage's two 128-row tiles).
+// 4-bit weights (§ "Dequantize weights during matrix multiplication"): the weight maps are
+// maps of the code bytes (box 32 bytes x 128 rows, no swizzle), each group's scale and bias
+// come from a.q4, and the MMA takes A from tensor memory instead of shared memory.
+template <bool Q4>
+__global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
     experts_kernel(const __grid_constant__ CUtensorMap tm_wg,
                    const __grid_constant__ CUtensorMap tm_wu,
                    const __grid_constant__ CUtensorMap tm_wsg,
@@ -78,11 +122,17 @@ __global__ void __launch_bounds__(kXThreads, 1)
                    const __grid_constant__ CUtensorMap tm_h,
                    const __grid_constant__ CUtensorMap tm_wd,
                    const __grid_constant__ CUtensorMap tm_wsd, XArgs a) {
+  using C = XCfg<Q4>;
+  constexpr int kXStages = C::kStages;
+  constexpr int kXStage = C::kStage;
+  constexpr int kXQueueReaders = 2 + 1 + kXEpiWarps + C::kDqWarps;  // every warp but the TMA's
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kXStages * kXStage);
   uint64_t* empty = full + kXStages;
-  uint64_t* tfull = empty + kXStages;  // [2] TMEM halves
+  uint64_t* cfull = empty + kXStages;  // [kXStages] codes landed (4-bit)
+  uint64_t* aempty = cfull + kXStages; // [2] dequantized A buffer free again (4-bit)
+  uint64_t* tfull = aempty + 2;        // [2] TMEM halves
   uint64_t* tempty = tfull + 2;        // [2]
   uint64_t* qfull = tempty + 2;        // [kXQueue] unit-index queue
   uint64_t* qempty = qfull + kXQueue;  // [kXQueue]
@@ -93,9 +143,13 @@ __global__ void __launch_bounds__(kXThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kXStages; ++s) {
-      mbar_init(&full[s], 1 + kXRowThreads);  // TMA producer + one arrival per row thread
+      // TMA producer + one arrival per row thread (+ one per dequantizing warp)
+      mbar_init(&full[s], 1 + kXRowThreads + C::kDqWarps);
       mbar_init(&empty[s], 1);
+      mbar_init(&cfull[s], 1);
     }
+    mbar_init(&aempty[0], 1);
+    mbar_init(&aempty[1], 1);
     for (int i = 0; i < kXQueue; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], kXQueueReaders);
@@ -181,9 +235,18 @@ __global__ void __launch_bounds__(kXThreads, 1)
           for (int kb = 0; kb < a.d / kBK; ++kb) {
             if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
             uint8_t* st = smem + stage * kXStage;
-            mbar_arrive_expect_tx(&full[stage], 2 * kTileA);
-            tma_load_2d(st, mg, &full[stage], kb * kBK, arow, pw);
-            tma_load_2d(st + kTileA, mu, &full[stage], kb * kBK, arow, pw);
+            if constexpr (Q4) {
+              // codes of both tiles (x counts bytes: 32 per 64-input step); the token rows
+              // arrive by cp.async, so full[] only gets this lane's plain arrival
+              mbar_arrive_expect_tx(&cfull[stage], 2 * kQTile);
+              tma_load_2d(st, mg, &cfull[stage], kb * (kBK / 2), arow, pw);
+              tma_load_2d(st + kQTile, mu, &cfull[stage], kb * (kBK / 2), arow, pw);
+              mbar_arrive(&full[stage]);
+            } else {
+              mbar_arrive_expect_tx(&full[stage], 2 * kTileA);
+              tma_load_2d(st, mg, &full[stage], kb * kBK, arow, pw);
+              tma_load_2d(st + kTileA, mu, &full[stage], kb * kBK, arow, pw);
+            }
             if (++stage == kXStages) { stage = 0; ph ^= 1; }
           }
         } else {
@@ -210,16 +273,25 @@ __global__ void __launch_bounds__(kXThreads, 1)
           const CUtensorMap* mw = shared ? &tm_wsd : &tm_wd;
           const int arow = (shared ? 0 : U.g * a.d) + U.mt * 2 * kMTile;
           const bool two = (U.mt * 2 + 1) * kMTile < a.d;
-          const uint32_t bytes = (two ? 2 : 1) * kTileA + (uint32_t)N * kBK * 2;
+          const uint32_t hbytes = (uint32_t)N * kBK * 2;
+          const uint32_t bytes = (Q4 ? 0 : (two ? 2 : 1) * kTileA) + hbytes;
           for (int kb = 0; kb < K / kBK; ++kb) {
             if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
             uint8_t* st = smem + stage * kXStage;
-            mbar_arrive_expect_tx(&full[stage], bytes);
             const uint64_t pw = shared ? keep_h : stream_w;
-            tma_load_2d(st, mw, &full[stage], kb * kBK, arow, pw);
-            if (two) tma_load_2d(st + kTileA, mw, &full[stage], kb * kBK, arow + kMTile, pw);
+            if constexpr (Q4) {
+              mbar_arrive_expect_tx(&cfull[stage], (two ? 2 : 1) * kQTile);
+              tma_load_2d(st, mw, &cfull[stage], kb * (kBK / 2), arow, pw);
+              if (two)
+                tma_load_2d(st + kQTile, mw, &cfull[stage], kb * (kBK / 2), arow + kMTile, pw);
+            }
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            if constexpr (!Q4) {
+              tma_load_2d(st, mw, &full[stage], kb * kBK, arow, pw);
+              if (two) tma_load_2d(st + kTileA, mw, &full[stage], kb * kBK, arow + kMTile, pw);
+            }
             for (int r = 0; r < N / 16; ++r)
-              tma_load_2d(st + 2 * kTileA + r * 2048, &tm_h, &full[stage], kb * kBK,
+              tma_load_2d(st + C::kBOff + r * 2048, &tm_h, &full[stage], kb * kBK,
                           U.p0 + 16 * r, keep_h);
             if (++stage == kXStages) { stage = 0; ph ^= 1; }
           }
@@ -231,6 +303,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t ph = 0, tph[2] = {0, 0};
+      int ab = 0;  // 4-bit: dequantized A buffer of the next stage
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int i = next_unit_1(k, ok);
@@ -252,13 +325,27 @@ __global__ void __launch_bounds__(kXThreads, 1)
           fence_proxy_async_smem();  // token rows of gate/up units come from cp.async
           tc_fence_after();
           const uint32_t s0 = smem_u32(smem + stage * kXStage);
-          const uint32_t s1 = s0 + kTileA, sb = s0 + 2 * kTileA;
+          const uint32_t s1 = s0 + kTileA, sb = s0 + C::kBOff;
+          if constexpr (Q4) {
+            // A from tensor memory: 16 inputs = 8 columns per MMA, tile 1 at +32 columns
+            const uint32_t a0 = tmem + abuf_col(ab);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bd = sdesc_k128(sb + kk * 32);
-            const uint32_t acc = (kb | kk) != 0;
-            mma_bf16(tmem, sdesc_k128(s0 + kk * 32), bd, idesc, acc);
-            if (two) mma_bf16(tmem + 256, sdesc_k128(s1 + kk * 32), bd, idesc, acc);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t bd = sdesc_k128(sb + kk * 32);
+              const uint32_t acc = (kb | kk) != 0;
+              mma_bf16_ts(tmem, a0 + kk * 8, bd, idesc, acc);
+              if (two) mma_bf16_ts(tmem + 256, a0 + 32 + kk * 8, bd, idesc, acc);
+            }
+            mma_commit(&aempty[ab]);
+            ab ^= 1;
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t bd = sdesc_k128(sb + kk * 32);
+              const uint32_t acc = (kb | kk) != 0;
+              mma_bf16(tmem, sdesc_k128(s0 + kk * 32), bd, idesc, acc);
+              if (two) mma_bf16(tmem + 256, sdesc_k128(s1 + kk * 32), bd, idesc, acc);
+            }
           }
           mma_commit(&empty[stage]);
           if (++stage == kXStages) { stage = 0; ph ^= 1; }
@@ -300,7 +387,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         if (!X.down) {
           const uint32_t sb =
-              smem_u32(smem + stage * kXStage + 2 * kTileA) + crow * 128 + swz;
+              smem_u32(smem + stage * kXStage + C::kBOff) + crow * 128 + swz;
 #pragma unroll
           for (int r = 0; r < kChunkRows / 8; ++r)
             if (r < nr) cp_async_16(sb + r * 1024, src[r] + kb * kBK, keep_x);
@@ -311,7 +398,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         if (++stage == kXStages) { stage = 0; ph ^= 1; }
       }
     }
-  } else {
+  } else if (warp < 12) {
     // ---- epilogue: thread = one weight row of the tile; the two warps of a lane quadrant
     // take alternate 16-column chunks
     const int q = warp & 3, half = (warp - 4) >> 2;
@@ -385,6 +472,83 @@ __global__ void __launch_bounds__(kXThreads, 1)
         }
         tph[0] ^= 1;
         tph[1] ^= 1;
+      }
+    }
+  } else if constexpr (Q4) {
+    // ---- dequantization: thread = row r of tile mtile (0: gate or the first down tile,
+    // 1: up or the second), in the lane quadrant its warp may address.  Per stage: the row's
+    // 64 codes (32 bytes) from shared memory, one scale and one bias, 32 columns of bf16 pairs
+    // into the A buffer in tensor memory.
+    const int q = warp & 3, mtile = (warp - 12) >> 2;
+    const int r = q * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    int stage = 0, ab = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int i = next_unit(k, ok);
+      if (i < 0) break;
+      const XUnit X = unit_at(a, i, n_gu);
+      const Unit& U = X.u;
+      const bool shared = U.g == kE;
+      int K, mat;
+      size_t row;
+      if (!X.down) {
+        K = a.d;
+        mat = (shared ? 3 : 0) + mtile;
+        row = (shared ? 0 : (size_t)U.g * a.f) + U.mt * kMTile + r;
+      } else {
+        K = shared ? a.fs : a.f;
+        mat = shared ? 5 : 2;
+        row = (shared ? 0 : (size_t)U.g * a.d) + (U.mt * 2 + mtile) * kMTile + r;
+      }
+      // a down unit whose outputs end inside its first tile has no second tile
+      const bool active = !X.down || mtile == 0 || (U.mt * 2 + 1) * kMTile < a.d;
+      const int G = K / kBK;
+      const unsigned short* sp = reinterpret_cast<const unsigned short*>(a.q4.s[mat]) + row * G;
+      const unsigned short* bp = reinterpret_cast<const unsigned short*>(a.q4.b[mat]) + row * G;
+      // the scale and bias of the next step are loaded one step ahead
+      uint32_t sv = active ? __ldg(sp) : 0u, bv = active ? __ldg(bp) : 0u;
+      for (int kb = 0; kb < G; ++kb) {
+        uint32_t sn = 0, bn = 0;
+        if (active && kb + 1 < G) {
+          sn = __ldg(sp + kb + 1);
+          bn = __ldg(bp + kb + 1);
+        }
+        // codes landed: convert into registers while the MMA may still read this A buffer
+        bool w = mbar_wait(&cfull[stage], ph, a.err);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        uint32_t v[32];
+        if (active) {
+          const uint4* cp =
+              reinterpret_cast<const uint4*>(smem + stage * kXStage + mtile * kQTile + r * 32);
+          const uint4 c0 = cp[0], c1 = cp[1];
+          const uint32_t s2 = sv | (sv << 16), b2 = bv | (bv << 16);
+          dequant_q4x8(c0.x, s2, b2, v + 0);
+          dequant_q4x8(c0.y, s2, b2, v + 4);
+          dequant_q4x8(c0.z, s2, b2, v + 8);
+          dequant_q4x8(c0.w, s2, b2, v + 12);
+          dequant_q4x8(c1.x, s2, b2, v + 16);
+          dequant_q4x8(c1.y, s2, b2, v + 20);
+          dequant_q4x8(c1.z, s2, b2, v + 24);
+          dequant_q4x8(c1.w, s2, b2, v + 28);
+        }
+        // every warp waits on both barriers each step, active or not, to keep their phases
+        w = mbar_wait(&aempty[ab], aph ^ 1, a.err);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        if (active) {
+          tmem_st32(tmem + lane_off + abuf_col(ab) + 32u * mtile, v);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+        sv = sn;
+        bv = bn;
+        if (++stage == kXStages) { stage = 0; ph ^= 1; }
+        ab ^= 1;
+        if (ab == 0) aph ^= 1;
       }
     }
   }
@@ -513,8 +677,12 @@ __global__ void __launch_bounds__(kCbThreads, 1)
 }  // namespace
 
 cudaError_t prepare_expert_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kXSmem);
+  cudaError_t e = cudaFuncSetAttribute(experts_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       XCfg<false>::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(experts_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           XCfg<true>::kSmem);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kCbSmem);
@@ -525,11 +693,19 @@ cudaError_t launch_experts(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
                            const CUtensorMap& tm_wsu, const CUtensorMap& tm_h,
                            const CUtensorMap& tm_wd, const CUtensorMap& tm_wsd, const Dims& D,
                            const RouteWs& ws, __nv_bfloat16* h, __nv_bfloat16* ys, int grid,
-                           cudaStream_t s) {
+                           cudaStream_t s, const Q4Weights* q4) {
   XArgs a{ws.units_gu, ws.units_dn, ws.n_units, ws.next_unit, ws.chunk_done, ws.grow, x, h, ys,
-          D.d, D.f, D.fs, D.hdim, ws.err};
-  return launch_pdl(experts_kernel, dim3(grid), dim3(kXThreads), kXSmem, s, tm_wg, tm_wu, tm_wsg,
-                    tm_wsu, tm_h, tm_wd, tm_wsd, a);
+          D.d, D.f, D.fs, D.hdim, ws.err, XQ4{}};
+  if (!q4)
+    return launch_pdl(experts_kernel<false>, dim3(grid), dim3(XCfg<false>::kThreads),
+                      XCfg<false>::kSmem, s, tm_wg, tm_wu, tm_wsg, tm_wsu, tm_h, tm_wd, tm_wsd, a);
+  const Q4Matrix* m[6] = {&q4->gate, &q4->up, &q4->down, &q4->s_gate, &q4->s_up, &q4->s_down};
+  for (int i = 0; i < 6; ++i) {
+    a.q4.s[i] = m[i]->scales;
+    a.q4.b[i] = m[i]->biases;
+  }
+  return launch_pdl(experts_kernel<true>, dim3(grid), dim3(XCfg<true>::kThreads),
+                    XCfg<true>::kSmem, s, tm_wg, tm_wu, tm_wsg, tm_wsu, tm_h, tm_wd, tm_wsd, a);
 }
 
 cudaError_t launch_combine(int T, const Dims& D, const float* topk_w, const RouteWs& ws,

@@ -87,15 +87,19 @@ constexpr int kFusedPlanBlocks = 128;
 cudaError_t launch_route_plan_scatter(int T, const Dims& D, const int32_t* topk_idx,
                                       int32_t* perm, const RouteWs& ws, cudaStream_t s);
 
+struct Q4Weights;
+
 // Both grouped GEMMs in one persistent launch: the gate/up units (SwiGLU epilogue, h [P][hdim]
 // bf16) and then the down units (ys [P][d] bf16), a down unit starting once every gate/up unit
-// of its chunk has published its h.
+// of its chunk has published its h.  With q4 NULL the weight maps are bf16 maps (box 64 x
+// 128, 128-byte swizzle); with q4 set they are maps of the 4-bit code bytes (box 32 bytes x
+// 128 rows, no swizzle) and q4 supplies the scales and biases.
 cudaError_t launch_experts(const __nv_bfloat16* x, const CUtensorMap& tm_wg,
                            const CUtensorMap& tm_wu, const CUtensorMap& tm_wsg,
                            const CUtensorMap& tm_wsu, const CUtensorMap& tm_h,
                            const CUtensorMap& tm_wd, const CUtensorMap& tm_wsd, const Dims& D,
                            const RouteWs& ws, __nv_bfloat16* h, __nv_bfloat16* ys, int grid,
-                           cudaStream_t s);
+                           cudaStream_t s, const Q4Weights* q4 = nullptr);
 
 // y[t] = sum_j w[t][j] ys[prow[t][j]] + ys[prow[t][8]] in fp32, rounded once to bf16
 // (persistent: at most `grid` blocks, one per SM).

@@ -1,12 +1,14 @@
-"""GPU parity of batch-1 decode with 4-bit group-affine experts (moe_create_q4) against the
-CPU oracle's 4-bit layer: routing bit-exact, outputs within the layer tolerance."""
+"""GPU parity of the layer with 4-bit group-affine experts (moe_create_q4) against the CPU
+oracle's 4-bit layer, on both paths (batch-1 matrix-vector decode and the dequantizing
+tensor-core grouped GEMM): routing bit-exact, outputs within the layer tolerance."""
 import numpy as np
 import pytest
 
 import sparse_moe_02_gb300 as moe
 import synth
+import oracle
 from _cases import (assert_close, bf16_bits, build_case, oracle_outputs_q4, oracle_route,
-                    q4_to_device, to_device)
+                    q4_to_device, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,28 +48,83 @@ def test_q4_decode_layers_of_the_benchmark():
         assert_close(got["y"], oracle_outputs_q4(c), f"q4 decode layer {layer}")
 
 
+# ---------------------------------------------------------------- tensor-core path (T > 1)
+# The grouped GEMM dequantizes each 64-input step of a weight tile to bf16 in tensor memory:
+# routing bit-exact, outputs within the layer tolerance of the oracle's fp32 dequantization.
+
+@pytest.mark.parametrize("d,f,fs,T,seed,skew", [
+    (512, 128, 128, 64, 0, False),     # the tiny layer's shape, every token
+    (512, 128, 256, 300, 1, False),    # ragged T, shared inner dim != routed
+    (640, 384, 128, 77, 3, False),     # d = 5 x 128: the last down unit has one 128-row tile
+    (1024, 256, 256, 500, 4, True),    # skewed routing: empty and crowded experts
+])
+def test_q4_prefill_matches_oracle(d, f, fs, T, seed, skew):
+    c = build_case("q4-prefill", d=d, f=f, fs=fs, T=T, seed=seed, skew=skew, full_host=False)
+    got = _run_q4(c)
+    ref = oracle_route(c)
+    assert np.array_equal(got["topk_idx"], ref["topk_idx"])
+    assert np.array_equal(got["perm"], ref["perm"])
+    assert np.array_equal(got["offsets"], ref["offsets"])
+    assert np.max(np.abs(got["topk_w"] - ref["topk_w"])) <= 1e-5
+    assert_close(got["y"], oracle_outputs_q4(c), f"q4 prefill d={d} f={f} fs={fs} T={T}")
+
+
+@pytest.mark.parametrize("skew", [False, True], ids=["balanced", "skewed"])
+def test_q4_prefill_4096(skew):
+    """The benchmark's prefill shape (T=4096, d=2048, f=fs=512) in the launch configuration
+    the benchmark times; outputs on sampled tokens."""
+    c = build_case("q4-prefill-4096", d=2048, f=512, fs=512, T=4096, seed=0, skew=skew,
+                   full_host=False)
+    got = _run_q4(c)
+    toks = sample_tokens(c.T, n_edge=16, stride=67)
+    idx, w = oracle.select(oracle.router_logits_f32(c.x[toks], c.w_r, c.bias), c.dims.k)
+    assert np.array_equal(got["topk_idx"][toks], idx)
+    assert_close(got["y"][toks], oracle_outputs_q4(c, toks), f"q4 prefill 4096 skew={skew}")
+
+
+def test_q4_chunked_and_single_token_tensor_core():
+    """Chunking leaves the bytes unchanged; T = 1 under the GEMM schedule goes through the
+    dequantizing grouped GEMM and matches the oracle."""
+    import torch
+    T = 700
+    c = build_case("q4-chunked", d=512, f=128, fs=256, T=T, seed=5, full_host=False)
+    W = q4_to_device(c)
+    x = torch.from_numpy(c.x.view(np.int16)).cuda().view(torch.bfloat16)
+    L0 = moe.MoeLayer(W, T)
+    L1 = moe.MoeLayer(W, T, chunk_tokens=256)
+    y0, y1 = bf16_bits(L0.forward(x)), bf16_bits(L1.forward(x))
+    torch.cuda.synchronize()
+    assert L0.device_error() == moe.MOE_OK and L1.device_error() == moe.MOE_OK
+    assert np.array_equal(y0, y1)
+    toks = sample_tokens(T, n_edge=16, stride=29)
+    assert_close(y1[toks], oracle_outputs_q4(c, toks), "q4 chunked")
+    L0.close()
+    L1.close()
+    c1 = build_case("q4-one", d=512, f=128, fs=256, T=1, seed=6, full_host=False)
+    got = _run_q4(c1, moe.MOE_SCHEDULE_GEMM)
+    assert_close(got["y"], oracle_outputs_q4(c1), "q4 T=1 tensor-core")
+
+
 def test_q4_handle_limits():
     import torch
     c = build_case("q4-limits", d=512, f=128, fs=128, T=5, seed=9, full_host=False)
     W = q4_to_device(c)
     x = torch.from_numpy(c.x.view(np.int16)).cuda().view(torch.bfloat16)
-    L = moe.MoeLayer(W, 8)
+    # the small-batch matrix-vector path reads bf16: GEMV with T > 1 is refused
+    L = moe.MoeLayer(W, 8, schedule=moe.MOE_SCHEDULE_GEMV)
     y = torch.empty_like(x)
-    # more than one token: the tensor-core path reads bf16 experts
     assert moe.moe_forward(L.handle, x.data_ptr(), 5, y.data_ptr(), None) == \
         moe.MOE_ERR_UNSUPPORTED
-    # routing works for any T (the router stays bf16)
+    L.close()
+    # AUTO: T = 5 on the tensor-core path; routing as the oracle's
+    L = moe.MoeLayer(W, 8)
+    y = L.forward(x)
     r = L.route(x)
     torch.cuda.synchronize()
     assert np.array_equal(r["topk_idx"].cpu().numpy(), oracle_route(c)["topk_idx"])
     assert L.device_error() == moe.MOE_OK
+    assert_close(bf16_bits(y), oracle_outputs_q4(c), "q4 T=5")
     L.close()
-    cfg = moe.moe_config(512, 256, 8, 128, 128, 8, moe.MOE_SCHEDULE_GEMM, 0)
-    w = moe.moe_weights_q4(W["w_router"].data_ptr(), None,
-                           *(moe.moe_q4_matrix(*(t.data_ptr() for t in W[n]))
-                             for n in synth.Q4_NAMES))
-    st, h = moe.moe_create_q4(cfg, w)
-    assert st == moe.MOE_ERR_UNSUPPORTED and not h.value
 
 
 def test_q4_device_fill_equals_host():
