@@ -60,6 +60,8 @@ def parse_args():
                    help="skip the T = 2..5 decode lines")
     p.add_argument("--sweep", action="store_true",
                    help="also time the prefill layer at T = 256 .. 131072 (balanced)")
+    p.add_argument("--sweep-tokens", type=str, default=None,
+                   help="comma-separated T values for --sweep (default: 256 .. 131072)")
     return p.parse_args()
 
 
@@ -345,13 +347,14 @@ def run_prefill(torch, moe, args, rank, world, P_hbm, P_tc, peak_note):
 SWEEP_T = (256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536, 131072)
 
 
-def time_prefill(torch, moe, T, skew, steps, warmup, seed, P_hbm, P_tc):
+def time_prefill(torch, moe, T, skew, steps, warmup, seed, P_hbm, P_tc, q4=False):
     """Layer time (L2 flushed before every step) at T tokens, balanced or skewed routing
     (router bias -2.4 ln(rank) over a seeded permutation of the experts), with the bytes and
-    FLOPs of that routing and the fraction of the binding floor max(bytes/B, FLOPs/P)."""
+    FLOPs of that routing and the fraction of the binding floor max(bytes/B, FLOPs/P).  With
+    q4 the experts are 4-bit (4.5 bits per weight with the group scales and biases)."""
     dims = synth.Dims(d=D, f=F, fs=FS)
     bias = synth.skew_bias(seed, 0, E) if skew else None
-    W = device_weights(torch, seed, 0, dims, bias)
+    W = (q4_device_weights if q4 else device_weights)(torch, seed, 0, dims, bias)
     x = torch.from_numpy(synth.x_rows(seed, 0, T, D).view(np.int16)).cuda().view(torch.bfloat16)
     y = torch.empty_like(x)
     layer = moe.MoeLayer(W, T)
@@ -372,9 +375,13 @@ def time_prefill(torch, moe, T, skew, steps, warmup, seed, P_hbm, P_tc):
     ms = statistics.median(a.elapsed_time(b) for a, b in ev)
     layer.close()
     _, _, byts, flops = algorithmic(counts, T)
+    if q4:
+        ne = int((counts > 0).sum())
+        byts -= (ne * 3 * F * D + 3 * FS * D) * 23 // 16  # 2 bytes -> 9/16 byte per weight
     t = ms / 1e3
     floor = max(byts / (P_hbm * 1e9), flops / (P_tc * 1e12))
-    return {"T": T, "routing": "skewed" if skew else "balanced", "ms": ms,
+    return {"T": T, "routing": "skewed" if skew else "balanced", "weights": "4-bit" if q4 else
+            "bf16", "ms": ms,
             "tokens_per_s": T / t, "hbm_frac": byts / t / 1e9 / P_hbm,
             "tensor_frac": flops / t / 1e12 / P_tc, "floor_us": floor * 1e6,
             "frac_of_floor": floor / t, "bound": "hbm" if byts / (P_hbm * 1e9) >= flops /
@@ -705,8 +712,12 @@ def main():
         torch, moe, T_PREFILL, True, min(args.steps, 50), max(3, args.warmup), rank, P_hbm, P_tc)
     sweep = None
     if args.sweep:
+        ts = [int(t) for t in args.sweep_tokens.split(",")] if args.sweep_tokens else SWEEP_T
         sweep = [time_prefill(torch, moe, t, False, min(args.steps, 20), 3, rank, P_hbm, P_tc)
-                 for t in SWEEP_T]
+                 for t in ts]
+        if not args.no_q4:
+            sweep += [time_prefill(torch, moe, t, False, min(args.steps, 20), 3, rank, P_hbm,
+                                   P_tc, q4=True) for t in ts]
     pre_q4 = None if args.no_q4 else run_prefill_q4(torch, moe, args, rank, P_hbm, P_tc)
     dec = None if args.no_decode else run_decode(torch, moe, args, rank, world, P_hbm)
     clk = clocks.stop()

@@ -91,6 +91,22 @@ __device__ __forceinline__ void dequant_q4x8(uint32_t c, uint32_t s2, uint32_t b
   }
 }
 
+// One row's 64 codes of a step (two 16-byte words in shared memory) to 32 columns of bf16
+// pairs with scale s and bias b (bf16 bits).
+__device__ __forceinline__ void dequant_q4_row(const uint4* cp, uint32_t s, uint32_t b,
+                                               uint32_t* v) {
+  const uint4 c0 = cp[0], c1 = cp[1];
+  const uint32_t s2 = s | (s << 16), b2 = b | (b << 16);
+  dequant_q4x8(c0.x, s2, b2, v + 0);
+  dequant_q4x8(c0.y, s2, b2, v + 4);
+  dequant_q4x8(c0.z, s2, b2, v + 8);
+  dequant_q4x8(c0.w, s2, b2, v + 12);
+  dequant_q4x8(c1.x, s2, b2, v + 16);
+  dequant_q4x8(c1.y, s2, b2, v + 20);
+  dequant_q4x8(c1.z, s2, b2, v + 24);
+  dequant_q4x8(c1.w, s2, b2, v + 28);
+}
+
 __device__ __forceinline__ XUnit unit_at(const XArgs& a, int i, int n_gu) {
   XUnit r;
   r.down = i >= n_gu;
@@ -109,7 +125,7 @@ __device__ __forceinline__ XUnit unit_at(const XArgs& a, int i, int n_gu) {
 // Warp roles: 0 = TMA producer (weight tiles; h rows of down units); 1 = MMA issuer (TMEM
 // owner); 2-3 = token-row producers of gate/up units (16-byte cp.async gathers from x into
 // the 128-byte swizzle; for down units they only arrive); 4-11 = epilogue; with 4-bit weights
-// 12-19 = dequantization (thread = one row of one of the stage's two 128-row tiles).
+// 12-19 = dequantization (two groups of four warps on alternate steps).
 // 4-bit weights (§ "Dequantize weights during matrix multiplication"): the weight maps are
 // maps of the code bytes (box 32 bytes x 128 rows, no swizzle), each group's scale and bias
 // come from a.q4, and the MMA takes A from tensor memory instead of shared memory.
@@ -143,8 +159,8 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kXStages; ++s) {
-      // TMA producer + one arrival per row thread (+ one per dequantizing warp)
-      mbar_init(&full[s], 1 + kXRowThreads + C::kDqWarps);
+      // TMA producer + one arrival per row thread (+ one per warp of a dequantizing group)
+      mbar_init(&full[s], 1 + kXRowThreads + C::kDqWarps / 2);
       mbar_init(&empty[s], 1);
       mbar_init(&cfull[s], 1);
     }
@@ -227,6 +243,25 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
         const bool shared = U.g == kE;
         const int N = round_up(U.nrows, kRowAlign);
         if (!push(nxt < n_all ? nxt : -1)) { ok = false; break; }
+        if constexpr (Q4) {
+          // the unit's group scales and biases (one contiguous block per array: consecutive
+          // rows) into L2 with its first codes, so that the dequantizing warps' loads hit L2
+          if (!X.down) {
+            const int G = a.d / kBK;
+            const size_t r0 = (shared ? 0 : (size_t)U.g * a.f) + U.mt * kMTile;
+            for (int m = 0; m < 2; ++m) {
+              const int mat = (shared ? 3 : 0) + m;
+              prefetch_l2_bulk(a.q4.s[mat] + r0 * G, kMTile * G * 2);
+              prefetch_l2_bulk(a.q4.b[mat] + r0 * G, kMTile * G * 2);
+            }
+          } else {
+            const int G = (shared ? a.fs : a.f) / kBK, mat = shared ? 5 : 2;
+            const size_t r0 = (shared ? 0 : (size_t)U.g * a.d) + U.mt * 2 * kMTile;
+            const int rows = (U.mt * 2 + 1) * kMTile < a.d ? 2 * kMTile : kMTile;
+            prefetch_l2_bulk(a.q4.s[mat] + r0 * G, rows * G * 2);
+            prefetch_l2_bulk(a.q4.b[mat] + r0 * G, rows * G * 2);
+          }
+        }
         if (!X.down) {
           const CUtensorMap* mg = shared ? &tm_wsg : &tm_wg;
           const CUtensorMap* mu = shared ? &tm_wsu : &tm_wu;
@@ -475,14 +510,18 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
       }
     }
   } else if constexpr (Q4) {
-    // ---- dequantization: thread = row r of tile mtile (0: gate or the first down tile,
-    // 1: up or the second), in the lane quadrant its warp may address.  Per stage: the row's
-    // 64 codes (32 bytes) from shared memory, one scale and one bias, 32 columns of bf16 pairs
-    // into the A buffer in tensor memory.
-    const int q = warp & 3, mtile = (warp - 12) >> 2;
+    // ---- dequantization: two groups of four warps take alternate pipeline steps (group g
+    // the steps that fill A buffer g; with an even number of ring stages each group always
+    // uses the same ring slots), so a warp has two step periods for its step.  Thread = row r
+    // of both tiles (gate and up, or the two down tiles) in the lane quadrant its warp may
+    // address.  Per step and tile: the row's 64 codes (32 bytes) from shared memory, one scale
+    // and one bias, 32 columns of bf16 pairs into the A buffer in tensor memory.
+    static_assert(kXStages % 2 == 0, "each dequantization group keeps its own ring slots");
+    const int q = warp & 3, grp = (warp - 12) >> 2;
     const int r = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    int stage = 0, ab = 0;
+    const uint32_t acol = abuf_col(grp);
+    int stage = grp, n = 0;  // this group's next ring slot; steps of the units before (both groups)
     uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -491,64 +530,73 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
       const XUnit X = unit_at(a, i, n_gu);
       const Unit& U = X.u;
       const bool shared = U.g == kE;
-      int K, mat;
-      size_t row;
+      int K, mat0, mat1;
+      size_t row0, row1;
       if (!X.down) {
         K = a.d;
-        mat = (shared ? 3 : 0) + mtile;
-        row = (shared ? 0 : (size_t)U.g * a.f) + U.mt * kMTile + r;
+        mat0 = shared ? 3 : 0;
+        mat1 = mat0 + 1;
+        row0 = row1 = (shared ? 0 : (size_t)U.g * a.f) + U.mt * kMTile + r;
       } else {
         K = shared ? a.fs : a.f;
-        mat = shared ? 5 : 2;
-        row = (shared ? 0 : (size_t)U.g * a.d) + (U.mt * 2 + mtile) * kMTile + r;
+        mat0 = mat1 = shared ? 5 : 2;
+        row0 = (shared ? 0 : (size_t)U.g * a.d) + U.mt * 2 * kMTile + r;
+        row1 = row0 + kMTile;
       }
       // a down unit whose outputs end inside its first tile has no second tile
-      const bool active = !X.down || mtile == 0 || (U.mt * 2 + 1) * kMTile < a.d;
+      const bool two = !X.down || (U.mt * 2 + 1) * kMTile < a.d;
       const int G = K / kBK;
-      const unsigned short* sp = reinterpret_cast<const unsigned short*>(a.q4.s[mat]) + row * G;
-      const unsigned short* bp = reinterpret_cast<const unsigned short*>(a.q4.b[mat]) + row * G;
-      // the scale and bias of the next step are loaded one step ahead
-      uint32_t sv = active ? __ldg(sp) : 0u, bv = active ? __ldg(bp) : 0u;
-      for (int kb = 0; kb < G; ++kb) {
-        uint32_t sn = 0, bn = 0;
-        if (active && kb + 1 < G) {
-          sn = __ldg(sp + kb + 1);
-          bn = __ldg(bp + kb + 1);
+      const unsigned short* sp0 = reinterpret_cast<const unsigned short*>(a.q4.s[mat0]) + row0 * G;
+      const unsigned short* bp0 = reinterpret_cast<const unsigned short*>(a.q4.b[mat0]) + row0 * G;
+      const unsigned short* sp1 = reinterpret_cast<const unsigned short*>(a.q4.s[mat1]) + row1 * G;
+      const unsigned short* bp1 = reinterpret_cast<const unsigned short*>(a.q4.b[mat1]) + row1 * G;
+      // this group's steps of the unit: kb = kb0, kb0 + 2, ...; each step's scales and biases
+      // are loaded one step of the group ahead
+      int kb = (grp ^ n) & 1;
+      n += G;
+      uint32_t s0 = 0, b0 = 0, s1 = 0, b1 = 0;
+      if (kb < G) {
+        s0 = __ldg(sp0 + kb);
+        b0 = __ldg(bp0 + kb);
+        if (two) {
+          s1 = __ldg(sp1 + kb);
+          b1 = __ldg(bp1 + kb);
         }
-        // codes landed: convert into registers while the MMA may still read this A buffer
+      }
+      for (; kb < G; kb += 2) {
+        uint32_t ns0 = 0, nb0 = 0, ns1 = 0, nb1 = 0;
+        if (kb + 2 < G) {
+          ns0 = __ldg(sp0 + kb + 2);
+          nb0 = __ldg(bp0 + kb + 2);
+          if (two) {
+            ns1 = __ldg(sp1 + kb + 2);
+            nb1 = __ldg(bp1 + kb + 2);
+          }
+        }
         bool w = mbar_wait(&cfull[stage], ph, a.err);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        const uint8_t* cbase = smem + stage * kXStage + r * 32;
         uint32_t v[32];
-        if (active) {
-          const uint4* cp =
-              reinterpret_cast<const uint4*>(smem + stage * kXStage + mtile * kQTile + r * 32);
-          const uint4 c0 = cp[0], c1 = cp[1];
-          const uint32_t s2 = sv | (sv << 16), b2 = bv | (bv << 16);
-          dequant_q4x8(c0.x, s2, b2, v + 0);
-          dequant_q4x8(c0.y, s2, b2, v + 4);
-          dequant_q4x8(c0.z, s2, b2, v + 8);
-          dequant_q4x8(c0.w, s2, b2, v + 12);
-          dequant_q4x8(c1.x, s2, b2, v + 16);
-          dequant_q4x8(c1.y, s2, b2, v + 20);
-          dequant_q4x8(c1.z, s2, b2, v + 24);
-          dequant_q4x8(c1.w, s2, b2, v + 28);
-        }
-        // every warp waits on both barriers each step, active or not, to keep their phases
-        w = mbar_wait(&aempty[ab], aph ^ 1, a.err);
+        dequant_q4_row(reinterpret_cast<const uint4*>(cbase), s0, b0, v);
+        w = mbar_wait(&aempty[grp], aph ^ 1, a.err);  // the MMA has read this A buffer
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
-        if (active) {
-          tmem_st32(tmem + lane_off + abuf_col(ab) + 32u * mtile, v);
-          tmem_wait_st();
+        tmem_st32(tmem + lane_off + acol, v);
+        if (two) {
+          dequant_q4_row(reinterpret_cast<const uint4*>(cbase + kQTile), s1, b1, v);
+          tmem_st32(tmem + lane_off + acol + 32u, v);
         }
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[stage]);
-        sv = sn;
-        bv = bn;
-        if (++stage == kXStages) { stage = 0; ph ^= 1; }
-        ab ^= 1;
-        if (ab == 0) aph ^= 1;
+        stage += 2;
+        if (stage >= kXStages) { stage -= kXStages; ph ^= 1; }
+        aph ^= 1;
+        s0 = ns0;
+        b0 = nb0;
+        s1 = ns1;
+        b1 = nb1;
       }
     }
   }
