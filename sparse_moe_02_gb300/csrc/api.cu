@@ -351,7 +351,7 @@ int create_handle(const moe_config* cfg, const moe_weights* w, const moe_weights
 
   const Dims& D = h->D;
   bool ok = encode_2d(&h->tm_wr, h->w.w_router, D.d, kE, moe::kBK, kE) &&
-            encode_2d(&h->tm_h, h->h, D.hdim, h->P_chunk, moe::kBK, 16);
+            encode_2d(&h->tm_h, h->h, D.hdim, h->P_chunk, moe::kBK, moe::kHBoxRows);
   // the tensor-core path's maps of the experts: 4-bit code bytes, or bf16 tiles
   if (h->q4) {
     const moe::Q4Weights& q = h->wq;

@@ -21,6 +21,8 @@ namespace {
 
 constexpr int kTileA = kMTile * kBK * 2;     // 128 weight rows x 64 (16 KB)
 constexpr int kTileB = kChunkRows * kBK * 2; // up to 192 token rows x 64 (24 KB)
+static_assert((kChunkRows + kHBoxRows - 1) / kHBoxRows * kHBoxRows <= kChunkRows,
+              "the h boxes of a down unit fit its token-row tile");
 
 // ---------------------------------------------------------------- gate/up + down, one launch
 
@@ -308,7 +310,10 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
           const CUtensorMap* mw = shared ? &tm_wsd : &tm_wd;
           const int arow = (shared ? 0 : U.g * a.d) + U.mt * 2 * kMTile;
           const bool two = (U.mt * 2 + 1) * kMTile < a.d;
-          const uint32_t hbytes = (uint32_t)N * kBK * 2;
+          // h rows in boxes of kHBoxRows (<= 3 boxes: N <= 192); the rows of the last box past
+          // N land in B rows the MMA does not read (past the end of h the box is zero-filled)
+          const int nbox = (N + kHBoxRows - 1) / kHBoxRows;
+          const uint32_t hbytes = (uint32_t)nbox * kHBoxRows * kBK * 2;
           const uint32_t bytes = (Q4 ? 0 : (two ? 2 : 1) * kTileA) + hbytes;
           for (int kb = 0; kb < K / kBK; ++kb) {
             if (!mbar_wait(&empty[stage], ph ^ 1, a.err)) { ok = false; break; }
@@ -325,9 +330,9 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
               tma_load_2d(st, mw, &full[stage], kb * kBK, arow, pw);
               if (two) tma_load_2d(st + kTileA, mw, &full[stage], kb * kBK, arow + kMTile, pw);
             }
-            for (int r = 0; r < N / 16; ++r)
-              tma_load_2d(st + C::kBOff + r * 2048, &tm_h, &full[stage], kb * kBK,
-                          U.p0 + 16 * r, keep_h);
+            for (int r = 0; r < nbox; ++r)
+              tma_load_2d(st + C::kBOff + r * (kHBoxRows * kBK * 2), &tm_h, &full[stage],
+                          kb * kBK, U.p0 + kHBoxRows * r, keep_h);
             if (++stage == kXStages) { stage = 0; ph ^= 1; }
           }
         }

@@ -16,6 +16,7 @@ constexpr int kChunkRows = 192;    // most token rows in one grouped-GEMM work u
 constexpr int kRowAlign = 16;      // expert groups start on 16-row boundaries (MMA N step)
 constexpr int kMTile = 128;        // weight rows per work unit (MMA M)
 constexpr int kBK = 64;            // K elements per pipeline stage (one 128-byte swizzle row)
+constexpr int kHBoxRows = 64;      // h rows per TMA box of a down unit (rows past N unused)
 
 __host__ __device__ constexpr int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
