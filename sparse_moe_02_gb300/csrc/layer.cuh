@@ -90,6 +90,10 @@ cudaError_t launch_route_plan_scatter(int T, const Dims& D, const int32_t* topk_
 
 struct Q4Weights;
 
+// Copy of `bytes` (a multiple of 16; both pointers 16-byte aligned) from page-locked host memory
+// the device can address to device memory, by the SMs (at most 4 blocks per SM).
+cudaError_t launch_host_copy(const void* src, void* dst, size_t bytes, int sms, cudaStream_t s);
+
 // Both grouped GEMMs in one persistent launch: the gate/up units (SwiGLU epilogue, h [P][hdim]
 // bf16) and then the down units (ys [P][d] bf16), a down unit starting once every gate/up unit
 // of its chunk has published its h.  With q4 NULL the weight maps are bf16 maps (box 64 x

@@ -238,10 +238,24 @@ def test_deterministic_and_host_entry_point():
     y2 = bf16_bits(L.forward(x))
     assert np.array_equal(y1, y2)
     xh = x.cpu().pin_memory()
+    # pinned y: written in place by the layer's last kernel
     yh = torch.empty_like(xh).pin_memory()
     L.forward_host(xh, yh)
     torch.cuda.synchronize()
     assert np.array_equal(bf16_bits(yh), y1)
+    # pageable x and y, and pinned y that is not 16-byte aligned: copied by the copy engine
+    yp = torch.empty_like(xh)
+    L.forward_host(x.cpu(), yp)
+    buf = torch.zeros(xh.numel() * 2 + 16, dtype=torch.uint8).pin_memory()
+    yo = buf[2:2 + xh.numel() * 2].view(torch.bfloat16).view(xh.shape)
+    L.forward_host(xh, yo)
+    # batch-1 decode through the host entry point (the decode kernel writes y in place)
+    y1h = torch.empty_like(xh[:1]).pin_memory()
+    L.forward_host(xh[:1], y1h)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(yp), y1)
+    assert np.array_equal(bf16_bits(yo), y1)
+    assert np.array_equal(bf16_bits(y1h), bf16_bits(L.forward(x[:1])))
     assert L.device_error() == moe.MOE_OK
     # T = 0 is a no-op; T beyond max_tokens is rejected before any launch
     assert moe.moe_forward(L.handle, x.data_ptr(), 0, x.data_ptr(), None) == moe.MOE_OK
