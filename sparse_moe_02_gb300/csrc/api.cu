@@ -258,18 +258,33 @@ bool use_batch(const moe_handle_s* h, int T) {
   return h->cfg.schedule == MOE_SCHEDULE_GEMV && moe::decode_batch_fits(h->D, T);
 }
 
-// The routing chain of the tensor-core schedule.
+// Calls whose whole token count is this small take the matrix-vector router (a warp per
+// router row over every SM, selection in the last block) instead of the tensor-core router,
+// whose single 128-token block would stream the whole router matrix through four SMs.
+// Decided on the call's T, not a chunk's, so that chunked calls route like unchunked ones.
+bool small_router(const moe_handle_s* h, int T) {
+  return T <= moe::kGemvMaxTokens && moe::decode_batch_fits(h->D, T);
+}
+
+// The routing chain of the tensor-core schedule (small: see small_router).
 int run_route_gemm(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w,
-                   int32_t* offsets, int32_t* perm, cudaStream_t s, bool prof) {
-  CUtensorMap tm_x;  // the router loads x in tiles of 128 rows x 64
-  if (!encode_2d(&tm_x, x, h->D.d, T, moe::kBK, moe::kBlockTokens)) return MOE_ERR_CUDA;
+                   int32_t* offsets, int32_t* perm, cudaStream_t s, bool prof, bool small) {
   moe::RouteWs w = h->rws;
   if (offsets) w.offsets = offsets;
   int st;
   if (prof && (st = prof_mark(h, s, 0))) return st;
-  if ((st = cuda_status(moe::launch_router_topk(tm_x, h->tm_wr, h->w.router_bias, T, h->D,
-                                                topk_idx, topk_w, w, s))))
-    return st;
+  if (small) {
+    if ((st = cuda_status(moe::launch_decode_batch_router_shared(
+             static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, T, topk_idx, topk_w,
+             nullptr, nullptr, h->dws, s, false, w.hist))))
+      return st;
+  } else {
+    CUtensorMap tm_x;  // the router loads x in tiles of 128 rows x 64
+    if (!encode_2d(&tm_x, x, h->D.d, T, moe::kBK, moe::kBlockTokens)) return MOE_ERR_CUDA;
+    if ((st = cuda_status(moe::launch_router_topk(tm_x, h->tm_wr, h->w.router_bias, T, h->D,
+                                                  topk_idx, topk_w, w, s))))
+      return st;
+  }
   if (prof && (st = prof_mark(h, s, 1))) return st;
   return cuda_status(moe::launch_route_plan_scatter(T, h->D, topk_idx, perm, w, s));
 }
@@ -277,10 +292,10 @@ int run_route_gemm(moe_handle h, const void* x, int T, int32_t* topk_idx, float*
 // The tensor-core schedule over T <= Tc tokens: routing chain, grouped GEMMs, combine
 // (profiling marks 0..4 when prof).
 int forward_gemm(moe_handle h, const __nv_bfloat16* xd, int T, __nv_bfloat16* yd,
-                 cudaStream_t s, bool prof) {
+                 cudaStream_t s, bool prof, bool small) {
   int st;
   if ((st = run_route_gemm(h, xd, T, h->rws.topk_idx, h->rws.topk_w, nullptr, h->rws.perm, s,
-                           prof)))
+                           prof, small)))
     return st;
   if (prof && (st = prof_mark(h, s, 2))) return st;
   if ((st = cuda_status(moe::launch_experts(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu,
@@ -432,7 +447,7 @@ int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk
     return cuda_status(moe::launch_decode_batch_router_shared(
         static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, T, idx, wt,
         offsets ? offsets : h->rws.offsets, pm, h->dws, s, false));
-  return run_route_gemm(h, x, T, idx, wt, offsets, pm, s, false);
+  return run_route_gemm(h, x, T, idx, wt, offsets, pm, s, false, small_router(h, T));
 }
 
 int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
@@ -499,7 +514,7 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
   }
 
   if (T <= h->Tc) {
-    if ((st = forward_gemm(h, xd, T, yd, s, true))) return st;
+    if ((st = forward_gemm(h, xd, T, yd, s, true, small_router(h, T)))) return st;
     return prof_finish_call(h, s, 4);
   }
   // longer than a chunk: the layer over consecutive chunks of at most Tc tokens, in order on
@@ -508,7 +523,7 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
   for (int t0 = 0; t0 < T; t0 += h->Tc) {
     const int n = T - t0 < h->Tc ? T - t0 : h->Tc;
     const size_t off = (size_t)t0 * h->D.d;
-    if ((st = forward_gemm(h, xd + off, n, yd + off, s, false))) return st;
+    if ((st = forward_gemm(h, xd + off, n, yd + off, s, false, small_router(h, T)))) return st;
   }
   return prof_finish_call(h, s, 1);
 }

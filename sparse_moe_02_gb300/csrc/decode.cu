@@ -392,6 +392,7 @@ struct BatchRouterArgs {
   float* topk_w;
   DecodeWs dw;
   int router_blocks;
+  int32_t* hist;  // when set: assignments per expert (the one 128-token block of the plan)
 };
 
 // Blocks [0, router_blocks): one router row per warp for all T tokens; in a routing-only
@@ -474,6 +475,12 @@ __global__ void __launch_bounds__(kWarps * 32) dec_batch_router_shared_kernel(Ba
       int n = 0;
       for (int i = 0; i < T * kTopK; ++i) n += S.ids[i / kTopK][i % kTopK] < e2;
       a.offsets[e2] = n;
+    }
+  if (a.hist)
+    for (int e2 = threadIdx.x; e2 < kE; e2 += blockDim.x) {
+      int n = 0;
+      for (int i = 0; i < T * kTopK; ++i) n += S.ids[i / kTopK][i % kTopK] == e2;
+      a.hist[e2] = n;
     }
   if (threadIdx.x == 0) *a.dw.counter = 0;  // ready for the next launch on the stream
 }
@@ -698,8 +705,8 @@ cudaError_t launch_decode_batch_router_shared(const __nv_bfloat16* x, const Deco
                                               const Dims& D, int T, int32_t* topk_idx,
                                               float* topk_w, int32_t* offsets, int32_t* perm,
                                               const DecodeWs& dw, cudaStream_t s,
-                                              bool with_shared) {
-  BatchRouterArgs a{x, W, D, T, topk_idx, offsets, perm, topk_w, dw, kE / kWarps};
+                                              bool with_shared, int32_t* hist) {
+  BatchRouterArgs a{x, W, D, T, topk_idx, offsets, perm, topk_w, dw, kE / kWarps, hist};
   const int blocks = a.router_blocks + (with_shared ? (D.fs + kWarps - 1) / kWarps : 0);
   return launch_pdl(dec_batch_router_shared_kernel, dim3(blocks), dim3(kWarps * 32),
                     (size_t)T * D.d * 2, s, a);
