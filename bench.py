@@ -594,15 +594,18 @@ SMALL_BATCH_T = (2, 3, 4, 5)
 def run_small_batch(torch, moe, args, Ws, seed, P_hbm):
     """Decode of T = 2..5 tokens per layer (the speculative-verify shape) over the same 40
     layers' weights, one CUDA graph per T and schedule: us/layer through the matrix-vector
-    path over the union of the tokens' experts (schedule GEMV) and through the default
-    tensor-core path, and the HBM fraction of the bytes this routing needs (gate/up/down of
-    the union of the tokens' experts, router, shared expert, x and y) for the faster one."""
+    path over the union of the tokens' experts (schedule GEMV), through the tensor-core path
+    (schedule GEMM) and through the default (AUTO: one single-token pass per token at T = 2,
+    the tensor-core path above), and the HBM fraction of the bytes this routing needs
+    (gate/up/down of the union of the tokens' experts, router, shared expert, x and y) for the
+    fastest."""
     out = []
     for T in SMALL_BATCH_T:
         x = torch.from_numpy(synth.x_rows(seed, 0, T, D).view(np.int16)).cuda() \
             .view(torch.bfloat16)
         row = {"T": T}
-        for name, sched in (("gemv", moe.MOE_SCHEDULE_GEMV), ("tensor_core", moe.MOE_SCHEDULE_AUTO)):
+        for name, sched in (("gemv", moe.MOE_SCHEDULE_GEMV), ("tensor_core", moe.MOE_SCHEDULE_GEMM),
+                            ("auto", moe.MOE_SCHEDULE_AUTO)):
             layers = [moe.MoeLayer(W, T, schedule=sched) for W in Ws]
             ys = [torch.empty_like(x) for _ in layers]
             if name == "gemv":
@@ -634,7 +637,8 @@ def run_small_batch(torch, moe, args, Ws, seed, P_hbm):
             del g
         nbytes = (statistics.mean(union) * 3 * F * D * 2 + 3 * FS * D * 2 + E * D * 2
                   + 2 * T * D * 2)
-        best = min(row["gemv_us_per_layer"], row["tensor_core_us_per_layer"])
+        best = min(row["gemv_us_per_layer"], row["tensor_core_us_per_layer"],
+                   row["auto_us_per_layer"])
         row.update({"union_experts": statistics.mean(union), "bytes_per_layer": nbytes,
                     "hbm_frac": nbytes / (best * 1e-6) / 1e9 / P_hbm})
         out.append(row)

@@ -67,8 +67,8 @@ typedef enum {
   MOE_ERR_NO_MEMORY = 7    /* workspace allocation failed */
 } moe_status;
 
-/* Kernel schedule: AUTO uses the matrix-vector path when T == 1 and the tensor-core
- * grouped-GEMM path otherwise.  GEMM forces the tensor-core path.  GEMV forces the
+/* Kernel schedule: AUTO uses the matrix-vector path when T == 1 (with bf16 experts also when
+ * T == 2, once per token) and the tensor-core grouped-GEMM path otherwise.  GEMM forces the tensor-core path.  GEMV forces the
  * matrix-vector path: T == 1, or 2 <= T <= 8 when the shape fits (T * max(f, fs) <= 4096 and
  * T * d <= 65536), where every weight row of the union of the tokens' experts is read once
  * and applied to each token that chose it (§ "Limits of further optimization": verifying a
@@ -189,7 +189,8 @@ int moe_last_cuda_error(void);
  * profiling.  Kernel order -- tensor-core schedule (4): router_topk, route_plan_scatter (one
  * launch up to T = 16384; above, a plan launch and a scatter launch share this slot),
  * experts (gate/up and down), combine; matrix-vector schedule (3):
- * decode_router_shared, decode_gateup, decode_down_combine.  All recorded calls must use one
+ * decode_router_shared, decode_gateup, decode_down_combine (T == 2 under AUTO: those three for
+ * each token, 6).  All recorded calls must use one
  * schedule. */
 int moe_profile_begin(moe_handle h, int n_calls);
 int moe_profile_end(moe_handle h, float* ms, int capacity, int* n_kernels, int* n_calls);

@@ -251,9 +251,18 @@ bool use_gemv(const moe_handle_s* h, int T) {
   return T == 1 && h->cfg.schedule != MOE_SCHEDULE_GEMM;
 }
 
+// Two tokens under AUTO with bf16 experts: one single-token pass per token, measured faster on
+// GB300 than the grouped GEMM over both tokens or one pass over the union of their experts.
+// Each token's routing is bit-identical to moe_route's (the batch router accumulates each
+// token's logits in the single-token router's order and selects with the same routine).
+bool per_token(const moe_handle_s* h, int T) {
+  return T == 2 && h->cfg.schedule == MOE_SCHEDULE_AUTO && !h->q4;
+}
+
 // 2..8 tokens whose shapes fit, on request (schedule GEMV): the matrix-vector path over the
-// union of their experts.  AUTO keeps these T on the tensor-core path, measured faster on
-// GB300 at T = 2..5 (bench.py's small-batch lines time both).
+// union of their experts.  AUTO keeps T = 3..8 on the tensor-core path and runs T = 2 as one
+// single-token pass per token, both measured faster on GB300 (bench.py's small-batch lines
+// time all three).
 bool use_batch(const moe_handle_s* h, int T) {
   return h->cfg.schedule == MOE_SCHEDULE_GEMV && moe::decode_batch_fits(h->D, T);
 }
@@ -478,21 +487,26 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
     return prof_finish_call(h, s, 3);
   }
 
-  if (use_gemv(h, T)) {
+  if (use_gemv(h, T) || per_token(h, T)) {
     const moe::DecodeWeights W = decode_weights(h);
-    if ((st = prof_mark(h, s, 0))) return st;
-    // the router alone: the shared expert's gate/up runs in the gate/up launch
-    if ((st = cuda_status(moe::launch_decode_router_shared(xd, W, h->D, nullptr, nullptr,
-                                                           nullptr, nullptr, h->dws, h->rws.err,
-                                                           s, false))))
-      return st;
-    if ((st = prof_mark(h, s, 1))) return st;
-    if ((st = cuda_status(moe::launch_decode_gateup(xd, W, h->D, h->rws.topk_idx, h->rws.topk_w,
-                                                    h->dws, s))))
-      return st;
-    if ((st = prof_mark(h, s, 2))) return st;
-    if ((st = cuda_status(moe::launch_decode_down_combine(W, h->D, h->dws, yd, s)))) return st;
-    return prof_finish_call(h, s, 3);
+    for (int t = 0; t < T; ++t) {
+      const __nv_bfloat16* xt = xd + (size_t)t * h->D.d;
+      if ((st = prof_mark(h, s, 3 * t))) return st;
+      // the router alone: the shared expert's gate/up runs in the gate/up launch
+      if ((st = cuda_status(moe::launch_decode_router_shared(xt, W, h->D, nullptr, nullptr,
+                                                             nullptr, nullptr, h->dws,
+                                                             h->rws.err, s, false))))
+        return st;
+      if ((st = prof_mark(h, s, 3 * t + 1))) return st;
+      if ((st = cuda_status(moe::launch_decode_gateup(xt, W, h->D, h->rws.topk_idx,
+                                                      h->rws.topk_w, h->dws, s))))
+        return st;
+      if ((st = prof_mark(h, s, 3 * t + 2))) return st;
+      if ((st = cuda_status(moe::launch_decode_down_combine(W, h->D, h->dws,
+                                                            yd + (size_t)t * h->D.d, s))))
+        return st;
+    }
+    return prof_finish_call(h, s, 3 * T);
   }
 
   if (!h->q4 && use_batch(h, T)) {  // the small-batch matrix-vector path reads bf16

@@ -313,6 +313,28 @@ def test_small_batch_decode_shape(T):
     assert_close(got["y"], oracle_outputs(c), f"small batch decode T={T}")
 
 
+def test_two_tokens_run_once_per_token():
+    """AUTO runs two bf16 tokens as one single-token pass each: the outputs are those of two
+    single-token calls byte for byte, and moe_route's selection and weights for the pair
+    equal the single-token routes bit for bit."""
+    import torch
+    c = build_case("two-tokens", d=2048, f=512, fs=512, T=2, seed=8, full_host=False)
+    W, x = to_device(c)
+    L = moe.MoeLayer(W, 2)
+    y2 = bf16_bits(L.forward(x))
+    y0, y1 = bf16_bits(L.forward(x[:1])), bf16_bits(L.forward(x[1:2]))
+    r2, r0, r1 = L.route(x), L.route(x[:1]), L.route(x[1:2])
+    torch.cuda.synchronize()
+    assert L.device_error() == moe.MOE_OK
+    assert np.array_equal(y2, np.concatenate([y0, y1]))
+    for k in ("topk_idx", "topk_w"):
+        both = r2[k].cpu().numpy()
+        assert np.array_equal(both, np.concatenate([r0[k].cpu().numpy(), r1[k].cpu().numpy()]))
+    _check_routing(c, {k: v.cpu().numpy() for k, v in r2.items()})
+    assert_close(y2, oracle_outputs(c), "two tokens")
+    L.close()
+
+
 def test_read_probe_hook():
     import torch
     buf = torch.ones(1 << 20, dtype=torch.bfloat16, device="cuda")
