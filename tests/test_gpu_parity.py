@@ -133,6 +133,18 @@ def test_decode_other_shapes(d, f):
     assert_close(got["y"], oracle_outputs(c), f"decode d={d} f={f}")
 
 
+# The tensor-core path at the largest shapes the interface accepts (d = 8192 with f = 512;
+# d = 4096 with f = fs = 2048): 128-step K loops, 16 gate/up weight tiles per group; outputs
+# on a few sampled tokens (the oracle needs only their experts' weights).
+@pytest.mark.parametrize("d,f", [(8192, 512), (4096, 2048)])
+def test_prefill_largest_shapes(d, f):
+    c = build_case("prefill-large", d=d, f=f, fs=f, T=300, seed=12, full_host=False)
+    got = _run(c, moe.MOE_SCHEDULE_GEMM)
+    toks = [0, 1, 150, 298, 299]
+    _check_routing(c, got, toks)
+    assert_close(got["y"][toks], oracle_outputs(c, toks), f"prefill d={d} f={f}")
+
+
 # Batch-1 decode where the shared expert's inner dim differs from the routed one and d is not
 # a power of two (rows end in a partial 4 KB chunk, blocks get uneven shares).
 @pytest.mark.parametrize("d,f,fs", [(640, 128, 384), (2176, 384, 128)])

@@ -82,6 +82,18 @@ def test_q4_prefill_4096(skew):
     assert_close(got["y"][toks], oracle_outputs_q4(c, toks), f"q4 prefill 4096 skew={skew}")
 
 
+@pytest.mark.parametrize("d,f", [(8192, 512), (4096, 2048)])
+def test_q4_prefill_largest_shapes(d, f):
+    """The dequantizing grouped GEMM at the largest shapes the interface accepts; outputs on a
+    few sampled tokens."""
+    c = build_case("q4-prefill-large", d=d, f=f, fs=f, T=300, seed=13, full_host=False)
+    got = _run_q4(c)
+    toks = [0, 1, 150, 298, 299]
+    idx, _ = oracle.select(oracle.router_logits_f32(c.x[toks], c.w_r, c.bias), c.dims.k)
+    assert np.array_equal(got["topk_idx"][toks], idx)
+    assert_close(got["y"][toks], oracle_outputs_q4(c, toks), f"q4 prefill d={d} f={f}")
+
+
 def test_q4_chunked_and_single_token_tensor_core():
     """Chunking leaves the bytes unchanged; T = 1 under the GEMM schedule goes through the
     dequantizing grouped GEMM and matches the oracle."""
