@@ -90,6 +90,21 @@ __device__ __forceinline__ float row_dot_rest(RowFrag& r, const __nv_bfloat16* r
   return acc;
 }
 
+// Block-wide copy of n 16-byte words (read through L2) into shared memory, kDepth loads of a
+// thread in flight before its stores: one round trip per batch instead of one per word.
+template <int kDepth = 8>
+__device__ __forceinline__ void stage_u4(const uint4* src, uint4* dst, int n) {
+  for (int base = threadIdx.x; base < n; base += kDepth * blockDim.x) {
+    uint4 v[kDepth];
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i)
+      if (base + i * (int)blockDim.x < n) v[i] = __ldcg(src + base + i * blockDim.x);
+#pragma unroll
+    for (int i = 0; i < kDepth; ++i)
+      if (base + i * (int)blockDim.x < n) dst[base + i * blockDim.x] = v[i];
+  }
+}
+
 __device__ __forceinline__ void stage_x(const __nv_bfloat16* x, uint4* xs, int d) {
   const uint4* src = reinterpret_cast<const uint4*>(x);
   for (int i = threadIdx.x; i < d / 8; i += blockDim.x) xs[i] = src[i];
@@ -415,10 +430,7 @@ __global__ void __launch_bounds__(kWarps * 32) dec_batch_router_shared_kernel(Ba
   }
   pdl_wait();  // x may be written by the previous kernel
   pdl_trigger();
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    for (int i = threadIdx.x; i < T * nch; i += blockDim.x) xs[i] = __ldcg(src + i);
-  }
+  stage_u4(reinterpret_cast<const uint4*>(a.x), xs, T * nch);
   __syncthreads();
   if (!router) {
     if (c < a.D.fs) {
@@ -506,10 +518,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_gateup_kernel(BatchG
   pdl_wait();     // the router logits come from the previous kernel
   pdl_trigger();  // the down kernel may start selecting and streaming its rows now
   batch_select(a.dw.logits, T, S);
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    for (int i = threadIdx.x; i < T * nch; i += blockDim.x) xs[i] = __ldcg(src + i);
-  }
+  stage_u4(reinterpret_cast<const uint4*>(a.x), xs, T * nch);
   if (blockIdx.x == 0 && (int)threadIdx.x < T * kTopK) {
     a.topk_idx[threadIdx.x] = S.ids[threadIdx.x / kTopK][threadIdx.x % kTopK];
     a.topk_w[threadIdx.x] = S.w[threadIdx.x / kTopK][threadIdx.x % kTopK];
@@ -574,11 +583,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_down_combine_kernel(
   if (n < d) load_group(0, n);
   pdl_wait();  // h comes from the gate/up kernel
   pdl_trigger();
-  {
-    const float4* src = reinterpret_cast<const float4*>(a.dw.hdec);
-    float4* dst = reinterpret_cast<float4*>(hs);
-    for (int i = threadIdx.x; i < T * 9 * hdim / 4; i += blockDim.x) dst[i] = __ldcg(src + i);
-  }
+  // four deep: the rows prefetched before the wait are live in registers meanwhile
+  stage_u4<4>(reinterpret_cast<const uint4*>(a.dw.hdec), reinterpret_cast<uint4*>(hs),
+              T * 9 * hdim / 4);
   __syncthreads();
   for (; n < d; n += nwarps) {
     float acc[kGemvMaxTokens];

@@ -123,7 +123,27 @@ __device__ __forceinline__ float q4_dot_rest(Q4Frag& r, const Q4Row& row, const 
 // Stages v (n bf16 values, n a multiple of 32) as fp32, swizzled, in vf[n] and the sums of
 // each 32 (ascending) in vs[n / 32]; every thread of the block calls this (it holds barriers).
 __device__ __forceinline__ void stage_f32(const __nv_bfloat16* src, float* vf, float* vs, int n) {
-  for (int i = threadIdx.x; i < n; i += blockDim.x) vf[swz(i)] = __bfloat162float(src[i]);
+  // 8 elements per 16-byte load, up to four loads of a thread in flight before its stores (one
+  // round trip per batch); the swizzle moves groups of 4 whole, so each half of a load is one
+  // float4 store
+  const uint4* s16 = reinterpret_cast<const uint4*>(src);
+  const int n8 = n / 8;
+  for (int base = threadIdx.x; base < n8; base += 4 * blockDim.x) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (base + i * (int)blockDim.x < n8) v[i] = s16[base + i * blockDim.x];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = base + i * (int)blockDim.x;
+      if (m < n8) {
+        *reinterpret_cast<float4*>(vf + swz(8 * m)) =
+            make_float4(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y));
+        *reinterpret_cast<float4*>(vf + swz(8 * m + 4)) =
+            make_float4(bf16_lo(v[i].z), bf16_hi(v[i].z), bf16_lo(v[i].w), bf16_hi(v[i].w));
+      }
+    }
+  }
   __syncthreads();
   // a piece's 32 values are its 32 slots in some order: summed in slot order
   for (int p = threadIdx.x; p < n / 32; p += blockDim.x) {
@@ -333,11 +353,27 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
   if (n < d) load(0, n);
   pdl_wait();  // h comes from the gate/up kernel
   pdl_trigger();
-  // each row h_j swizzled on its own (pieces counted from the row's start): all loads in
-  // flight at once, then the sums per 32 from shared memory
-  for (int j = 0; j < 9; ++j)
-    for (int c = threadIdx.x; c < hdim; c += blockDim.x)
-      hf[j * hdim + swz(c)] = __ldcg(a.dw.hdec + (size_t)j * hdim + c);
+  // each row h_j swizzled on its own (pieces counted from the row's start), in float4 groups,
+  // which the swizzle moves whole: eight 16-byte loads of a thread in flight before its stores
+  // (one round trip per batch), then the sums per 32 from shared memory
+  {
+    const float4* src = reinterpret_cast<const float4*>(a.dw.hdec);
+    const int r4 = hdim / 4, n4 = 9 * r4;
+    for (int base = threadIdx.x; base < n4; base += 8 * blockDim.x) {
+      float4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (base + i * (int)blockDim.x < n4) v[i] = __ldcg(src + base + i * blockDim.x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = base + i * (int)blockDim.x;
+        if (q < n4) {
+          const int j = q / r4, c = (q - j * r4) * 4;
+          *reinterpret_cast<float4*>(hf + j * hdim + swz(c)) = v[i];
+        }
+      }
+    }
+  }
   __syncthreads();
   // a piece's 32 values are its 32 slots in some order: summed in slot order
   for (int q = threadIdx.x; q < 9 * (hdim / 32); q += blockDim.x) {
