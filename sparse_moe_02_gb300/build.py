@@ -11,7 +11,7 @@ OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 SOURCES = ["api.cu", "route.cu", "experts.cu", "decode.cu", "decode_q4.cu", "noalloc.cu", "probe.cu",
            "hostio.cu"]
-HEADERS = ["layer.cuh", "ptx.cuh", "select.cuh"]
+HEADERS = ["layer.cuh", "plan.cuh", "ptx.cuh", "select.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + CSRC,
          "-I" + os.path.join(ROOT, "include")]

@@ -283,10 +283,13 @@ int run_route_gemm(moe_handle h, const void* x, int T, int32_t* topk_idx, float*
   int st;
   if (prof && (st = prof_mark(h, s, 0))) return st;
   if (small) {
+    // routing and the plan in one launch (the plan's profiling slot stays empty)
     if ((st = cuda_status(moe::launch_decode_batch_router_shared(
              static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, T, topk_idx, topk_w,
-             nullptr, nullptr, h->dws, s, false, w.hist))))
+             nullptr, perm, h->dws, s, false, &w))))
       return st;
+    if (prof && (st = prof_mark(h, s, 1))) return st;
+    return MOE_OK;
   } else {
     CUtensorMap tm_x;  // the router loads x in tiles of 128 rows x 64
     if (!encode_2d(&tm_x, x, h->D.d, T, moe::kBK, moe::kBlockTokens)) return MOE_ERR_CUDA;

@@ -14,6 +14,7 @@
 #include <algorithm>
 
 #include "layer.cuh"
+#include "plan.cuh"
 #include "ptx.cuh"
 #include "select.cuh"
 
@@ -407,7 +408,9 @@ struct BatchRouterArgs {
   float* topk_w;
   DecodeWs dw;
   int router_blocks;
-  int32_t* hist;  // when set: assignments per expert (the one 128-token block of the plan)
+  bool plan;      // routing for the tensor-core schedule: the last block also builds the plan
+  PlanArgs pa;    // (offsets, group starts, unit lists) in rws and scatters the tokens,
+  RouteWs rws;    // perm included, so that no separate plan launch follows
 };
 
 // Blocks [0, router_blocks): one router row per warp for all T tokens; in a routing-only
@@ -469,6 +472,29 @@ __global__ void __launch_bounds__(kWarps * 32) dec_batch_router_shared_kernel(Ba
   if (!s_last) return;
   __threadfence();
   batch_select(a.dw.logits, T, S);
+  if (a.plan) {
+    // the plan of the tensor-core schedule (one token block): per-expert counts, groups,
+    // unit lists, and the scatter of the T tokens (it reads topk_idx as written here)
+    __shared__ GroupTable G;
+    __shared__ int s_pre[kE];
+    __shared__ uint32_t mask[4][kE];
+    if ((int)threadIdx.x < T * kTopK) {
+      const int t = threadIdx.x / kTopK, j = threadIdx.x % kTopK;
+      a.topk_idx[t * kTopK + j] = S.ids[t][j];
+      a.topk_w[t * kTopK + j] = S.w[t][j];
+    }
+    for (int i = threadIdx.x; i < 4 * kE; i += blockDim.x) (&mask[0][0])[i] = 0u;
+    const int e2 = threadIdx.x;  // 256 threads: one per expert
+    int cnt = 0;
+    for (int i = 0; i < T * kTopK; ++i) cnt += S.ids[i / kTopK][i % kTopK] == e2;
+    s_pre[e2] = 0;
+    plan_groups(a.pa, cnt, G, a.rws, true);  // ends with a barrier
+    plan_units(G, a.rws.units_gu, false, 0, G.n_gu, T);
+    plan_units(G, a.rws.units_dn, true, 0, G.n_dn, T);
+    scatter_block(0, T, a.topk_idx, a.perm, a.rws, mask, s_pre, G.off, G.poff, G.p_shared);
+    if (threadIdx.x == 0) *a.dw.counter = 0;  // ready for the next launch on the stream
+    return;
+  }
   if ((int)threadIdx.x < T * kTopK) {
     const int t = threadIdx.x / kTopK, j = threadIdx.x % kTopK, id = S.ids[t][j];
     a.topk_idx[t * kTopK + j] = id;
@@ -488,12 +514,7 @@ __global__ void __launch_bounds__(kWarps * 32) dec_batch_router_shared_kernel(Ba
       for (int i = 0; i < T * kTopK; ++i) n += S.ids[i / kTopK][i % kTopK] < e2;
       a.offsets[e2] = n;
     }
-  if (a.hist)
-    for (int e2 = threadIdx.x; e2 < kE; e2 += blockDim.x) {
-      int n = 0;
-      for (int i = 0; i < T * kTopK; ++i) n += S.ids[i / kTopK][i % kTopK] == e2;
-      a.hist[e2] = n;
-    }
+
   if (threadIdx.x == 0) *a.dw.counter = 0;  // ready for the next launch on the stream
 }
 
@@ -712,8 +733,9 @@ cudaError_t launch_decode_batch_router_shared(const __nv_bfloat16* x, const Deco
                                               const Dims& D, int T, int32_t* topk_idx,
                                               float* topk_w, int32_t* offsets, int32_t* perm,
                                               const DecodeWs& dw, cudaStream_t s,
-                                              bool with_shared, int32_t* hist) {
-  BatchRouterArgs a{x, W, D, T, topk_idx, offsets, perm, topk_w, dw, kE / kWarps, hist};
+                                              bool with_shared, const RouteWs* plan) {
+  BatchRouterArgs a{x, W, D, T, topk_idx, offsets, perm, topk_w, dw, kE / kWarps, plan != nullptr,
+                    plan_args(T, D), plan ? *plan : RouteWs{}};
   const int blocks = a.router_blocks + (with_shared ? (D.fs + kWarps - 1) / kWarps : 0);
   return launch_pdl(dec_batch_router_shared_kernel, dim3(blocks), dim3(kWarps * 32),
                     (size_t)T * D.d * 2, s, a);

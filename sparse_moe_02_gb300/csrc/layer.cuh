@@ -177,15 +177,17 @@ cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D, co
 // Small-batch decode of T = 2..kGemvMaxTokens tokens (decode_batch_fits): the same three
 // launches as the single-token path, over the union of the tokens' experts (each weight row
 // read once, applied to every token that chose it).  With topk_idx not NULL the router launch
-// is routing only (its last block writes topk_idx, topk_w and, where not NULL, offsets, perm
-// and hist, the assignments per expert as the plan of the tensor-core path reads them).
+// is routing only (its last block writes topk_idx, topk_w and, where not NULL, offsets and
+// perm); with plan not NULL it is the routing of the tensor-core schedule for T <= 128: the
+// last block also writes the plan (offsets, group starts, unit lists, chunk counters) into
+// *plan and scatters the tokens (perm, the padded rows), so no plan launch follows.
 bool decode_batch_fits(const Dims& D, int T);
 cudaError_t prepare_decode_batch_kernels();
 cudaError_t launch_decode_batch_router_shared(const __nv_bfloat16* x, const DecodeWeights& W,
                                               const Dims& D, int T, int32_t* topk_idx,
                                               float* topk_w, int32_t* offsets, int32_t* perm,
                                               const DecodeWs& dw, cudaStream_t s,
-                                              bool with_shared, int32_t* hist = nullptr);
+                                              bool with_shared, const RouteWs* plan = nullptr);
 cudaError_t launch_decode_batch_gateup(const __nv_bfloat16* x, const DecodeWeights& W,
                                        const Dims& D, int T, int32_t* topk_idx, float* topk_w,
                                        const DecodeWs& dw, int sms, cudaStream_t s);
