@@ -105,9 +105,14 @@ def test_q4_chunked_and_single_token_tensor_core():
     L0 = moe.MoeLayer(W, T)
     L1 = moe.MoeLayer(W, T, chunk_tokens=256)
     y0, y1 = bf16_bits(L0.forward(x)), bf16_bits(L1.forward(x))
+    # the host entry point over chunks (page-locked buffers: y written in place)
+    xh = x.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    L1.forward_host(xh, yh)
     torch.cuda.synchronize()
     assert L0.device_error() == moe.MOE_OK and L1.device_error() == moe.MOE_OK
     assert np.array_equal(y0, y1)
+    assert np.array_equal(bf16_bits(yh), y1)
     toks = sample_tokens(T, n_edge=16, stride=29)
     assert_close(y1[toks], oracle_outputs_q4(c, toks), "q4 chunked")
     L0.close()
