@@ -562,7 +562,7 @@ def run_decode_q4(torch, moe, args, seed, P_hbm):
     return {"us_per_layer": us, "GB_per_s": gbs, "bytes_per_layer": DECODE_Q4_BYTES_PER_LAYER,
             "hbm_frac": gbs / P_hbm, "layers": len(layers),
             "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in
-                                zip(("q4_router_shared", "q4_gateup", "q4_down_combine"), kms)},
+                                zip(("router", "q4_gateup", "q4_down_combine"), kms)},
             "weights": "4-bit codes, group 64, bf16 scale and bias; router bf16"}
 
 

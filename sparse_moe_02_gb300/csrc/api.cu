@@ -477,7 +477,11 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
 
   if (h->q4 && use_gemv(h, T)) {  // 4-bit experts, batch-1 decode
     if ((st = prof_mark(h, s, 0))) return st;
-    if ((st = cuda_status(moe::launch_decode_q4_router_shared(xd, h->wq, h->D, h->dws, s))))
+    // the router is bf16 on 4-bit handles too: the bf16 path's router launch, so that the
+    // routing equals moe_route's bit for bit
+    if ((st = cuda_status(moe::launch_decode_router_shared(xd, decode_weights(h), h->D, nullptr,
+                                                           nullptr, nullptr, nullptr, h->dws,
+                                                           h->rws.err, s, false))))
       return st;
     if ((st = prof_mark(h, s, 1))) return st;
     if ((st = cuda_status(moe::launch_decode_q4_gateup(xd, h->wq, h->D, h->rws.topk_idx,

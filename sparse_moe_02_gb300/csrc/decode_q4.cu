@@ -162,75 +162,6 @@ __device__ __forceinline__ void stage_f32(const __nv_bfloat16* src, float* vf, f
   __syncthreads();
 }
 
-// 8 bf16 weights times elements 8 cc .. 8 cc + 7 of the swizzled vector v (router rows).
-__device__ __forceinline__ float dot8_bf16_f32(uint4 w, const float* v, int cc) {
-  const float4 a = piece_f4(v, cc >> 2, 2 * (cc & 3));
-  const float4 b = piece_f4(v, cc >> 2, 2 * (cc & 3) + 1);
-  float s = 0.f;
-  s = fmaf(bf16_lo(w.x), a.x, s);
-  s = fmaf(bf16_hi(w.x), a.y, s);
-  s = fmaf(bf16_lo(w.y), a.z, s);
-  s = fmaf(bf16_hi(w.y), a.w, s);
-  s = fmaf(bf16_lo(w.z), b.x, s);
-  s = fmaf(bf16_hi(w.z), b.y, s);
-  s = fmaf(bf16_lo(w.w), b.z, s);
-  return fmaf(bf16_hi(w.w), b.w, s);
-}
-
-constexpr int kRPre = 8;  // 16-byte pieces per lane of a bf16 router row held in registers
-
-struct Q4RouterSharedArgs {
-  const __nv_bfloat16* x;
-  Q4Weights W;
-  Dims D;
-  DecodeWs dw;
-};
-
-// Blocks [0, E / kQWarps): one bf16 router row per warp -> logits; blocks after: one
-// shared-expert feature per warp (its 4-bit gate and up rows) -> h_s.  Weight rows are
-// requested before waiting on the previous kernel (they do not depend on it).
-__global__ void __launch_bounds__(kQWarps * 32) dec_q4_router_shared_kernel(Q4RouterSharedArgs a) {
-  extern __shared__ float qsm[];  // x as fp32 [d], then its sums per 32 [d / 32]
-  float* xf = qsm;
-  float* xs = qsm + a.D.d;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = a.D.d, nch = d / 8, np = d / 32;
-  const int router_blocks = kE / kQWarps;
-  const bool router = (int)blockIdx.x < router_blocks;
-  const int e = blockIdx.x * kQWarps + warp;
-  const int c = ((int)blockIdx.x - router_blocks) * kQWarps + warp;  // shared feature
-  const __nv_bfloat16* rrow = a.W.w_r + (size_t)e * d;
-  uint4 rr[kRPre];
-  Q4Frag g, u;
-  if (router) {
-#pragma unroll
-    for (int i = 0; i < kRPre; ++i)
-      if (lane + 32 * i < nch) rr[i] = ld_stream_u4(rrow + (size_t)(lane + 32 * i) * 8);
-  } else if (c < a.D.fs) {
-    q4_load(g, a.W.s_gate.row(c, d), np, lane, 0);
-    q4_load(u, a.W.s_up.row(c, d), np, lane, 0);
-  }
-  pdl_wait();  // x may be written by the previous kernel
-  pdl_trigger();
-  stage_f32(a.x, xf, xs, d);
-  if (router) {
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < kRPre; ++i) {
-      const int cc = lane + 32 * i;
-      if (cc < nch) acc += dot8_bf16_f32(rr[i], xf, cc);
-    }
-    for (int cc = lane + 32 * kRPre; cc < nch; cc += 32)
-      acc += dot8_bf16_f32(ld_stream_u4(rrow + (size_t)cc * 8), xf, cc);
-    acc = warp_sum_q(acc);
-    if (lane == 0) a.dw.logits[e] = acc + (a.W.bias ? a.W.bias[e] : 0.f);
-  } else if (c < a.D.fs) {
-    const float gv = warp_sum_q(q4_dot_rest(g, a.W.s_gate.row(c, d), xf, xs, np, lane));
-    const float uv = warp_sum_q(q4_dot_rest(u, a.W.s_up.row(c, d), xf, xs, np, lane));
-    if (lane == 0) a.dw.hdec[(size_t)8 * a.D.hdim + c] = silu_mul(gv, uv);
-  }
-}
-
 struct Q4GateUpArgs {
   const __nv_bfloat16* x;
   Q4Weights W;
@@ -420,24 +351,13 @@ __global__ void __launch_bounds__(kQWarps * 32, 2) dec_q4_down_combine_kernel(Q4
 
 cudaError_t prepare_decode_q4_kernels() {
   // dynamic shared memory at the largest supported shape (d = 8192, hdim = 2048)
-  cudaError_t e = cudaFuncSetAttribute(dec_q4_router_shared_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       8192 * 4 + 256 * 4);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   if ((e = cudaFuncSetAttribute(dec_q4_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 8192 * 4 + 256 * 4)) != cudaSuccess)
     return e;
   return cudaFuncSetAttribute(dec_q4_down_combine_kernel,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               9 * 2048 * 4 + 9 * 64 * 4);
-}
-
-cudaError_t launch_decode_q4_router_shared(const __nv_bfloat16* x, const Q4Weights& W,
-                                           const Dims& D, const DecodeWs& dw, cudaStream_t s) {
-  Q4RouterSharedArgs a{x, W, D, dw};
-  const int blocks = kE / kQWarps;  // router rows only: the shared gate/up is in the next launch
-  return launch_pdl(dec_q4_router_shared_kernel, dim3(blocks), dim3(kQWarps * 32),
-                    (size_t)D.d * 4 + (size_t)D.d / 32 * 4, s, a);
 }
 
 cudaError_t launch_decode_q4_gateup(const __nv_bfloat16* x, const Q4Weights& W, const Dims& D,

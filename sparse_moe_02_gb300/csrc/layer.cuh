@@ -195,11 +195,10 @@ cudaError_t launch_decode_batch_down_combine(const DecodeWeights& W, const Dims&
                                              const DecodeWs& dw, __nv_bfloat16* y, int sms,
                                              cudaStream_t s);
 
-// Batch-1 decode with 4-bit experts: router + shared gate/up, the 8 selected experts' gate/up,
-// down rows weighted and combined in fixed order (three launches, as the bf16 path).
+// Batch-1 decode with 4-bit experts: the router launch of the bf16 path (the router stays
+// bf16), then the shared expert's and the 8 selected experts' 4-bit gate/up, and the down rows
+// weighted and combined in fixed order.
 cudaError_t prepare_decode_q4_kernels();
-cudaError_t launch_decode_q4_router_shared(const __nv_bfloat16* x, const Q4Weights& W,
-                                           const Dims& D, const DecodeWs& dw, cudaStream_t s);
 cudaError_t launch_decode_q4_gateup(const __nv_bfloat16* x, const Q4Weights& W, const Dims& D,
                                     int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
                                     int sms, cudaStream_t s);
