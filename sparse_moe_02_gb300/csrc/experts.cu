@@ -447,33 +447,39 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
     const uint64_t pol_keep = policy_evict_last();  // ys: read back soon by the combine
     uint32_t tph[2] = {0, 0};
     bool ok = true;
+    // the unit's accumulators are released as soon as this warp's last TMEM read of them has
+    // completed, so that the next unit's MMAs overlap the last chunk's arithmetic and stores
+    auto release = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tempty[0]);
+        mbar_arrive(&tempty[1]);
+      }
+    };
     for (int k = 0; ok; ++k) {
       const int i = next_unit(k, ok);
       if (i < 0) break;
       const XUnit X = unit_at(a, i, n_gu);
       const Unit& U = X.u;
       const int N = round_up(U.nrows, kRowAlign);
+      const bool w0 = mbar_wait(&tfull[0], tph[0], a.err);
+      const bool w1 = mbar_wait(&tfull[1], tph[1], a.err);
+      if (!__all_sync(0xffffffffu, w0 && w1)) break;
+      tc_fence_after();
+      if (half * 16 >= N) release();  // no columns for this warp in this unit
       if (!X.down) {
-        const bool w0 = mbar_wait(&tfull[0], tph[0], a.err);
-        const bool w1 = mbar_wait(&tfull[1], tph[1], a.err);
-        if (!__all_sync(0xffffffffu, w0 && w1)) break;
-        tc_fence_after();
         __nv_bfloat16* hp = a.h + (size_t)U.p0 * a.hdim + U.mt * kMTile + m;
         for (int j0 = half * 16; j0 < N; j0 += 32) {
           uint32_t g[16], v[16];
           tmem_ld16(tmem + lane_off + (uint32_t)j0, g);
           tmem_ld16(tmem + lane_off + 256u + (uint32_t)j0, v);
           tmem_wait_ld();
+          if (j0 + 32 >= N) release();
 #pragma unroll
           for (int r = 0; r < 16; ++r)
             hp[(size_t)(j0 + r) * a.hdim] =
                 __float2bfloat16_rn(silu_mul(__uint_as_float(g[r]), __uint_as_float(v[r])));
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&tempty[0]);
-          mbar_arrive(&tempty[1]);
         }
         tph[0] ^= 1;
         tph[1] ^= 1;
@@ -484,10 +490,6 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
           atomicAdd(a.chunk_done + U.cid, 1);
         }
       } else {
-        const bool w0 = mbar_wait(&tfull[0], tph[0], a.err);
-        const bool w1 = mbar_wait(&tfull[1], tph[1], a.err);
-        if (!__all_sync(0xffffffffu, w0 && w1)) break;
-        tc_fence_after();
         const bool two = (U.mt * 2 + 1) * kMTile < a.d;
         __nv_bfloat16* yp = a.ys + (size_t)U.p0 * a.d + U.mt * 2 * kMTile + m;
         for (int j0 = half * 16; j0 < N; j0 += 32) {
@@ -495,6 +497,7 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
           tmem_ld16(tmem + lane_off + (uint32_t)j0, r0);
           if (two) tmem_ld16(tmem + lane_off + 256u + (uint32_t)j0, r1);
           tmem_wait_ld();
+          if (j0 + 32 >= N) release();
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             st_b16_hint(yp + (size_t)(j0 + c) * a.d, __float2bfloat16_rn(__uint_as_float(r0[c])),
@@ -503,12 +506,6 @@ __global__ void __launch_bounds__(XCfg<Q4>::kThreads, 1)
               st_b16_hint(yp + (size_t)(j0 + c) * a.d + kMTile,
                           __float2bfloat16_rn(__uint_as_float(r1[c])), pol_keep);
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&tempty[0]);
-          mbar_arrive(&tempty[1]);
         }
         tph[0] ^= 1;
         tph[1] ^= 1;
