@@ -13,6 +13,8 @@
 // summed in fixed order per output.
 #include <algorithm>
 
+#include <type_traits>
+
 #include "layer.cuh"
 #include "plan.cuh"
 #include "ptx.cuh"
@@ -347,13 +349,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_down_combine_kernel(DownAr
 // Lane-partial dot products of one d-element row with the x rows of the tokens in `mask`
 // (bit t: token t, at xs + t * nch), kPre*32 pieces at a time; the first such piece group is
 // already in r.  mask is the same in every lane.
+template <int NT>
 __device__ __forceinline__ void row_dot_tokens(RowFrag& r, const __nv_bfloat16* row,
                                                const uint4* xs, int nch, int mask, int lane,
-                                               float (&acc)[kGemvMaxTokens]) {
+                                               float (&acc)[NT]) {
   for (int base = 0; base < nch; base += kPre * 32) {
     if (base) row_load(r, row, nch, lane, base);
 #pragma unroll
-    for (int t = 0; t < kGemvMaxTokens; ++t)
+    for (int t = 0; t < NT; ++t)
       if ((mask >> t) & 1) acc[t] += row_dot(r, xs + (size_t)t * nch, nch, lane, base);
   }
 }
@@ -531,11 +534,15 @@ struct BatchGateUpArgs {
 // Items (union expert k, feature c), one warp per item over a resident grid: the gate and up
 // rows are read once; h[t][slot][c] = silu(gate . x_t) * (up . x_t) for every token t that
 // chose the expert.
+// Instantiated per token count TT (= a.T): the per-token loops unroll TT times, so a small
+// batch runs a small body (unrolled for the largest batch, the code missed in the instruction
+// cache).
+template <int TT>
 __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_gateup_kernel(BatchGateUpArgs a) {
   extern __shared__ uint4 xs[];  // [T][d/8]
   __shared__ BatchSel S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = a.D.d, f = a.D.f, nch = d / 8, T = a.T;
+  const int d = a.D.d, f = a.D.f, nch = d / 8, T = TT;
   pdl_wait();     // the router logits come from the previous kernel
   pdl_trigger();  // the down kernel may start selecting and streaming its rows now
   batch_select(a.dw.logits, T, S);
@@ -552,14 +559,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_gateup_kernel(BatchG
     RowFrag rg, ru;
     row_load(rg, a.W.w_gate + row, nch, lane, 0);
     row_load(ru, a.W.w_up + row, nch, lane, 0);
-    float g[kGemvMaxTokens], u[kGemvMaxTokens];
+    float g[TT], u[TT];
 #pragma unroll
-    for (int t = 0; t < kGemvMaxTokens; ++t) g[t] = u[t] = 0.f;
+    for (int t = 0; t < TT; ++t) g[t] = u[t] = 0.f;
     row_dot_tokens(rg, a.W.w_gate + row, xs, nch, mask, lane, g);
     row_dot_tokens(ru, a.W.w_up + row, xs, nch, mask, lane, u);
 #pragma unroll
-    for (int t = 0; t < kGemvMaxTokens; ++t)
-      if (t < T && ((mask >> t) & 1)) {
+    for (int t = 0; t < TT; ++t)
+      if ((mask >> t) & 1) {
         const float gv = warp_sum(g[t]), uv = warp_sum(u[t]);
         if (lane == 0)
           a.dw.hdec[((size_t)t * 9 + batch_slot(S, t, e)) * a.D.hdim + c] = silu_mul(gv, uv);
@@ -581,11 +588,12 @@ constexpr int kBatchRows = 8;  // union experts whose down rows one warp has in 
 // time (the first eight requested before waiting for h), each applied to the tokens that
 // chose it; per lane and token the terms w_tj (down_e[n] . h_tj) add in ascending expert id,
 // then the shared expert's; one warp reduction per token gives y[t][n].
+template <int TT>
 __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_down_combine_kernel(BatchDownArgs a) {
   extern __shared__ float hs[];  // [T][9][hdim]
   __shared__ BatchSel S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = a.D.d, f = a.D.f, fs = a.D.fs, hdim = a.D.hdim, T = a.T;
+  const int d = a.D.d, f = a.D.f, fs = a.D.fs, hdim = a.D.hdim, T = TT;
   const int nc = f / 8;
   batch_select(a.dw.logits, T, S);  // final: the router finished before this launch started
   const int nwarps = gridDim.x * kWarps;
@@ -609,9 +617,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_down_combine_kernel(
               T * 9 * hdim / 4);
   __syncthreads();
   for (; n < d; n += nwarps) {
-    float acc[kGemvMaxTokens];
+    float acc[TT];
 #pragma unroll
-    for (int t = 0; t < kGemvMaxTokens; ++t) acc[t] = 0.f;
+    for (int t = 0; t < TT; ++t) acc[t] = 0.f;
     for (int k0 = 0; k0 < S.nu; k0 += kBatchRows) {
       if (k0) load_group(k0, n);
 #pragma unroll
@@ -620,7 +628,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_down_combine_kernel(
         const int e = S.ulist[k0 + q], mask = S.tmask[e];
         const __nv_bfloat16* row = a.W.w_down + ((size_t)e * d + n) * f;
 #pragma unroll
-        for (int t = 0; t < kGemvMaxTokens; ++t)
+        for (int t = 0; t < TT; ++t)
           if (t < T && ((mask >> t) & 1)) {
             const int j = batch_slot(S, t, e);
             const float* ht = hs + ((size_t)t * 9 + j) * hdim;
@@ -641,11 +649,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_down_combine_kernel(
     for (int cc = lane; cc < fs / 8; cc += 32) {
       const uint4 wv = ld_stream_u4(srow + (size_t)cc * 8);
 #pragma unroll
-      for (int t = 0; t < kGemvMaxTokens; ++t)
+      for (int t = 0; t < TT; ++t)
         if (t < T) acc[t] += dot8_f32(wv, hs + ((size_t)t * 9 + 8) * hdim + cc * 8);
     }
 #pragma unroll
-    for (int t = 0; t < kGemvMaxTokens; ++t)
+    for (int t = 0; t < TT; ++t)
       if (t < T) {
         const float v = warp_sum(acc[t]);
         if (lane == 0) a.y[(size_t)t * d + n] = __float2bfloat16_rn(v);
@@ -716,17 +724,44 @@ bool decode_batch_fits(const Dims& D, int T) {
          T * D.d <= kBatchMaxTD;
 }
 
+namespace {
+// Calls f(std::integral_constant<int, T>{}) for T = 1..kGemvMaxTokens (the token count of a
+// small batch as a compile-time constant); other T: invalid value.
+template <class F>
+cudaError_t batch_dispatch(int T, F&& f) {
+  switch (T) {
+    case 1: return f(std::integral_constant<int, 1>{});
+    case 2: return f(std::integral_constant<int, 2>{});
+    case 3: return f(std::integral_constant<int, 3>{});
+    case 4: return f(std::integral_constant<int, 4>{});
+    case 5: return f(std::integral_constant<int, 5>{});
+    case 6: return f(std::integral_constant<int, 6>{});
+    case 7: return f(std::integral_constant<int, 7>{});
+    case 8: return f(std::integral_constant<int, 8>{});
+    default: return cudaErrorInvalidValue;
+  }
+}
+static_assert(kGemvMaxTokens == 8, "batch_dispatch covers 1..kGemvMaxTokens");
+}  // namespace
+
 cudaError_t prepare_decode_batch_kernels() {
   cudaError_t e;
   const int xs = kBatchMaxTD * 2, hs = kBatchMaxTHdim * 9 * 4;
   if ((e = cudaFuncSetAttribute(dec_batch_router_shared_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, xs)) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(dec_batch_gateup_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, xs)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(dec_batch_down_combine_kernel,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, hs);
+  for (int T = 1; T <= kGemvMaxTokens; ++T) {
+    e = batch_dispatch(T, [&](auto tt) {
+      constexpr int TT = decltype(tt)::value;
+      cudaError_t r = cudaFuncSetAttribute(dec_batch_gateup_kernel<TT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, xs);
+      if (r != cudaSuccess) return r;
+      return cudaFuncSetAttribute(dec_batch_down_combine_kernel<TT>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, hs);
+    });
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode_batch_router_shared(const __nv_bfloat16* x, const DecodeWeights& W,
@@ -745,8 +780,10 @@ cudaError_t launch_decode_batch_gateup(const __nv_bfloat16* x, const DecodeWeigh
                                        const Dims& D, int T, int32_t* topk_idx, float* topk_w,
                                        const DecodeWs& dw, int sms, cudaStream_t s) {
   BatchGateUpArgs a{x, W, D, T, topk_idx, topk_w, dw};
-  return launch_pdl(dec_batch_gateup_kernel, dim3(2 * sms), dim3(kWarps * 32),
-                    (size_t)T * D.d * 2, s, a);
+  return batch_dispatch(T, [&](auto tt) {
+    return launch_pdl(dec_batch_gateup_kernel<decltype(tt)::value>, dim3(2 * sms),
+                      dim3(kWarps * 32), (size_t)T * D.d * 2, s, a);
+  });
 }
 
 cudaError_t launch_decode_batch_down_combine(const DecodeWeights& W, const Dims& D, int T,
@@ -754,8 +791,10 @@ cudaError_t launch_decode_batch_down_combine(const DecodeWeights& W, const Dims&
                                              cudaStream_t s) {
   BatchDownArgs a{W, D, T, dw, y};
   const int grid = std::min(2 * sms, (D.d + kWarps - 1) / kWarps);
-  return launch_pdl(dec_batch_down_combine_kernel, dim3(grid), dim3(kWarps * 32),
-                    (size_t)T * 9 * D.hdim * sizeof(float), s, a);
+  return batch_dispatch(T, [&](auto tt) {
+    return launch_pdl(dec_batch_down_combine_kernel<decltype(tt)::value>, dim3(grid),
+                      dim3(kWarps * 32), (size_t)T * 9 * D.hdim * sizeof(float), s, a);
+  });
 }
 
 }  // namespace moe
