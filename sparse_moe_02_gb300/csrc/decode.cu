@@ -419,12 +419,14 @@ struct BatchRouterArgs {
 // Blocks [0, router_blocks): one router row per warp for all T tokens; in a routing-only
 // launch the last block to finish selects and writes topk_idx / topk_w / offsets / perm.
 // Blocks after: one shared-expert feature per warp, h_s[t][c] for every token.
+// Instantiated per token count TT (= a.T), as the gate/up and down kernels below.
+template <int TT>
 __global__ void __launch_bounds__(kWarps * 32) dec_batch_router_shared_kernel(BatchRouterArgs a) {
   extern __shared__ uint4 xs[];  // [T][d/8]
   __shared__ int s_last;
   __shared__ BatchSel S;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = a.D.d, nch = d / 8, T = a.T;
+  const int d = a.D.d, nch = d / 8, T = TT;
   const bool router = (int)blockIdx.x < a.router_blocks;
   const int c = ((int)blockIdx.x - a.router_blocks) * kWarps + warp;
   RowFrag r0, r1;
@@ -440,31 +442,29 @@ __global__ void __launch_bounds__(kWarps * 32) dec_batch_router_shared_kernel(Ba
   __syncthreads();
   if (!router) {
     if (c < a.D.fs) {
-      float g[kGemvMaxTokens], u[kGemvMaxTokens];
+      float g[TT], u[TT];
 #pragma unroll
-      for (int t = 0; t < kGemvMaxTokens; ++t) g[t] = u[t] = 0.f;
+      for (int t = 0; t < TT; ++t) g[t] = u[t] = 0.f;
       row_dot_tokens(r0, a.W.ws_gate + (size_t)c * d, xs, nch, (1 << T) - 1, lane, g);
       row_dot_tokens(r1, a.W.ws_up + (size_t)c * d, xs, nch, (1 << T) - 1, lane, u);
 #pragma unroll
-      for (int t = 0; t < kGemvMaxTokens; ++t)
-        if (t < T) {
-          const float gv = warp_sum(g[t]), uv = warp_sum(u[t]);
-          if (lane == 0) a.dw.hdec[((size_t)t * 9 + 8) * a.D.hdim + c] = silu_mul(gv, uv);
-        }
+      for (int t = 0; t < TT; ++t) {
+        const float gv = warp_sum(g[t]), uv = warp_sum(u[t]);
+        if (lane == 0) a.dw.hdec[((size_t)t * 9 + 8) * a.D.hdim + c] = silu_mul(gv, uv);
+      }
     }
     return;
   }
   const int e = blockIdx.x * kWarps + warp;
-  float l[kGemvMaxTokens];
+  float l[TT];
 #pragma unroll
-  for (int t = 0; t < kGemvMaxTokens; ++t) l[t] = 0.f;
+  for (int t = 0; t < TT; ++t) l[t] = 0.f;
   row_dot_tokens(r0, a.W.w_r + (size_t)e * d, xs, nch, (1 << T) - 1, lane, l);
 #pragma unroll
-  for (int t = 0; t < kGemvMaxTokens; ++t)
-    if (t < T) {
-      const float v = warp_sum(l[t]);
-      if (lane == 0) a.dw.logits[(size_t)t * kE + e] = v + (a.W.bias ? a.W.bias[e] : 0.f);
-    }
+  for (int t = 0; t < TT; ++t) {
+    const float v = warp_sum(l[t]);
+    if (lane == 0) a.dw.logits[(size_t)t * kE + e] = v + (a.W.bias ? a.W.bias[e] : 0.f);
+  }
   if (!a.topk_idx) return;  // the forward path selects in the next two kernels
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -747,14 +747,14 @@ static_assert(kGemvMaxTokens == 8, "batch_dispatch covers 1..kGemvMaxTokens");
 cudaError_t prepare_decode_batch_kernels() {
   cudaError_t e;
   const int xs = kBatchMaxTD * 2, hs = kBatchMaxTHdim * 9 * 4;
-  if ((e = cudaFuncSetAttribute(dec_batch_router_shared_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, xs)) != cudaSuccess)
-    return e;
   for (int T = 1; T <= kGemvMaxTokens; ++T) {
     e = batch_dispatch(T, [&](auto tt) {
       constexpr int TT = decltype(tt)::value;
-      cudaError_t r = cudaFuncSetAttribute(dec_batch_gateup_kernel<TT>,
+      cudaError_t r = cudaFuncSetAttribute(dec_batch_router_shared_kernel<TT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, xs);
+      if (r != cudaSuccess) return r;
+      r = cudaFuncSetAttribute(dec_batch_gateup_kernel<TT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, xs);
       if (r != cudaSuccess) return r;
       return cudaFuncSetAttribute(dec_batch_down_combine_kernel<TT>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, hs);
@@ -772,8 +772,10 @@ cudaError_t launch_decode_batch_router_shared(const __nv_bfloat16* x, const Deco
   BatchRouterArgs a{x, W, D, T, topk_idx, offsets, perm, topk_w, dw, kE / kWarps, plan != nullptr,
                     plan_args(T, D), plan ? *plan : RouteWs{}};
   const int blocks = a.router_blocks + (with_shared ? (D.fs + kWarps - 1) / kWarps : 0);
-  return launch_pdl(dec_batch_router_shared_kernel, dim3(blocks), dim3(kWarps * 32),
-                    (size_t)T * D.d * 2, s, a);
+  return batch_dispatch(T, [&](auto tt) {
+    return launch_pdl(dec_batch_router_shared_kernel<decltype(tt)::value>, dim3(blocks),
+                      dim3(kWarps * 32), (size_t)T * D.d * 2, s, a);
+  });
 }
 
 cudaError_t launch_decode_batch_gateup(const __nv_bfloat16* x, const DecodeWeights& W,
