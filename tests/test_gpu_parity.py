@@ -305,8 +305,9 @@ def test_gemv_schedule_rejects_shapes_it_does_not_fit():
 
 # Small batches (2..8 tokens, the speculative-verify shape): the matrix-vector path over the
 # union of the tokens' experts, routing bit-exact and outputs within tolerance, against the
-# oracle; the same tokens through the tensor-core path agree too.
-@pytest.mark.parametrize("T", [2, 3, 5, 8])
+# oracle; the same tokens through the tensor-core path agree too.  Every T: the small-batch
+# kernels are compiled once per token count.
+@pytest.mark.parametrize("T", [2, 3, 4, 5, 6, 7, 8])
 def test_small_batch_decode(T):
     c = build_case("small-batch", d=512, f=128, fs=256, T=T, seed=40 + T)
     for sched in (moe.MOE_SCHEDULE_GEMV, moe.MOE_SCHEDULE_AUTO, moe.MOE_SCHEDULE_GEMM):
@@ -315,14 +316,16 @@ def test_small_batch_decode(T):
         assert_close(got["y"], oracle_outputs(c), f"small batch T={T} schedule {sched}")
 
 
-@pytest.mark.parametrize("T", [2, 5])
+@pytest.mark.parametrize("T", [2, 4, 5])
 def test_small_batch_decode_shape(T):
-    # the benchmark's decode dimensions, d=2048, f=fs=512
+    # the benchmark's decode dimensions, d=2048, f=fs=512, through the matrix-vector path and
+    # the default schedule (the tensor-core path routed and planned by the small router)
     c = build_case("small-batch-decode", d=2048, f=512, fs=512, T=T, seed=7, layer=T,
                    full_host=False)
-    got = _run(c, moe.MOE_SCHEDULE_GEMV)
-    _check_routing(c, got)
-    assert_close(got["y"], oracle_outputs(c), f"small batch decode T={T}")
+    for sched in (moe.MOE_SCHEDULE_GEMV, moe.MOE_SCHEDULE_AUTO):
+        got = _run(c, sched)
+        _check_routing(c, got)
+        assert_close(got["y"], oracle_outputs(c), f"small batch decode T={T} schedule {sched}")
 
 
 def test_two_tokens_run_once_per_token():
