@@ -68,11 +68,12 @@ typedef enum {
 } moe_status;
 
 /* Kernel schedule: AUTO uses the matrix-vector path when T == 1 (with bf16 experts also when
- * T == 2, once per token) and the tensor-core grouped-GEMM path otherwise.  GEMM forces the tensor-core path.  GEMV forces the
- * matrix-vector path: T == 1, or 2 <= T <= 8 when the shape fits (T * max(f, fs) <= 4096 and
- * T * d <= 65536), where every weight row of the union of the tokens' experts is read once
- * and applied to each token that chose it (§ "Limits of further optimization": verifying a
- * few draft tokens at once); other T are rejected with MOE_ERR_UNSUPPORTED. */
+ * T == 2, once per token) and the tensor-core grouped-GEMM path otherwise.  GEMM forces the
+ * tensor-core path.  GEMV forces the matrix-vector path: T == 1, or 2 <= T <= 8 when the
+ * shape fits (T * max(f, fs) <= 4096 and T * d <= 65536), where every weight row of the union
+ * of the tokens' experts is read once and applied to each token that chose it (§ "Limits of
+ * further optimization": verifying a few draft tokens at once); other T are rejected with
+ * MOE_ERR_UNSUPPORTED. */
 typedef enum { MOE_SCHEDULE_AUTO = 0, MOE_SCHEDULE_GEMM = 1, MOE_SCHEDULE_GEMV = 2 } moe_schedule;
 
 typedef struct moe_handle_s* moe_handle;
