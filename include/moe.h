@@ -202,16 +202,21 @@ int moe_profile_end(moe_handle h, float* ms, int capacity, int* n_kernels, int* 
  * KV-cache or activation pool owning nearly all of HBM), or latency-critical code that may
  * not call cudaMalloc because it can synchronise the whole device.
  * Computes, for x [d] bf16 (one token) and w_router [E=256][d] bf16 (+ router_bias [E] fp32
- * or NULL), the same routing as moe_route with T == 1 on a handle: topk_idx [8] int32 (the
- * 8 largest logits, ties to the lower id, ascending expert id) and topk_w [8] fp32 (their
- * softmax weights), all device pointers owned by the caller.
+ * or NULL), the routing that moe_route computes with T == 1 on a handle: topk_idx [8] int32
+ * (the 8 largest logits, ties to the lower id, ascending expert id) and topk_w [8] fp32
+ * (their softmax weights), all device pointers owned by the caller.  The logits are fp32 sums
+ * of the same products in a different order than the handle's router (for d > 2048 the last
+ * bits can differ), so the kept experts are the same whenever the 8th and 9th logits are
+ * further apart than fp32 rounding.
  * Scratch: a 1,280-byte file-scope device array (the 256 logits and a block counter) that
  * every GPU loading this library holds until exit.  All calls share it and it keeps the last
  * call's contents: calls that overlap on the GPU race (keep them on one stream or ordered);
  * each call clears the counter before its kernel.  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  Allocates nothing (no cudaMalloc, cudaFree or allocating
- * library routine).
+ * call before any stream capture.  The address is kept per device and context: after a
+ * cudaDeviceReset (a new context, where the array may sit elsewhere) the next call looks it
+ * up again, so make that call, too, outside any stream capture.  Allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).
  * Errors: MOE_ERR_INVALID_ARG (NULL pointer), MOE_ERR_UNSUPPORTED (d not a multiple of 128
  * or outside 128..8192, the limit of its shared-memory copy of x), MOE_ERR_ALIGNMENT (x,
  * w_router not 16-byte aligned; bias, outputs not 4-byte aligned), MOE_ERR_CUDA. */

@@ -318,14 +318,6 @@ int forward_gemm(moe_handle h, const __nv_bfloat16* xd, int T, __nv_bfloat16* yd
   return cuda_status(moe::launch_combine(T, h->D, h->rws.topk_w, h->rws, h->ys, yd, h->sms, s));
 }
 
-}  // namespace
-
-extern "C" {
-
-}  // extern "C"
-
-namespace {
-
 // moe_create and moe_create_q4: exactly one of w (bf16 experts) and wq (4-bit experts).
 int create_handle(const moe_config* cfg, const moe_weights* w, const moe_weights_q4* wq,
                   moe_handle* out) {

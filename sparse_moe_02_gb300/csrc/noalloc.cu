@@ -12,6 +12,7 @@
 // The array is shared by every call: calls whose kernels overlap on the GPU race on it (use
 // one stream, or order the calls).  Its contents persist between calls; the counter, the
 // only part that must start at zero, is cleared by each call before its kernel runs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -42,9 +43,13 @@ __device__ __forceinline__ float na_dot8(uint4 w, uint4 x) {
   return s;
 }
 
-// Same arithmetic as the handle's batch-1 router: warp per router row, fp32 dot product,
-// the last block to finish keeps the 8 largest logits (ties: lower expert id) in ascending
-// id with their softmax weights.
+// The handle's selection rule with its own summation order: warp per router row, each lane
+// keeping one fp32 running sum over its 16-byte chunks (lane l: chunks l, l + 32, ...), then a
+// warp shuffle reduction.  The handle's batch-1 router sums each 256-chunk piece separately
+// before adding the pieces, so for d > 2048 the two fp32 logits can differ in their last bits;
+// the kept experts agree whenever the 8th and 9th logits are further apart than that rounding.
+// The last block to finish keeps the 8 largest logits (ties: lower expert id) in ascending id
+// with their softmax weights.
 __global__ void __launch_bounds__(kNaWarps * 32)
     route_one_static_kernel(const __nv_bfloat16* x, int d, const __nv_bfloat16* w_r,
                             const float* bias, int32_t* topk_idx, float* topk_w, float* scratch) {
@@ -124,17 +129,48 @@ __global__ void __launch_bounds__(kNaWarps * 32)
 
 std::mutex g_setup_mu;
 float* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on device `dev` (which must be current), looked up
-// once per device: in host code the array's name is only a host-side stand-in.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry point (the library does not link the
+// driver library directly).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  }
+  return fn;
+}
+
+// Device address of the scratch array on device `dev` (which must be current): in host code
+// the array's name is only a host-side stand-in.  The address is looked up with the device
+// current and kept for that device's context; when the current context is a different one
+// (after cudaDeviceReset the runtime creates a new primary context and loads the module again,
+// so the array may have moved) it is looked up again.
 cudaError_t scratch_for_device(int dev, float** out) {
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (!get) return cudaErrorInvalidDevice;
+  // NULL before the runtime has made a context current on this thread
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return cudaErrorInvalidDevice;
+  if (ctx && g_scratch_ptr[dev] && g_scratch_ctx[dev] == ctx) {
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
   }
+  // the lookup itself makes the device's primary context current if none is
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+  if (e != cudaSuccess) return e;
+  if (get(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorInvalidDevice;
+  g_scratch_ptr[dev] = static_cast<float*>(p);
+  g_scratch_ctx[dev] = ctx;
   *out = g_scratch_ptr[dev];
   return cudaSuccess;
 }
@@ -160,8 +196,15 @@ extern "C" int moe_route_one_noalloc(const void* x, int d, const void* w_router,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the block counter must start at zero
   if (cudaMemsetAsync(scratch + moe::kE, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
-  moe::route_one_static_kernel<<<moe::kNaBlocks, moe::kNaWarps * 32, (size_t)d * 2, s>>>(
-      static_cast<const __nv_bfloat16*>(x), d, static_cast<const __nv_bfloat16*>(w_router),
-      router_bias, topk_idx, topk_w, scratch);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  // the launch's own status (not cudaGetLastError, which would also report and clear an
+  // unrelated earlier error of the caller's)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(moe::kNaBlocks);
+  cfg.blockDim = dim3(moe::kNaWarps * 32);
+  cfg.dynamicSmemBytes = (size_t)d * 2;
+  cfg.stream = s;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, moe::route_one_static_kernel, static_cast<const __nv_bfloat16*>(x), d,
+      static_cast<const __nv_bfloat16*>(w_router), router_bias, topk_idx, topk_w, scratch);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
