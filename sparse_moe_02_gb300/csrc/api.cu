@@ -196,6 +196,7 @@ void layout(moe_handle_s* h, char* base, size_t* total) {
   h->rws.err = c.take<int>(1);
   h->dws.logits = c.take<float>((size_t)moe::kGemvMaxTokens * kE);
   h->dws.counter = c.take<int>(1);
+  h->dws.gu_next = c.take<int>(1);
   h->dws.hdec = c.take<float>((size_t)moe::kGemvMaxTokens * 9 * h->D.hdim);
   // the large per-slot buffers hold one forward chunk (Tc tokens, P_chunk padded rows)
   h->h = c.take<__nv_bfloat16>((size_t)h->P_chunk * h->D.hdim);
@@ -406,6 +407,7 @@ int create_handle(const moe_config* cfg, const moe_weights* w, const moe_weights
   if ((st = cuda_status(moe::prepare_expert_kernels()))) return fail(st);
   if ((st = cuda_status(moe::prepare_decode_kernels(D.hdim)))) return fail(st);
   if ((st = cuda_status(moe::prepare_decode_batch_kernels()))) return fail(st);
+  if ((st = cuda_status(moe::prepare_decode_stream_kernels()))) return fail(st);
   if ((st = cuda_status(moe::prepare_decode_q4_kernels()))) return fail(st);
   if ((st = cuda_status(cudaDeviceSynchronize()))) return fail(st);
   *out = h;
@@ -497,12 +499,22 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
                                                              h->rws.err, s, false))))
         return st;
       if ((st = prof_mark(h, s, 3 * t + 1))) return st;
+      __nv_bfloat16* yt = yd + (size_t)t * h->D.d;
+      if (moe::decode_stream_fits(h->D, h->sms)) {
+        // selection, gate/up and down with the combine in one launch (its profiling slot 2
+        // stays empty)
+        if ((st = cuda_status(moe::launch_decode_stream(xt, W, h->D, h->rws.topk_idx,
+                                                        h->rws.topk_w, h->dws, yt, h->rws.err,
+                                                        h->sms, s))))
+          return st;
+        if ((st = prof_mark(h, s, 3 * t + 2))) return st;
+        continue;
+      }
       if ((st = cuda_status(moe::launch_decode_gateup(xt, W, h->D, h->rws.topk_idx,
                                                       h->rws.topk_w, h->dws, s))))
         return st;
       if ((st = prof_mark(h, s, 3 * t + 2))) return st;
-      if ((st = cuda_status(moe::launch_decode_down_combine(W, h->D, h->dws,
-                                                            yd + (size_t)t * h->D.d, s))))
+      if ((st = cuda_status(moe::launch_decode_down_combine(W, h->D, h->dws, yt, s))))
         return st;
     }
     return prof_finish_call(h, s, 3 * T);

@@ -108,6 +108,15 @@ __device__ __forceinline__ void stage_u4(const uint4* src, uint4* dst, int n) {
   }
 }
 
+// The whole block waits for the previous kernel on the stream, but only warp 0 executes
+// griddepcontrol.wait: the other warps park on a hardware barrier, so that the waiting warps
+// of the blocks that start early (beside the previous layer's blocks) take no issue slots from
+// the blocks still working on the same SM.
+__device__ __forceinline__ void pdl_wait_block() {
+  if (threadIdx.x < 32) pdl_wait();
+  __syncthreads();
+}
+
 __device__ __forceinline__ void stage_x(const __nv_bfloat16* x, uint4* xs, int d) {
   const uint4* src = reinterpret_cast<const uint4*>(x);
   for (int i = threadIdx.x; i < d / 8; i += blockDim.x) xs[i] = src[i];
@@ -128,6 +137,9 @@ struct RouterSharedArgs {
 // Blocks [0, router_blocks): one router row per warp, then the last block to finish selects
 // the top 8.  Blocks after: one shared-expert feature (gate and up rows) per warp.  Weight
 // rows are requested before waiting on the previous kernel (they do not depend on it).
+// kShared: the launch also has the shared-expert blocks (a router-only launch keeps one row
+// in registers per warp, small enough to stay resident beside the streamed decode launches).
+template <bool kShared>
 __global__ void __launch_bounds__(kWarps * 32) dec_router_shared_kernel(RouterSharedArgs a) {
   extern __shared__ uint4 xs[];
   __shared__ int s_last;
@@ -139,17 +151,20 @@ __global__ void __launch_bounds__(kWarps * 32) dec_router_shared_kernel(RouterSh
   RowFrag r0, r1;
   if (router) {
     row_load(r0, a.W.w_r + (size_t)(blockIdx.x * kWarps + warp) * d, nch, lane, 0);
-  } else if (c < a.D.fs) {
+  } else if (kShared && c < a.D.fs) {
     row_load(r0, a.W.ws_gate + (size_t)c * d, nch, lane, 0);
     row_load(r1, a.W.ws_up + (size_t)c * d, nch, lane, 0);
   }
-  pdl_wait();  // x may be written by the previous kernel
-  pdl_trigger();
+  pdl_trigger();    // the next launch only prefetches weights before its own wait
+  pdl_wait_block();  // x may be written by the previous kernel
+  // the streamed gate/up launch of this forward hands out work from this counter; every
+  // launch that used it before has completed (the previous kernel on the stream has)
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.dw.gu_next = 0;
   stage_x(a.x, xs, d);
 
   if (!router) {
     // shared expert: h_s[c] = silu(gate_c . x) * (up_c . x)
-    if (c < a.D.fs) {
+    if (kShared && c < a.D.fs) {
       const float g = warp_sum(row_dot_rest(r0, a.W.ws_gate + (size_t)c * d, xs, nch, lane));
       const float u = warp_sum(row_dot_rest(r1, a.W.ws_up + (size_t)c * d, xs, nch, lane));
       if (lane == 0) a.dw.hdec[(size_t)8 * a.D.hdim + c] = silu_mul(g, u);
@@ -662,6 +677,390 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_down_combine_kernel(
   }
 }
 
+// ---------------------------------------------------------------- streamed batch-1 decode
+//
+// The layer's expert work after the router as one launch of one block per SM (§ "Optimize the
+// one-row weight path": the one-row path is bound by reading weights; § "Reduce intermediate
+// and state traffic": the gated activation is fused with the input projections, and the
+// routing scores and the shared expert with the output projection).  A block takes about
+// 212 KB of shared memory at d = 2048, f = 512, so exactly one runs on every SM:
+//   - warp 0 selects the top 8 once the router launch has finished and copies the block's slice
+//     of down rows -- outputs [n0, n1) of the 8 experts and of the shared expert, about 126 KB
+//     -- into shared memory, the routed ones while the slot warps fetch their last items;
+//   - each of eight further warps owns one ring slot (one feature's gate and up rows) and takes
+//     every G-th feature (the shared expert's, then the selected experts'): it requests the rows
+//     of all its later items into L2 at once (HBM needs about 20 MB in flight over the chip to
+//     run at full rate, far more than the ring holds), refills the slot by bulk asynchronous
+//     copies as soon as it has read it, takes the dot products with x and writes
+//     h = silu(gate . x) * (up . x) (fp32) to global memory;
+//   - the blocks then meet at a grid-wide barrier (a counter the router launch zeroes; the
+//     launch's blocks are all resident, one per SM, once the previous layer's have left), load
+//     all of h and combine their outputs in fixed order.
+// Shapes whose buffers do not fit use dec_gateup / dec_down_combine above.
+
+constexpr int kStSlots = 8;                    // ring slots: one feature's gate and up rows each
+constexpr int kStThreads = 32 * (1 + kStSlots);  // warp 0 + one warp per slot
+constexpr int kCbWarps = kStSlots;             // the slot warps also run the combine
+constexpr int kStMaxOut = 16;                  // outputs per block: four per output group
+constexpr int kDownLead = 12;                  // gate/up items left when the down rows go out
+
+struct StreamArgs {
+  const __nv_bfloat16* x;
+  DecodeWeights W;
+  Dims D;
+  int32_t* topk_idx;  // written by block 0 (the selection behind this forward)
+  float* topk_w;
+  DecodeWs dw;
+  __nv_bfloat16* y;
+  int* err;
+};
+
+// Shared-memory layout of a block: the ring, x (bf16), the down rows (up to nn = ceil(d / G)
+// outputs x (8 f + fs) bf16), h as two planes (see h_piece), the mbarriers.
+struct StLayout {
+  uint32_t xs, rows, hp, bars, total;
+};
+__host__ __device__ inline StLayout st_layout(const Dims& D, int G) {
+  StLayout L;
+  const int nn = (D.d + G - 1) / G;
+  L.xs = (uint32_t)kStSlots * 4 * D.d;
+  L.rows = L.xs + 2 * D.d;
+  L.hp = L.rows + round_up(nn * (8 * D.f + D.fs) * 2, 16);
+  L.bars = L.hp + 9 * D.hdim * 4;
+  L.total = L.bars + (kStSlots + 2) * 8;
+  return L;
+}
+
+// 8 bf16 weights times 8 fp32 values.
+__device__ __forceinline__ float dot8_f32v(uint4 w, float4 h0, float4 h1) {
+  float a = bf16_lo(w.x) * h0.x, b = bf16_hi(w.x) * h0.y;
+  a = fmaf(bf16_lo(w.y), h0.z, a);
+  b = fmaf(bf16_hi(w.y), h0.w, b);
+  a = fmaf(bf16_lo(w.z), h1.x, a);
+  b = fmaf(bf16_hi(w.z), h1.y, b);
+  a = fmaf(bf16_lo(w.w), h1.z, a);
+  b = fmaf(bf16_hi(w.w), h1.w, b);
+  return a + b;
+}
+
+// The h vectors in shared memory as two planes: plane q holds floats 4q .. 4q + 3 of every
+// 8-float piece, piece c of expert rank j (j = 8: the shared expert) at float4 index
+// j * hdim / 8 + c of its plane -- so that 32 lanes reading 32 consecutive pieces read 512
+// contiguous bytes per load (no bank conflict), against 32-byte strides in the plain layout.
+__device__ __forceinline__ float4 h_piece(const float4* hp, int hdim, int j, int c, int q) {
+  return hp[(size_t)q * (9 * hdim / 8) + (size_t)j * (hdim / 8) + c];
+}
+
+// out[i] = bf16(sum_j w_j (rows_j[i] . h_j) + rows_s[i] . h_s) for i < nn (1 <= nn <= 16), by
+// the kCbWarps warps of the combine (cw: this warp's index among them, ct: this thread's): the
+// rows of expert rank j at rows + j nn 2f, the shared expert's at rows + 8 nn 2f (2fs bytes
+// each).  Combine warp w takes the outputs w % 4, w % 4 + 4, ... and half w / 4 of every row's
+// 16-byte pieces, lane l the pieces l, l + 32, ... of that half: each row byte and each h byte
+// is read once per warp that needs it, in 512-byte conflict-free loads.  Per output and piece
+// the terms run over the experts in ascending id, then the shared expert; pieces within a lane,
+// then lanes, then the two halves are added after.  All combine threads call this (it holds
+// named barrier 4); part is shared scratch of kCbWarps * 4 floats.
+__device__ __forceinline__ void dn_combine_rows(const uint8_t* rows, const float4* hp, int nn,
+                                                int f, int fs, int hdim, const float* w,
+                                                float* part, __nv_bfloat16* out, int cw,
+                                                int ct) {
+  const int lane = ct & 31;
+  const int og = cw & 3, half = cw >> 2;
+  const size_t rb = (size_t)f * 2, srb = (size_t)fs * 2;
+  // the four outputs of this warp; past nn the last row is read again and its sum dropped, so
+  // that the loop body has no branch (a branch per output keeps the compiler from interleaving
+  // the outputs' dot products, and the warp then stalls on each short chain)
+  int oi[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) oi[m] = min(og + 4 * m, nn - 1);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  auto piece = [&](int j, int c, const uint8_t* base, size_t pitch, float wj) {
+    const float4 ha = h_piece(hp, hdim, j, c, 0), hb = h_piece(hp, hdim, j, c, 1);
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      acc[m] = fmaf(wj, dot8_f32v(reinterpret_cast<const uint4*>(base + oi[m] * pitch)[c], ha, hb),
+                    acc[m]);
+  };
+  if (f == fs && f % 512 == 0) {
+    // one row length, a whole number of pieces per lane: pieces outer, the 9 experts unrolled
+    // inside (straight-line code over all of them)
+    const int K8 = f / 8;
+    for (int c = half * K8 / 2 + lane; c < (half + 1) * K8 / 2; c += 32) {
+#pragma unroll
+      for (int j = 0; j < 9; ++j) piece(j, c, rows + j * nn * rb, rb, j < 8 ? w[j] : 1.0f);
+    }
+  } else {
+#pragma unroll 1
+    for (int j = 0; j < 9; ++j) {
+      const int K8 = (j < 8 ? f : fs) / 8;
+      const uint8_t* base = rows + (j < 8 ? j * nn * rb : 8 * nn * rb);
+      const size_t pitch = j < 8 ? rb : srb;
+      const float wj = j < 8 ? w[j] : 1.0f;
+      for (int c = half * K8 / 2 + lane; c < (half + 1) * K8 / 2; c += 32)
+        piece(j, c, base, pitch, wj);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const float v = warp_sum(acc[m]);
+    if (lane == 0) part[cw * 4 + m] = v;
+  }
+  named_sync(4, kCbWarps * 32);
+  if (ct < nn) {
+    const int g = ct & 3, m = ct >> 2;
+    out[ct] = __float2bfloat16_rn(part[g * 4 + m] + part[(g + 4) * 4 + m]);
+  }
+}
+static_assert(kCbWarps == 8, "the combine pairs warps w and w + 4 (two halves of K)");
+
+// At most 168 registers: beside a router block (256 x 64 registers) on the same SM.
+__global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t ssm[];
+  __shared__ int s_ids[kTopK];
+  __shared__ float s_w[kTopK];
+  __shared__ float s_part[kCbWarps * 4];
+  __shared__ int s_fail;
+  __shared__ int s_issued;  // gate/up items whose copies the slot warps have issued
+  const int d = a.D.d, f = a.D.f, fs = a.D.fs, hdim = a.D.hdim, nch = d / 8;
+  const int G = gridDim.x, b = blockIdx.x;
+  const StLayout Ly = st_layout(a.D, G);
+  const uint32_t row_bytes = (uint32_t)d * 2, slot_bytes = 2 * row_bytes;
+  uint8_t* ring = ssm;
+  uint4* xs = reinterpret_cast<uint4*>(ssm + Ly.xs);
+  uint8_t* rows = ssm + Ly.rows;
+  float* hs = reinterpret_cast<float*>(ssm + Ly.hp);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ssm + Ly.bars);
+  uint64_t* sel_ready = full + kStSlots;  // s_ids holds this forward's selection
+  uint64_t* dbar = sel_ready + 1;         // the down rows have landed
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = (int)((long long)b * d / G), nn = (int)((long long)(b + 1) * d / G) - n0;
+  const uint32_t rb = (uint32_t)f * 2, srb = (uint32_t)fs * 2;
+  // this block's gate/up items: the shared expert's features b, b + G, ..., then the routed
+  // features r = j f + c (j: rank of the expert in ascending id) b, b + G, ...: at any moment
+  // the blocks together request consecutive rows, a few sequential sweeps for DRAM
+  const int ns = fs > b ? (fs - b + G - 1) / G : 0;
+  const int nr = kTopK * f;
+  const int nitems = ns + (nr > b ? (nr - b + G - 1) / G : 0);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStSlots; ++i) mbar_init(&full[i], 1);
+    mbar_init(sel_ready, 1);
+    mbar_init(dbar, 1);
+    s_fail = 0;
+    s_issued = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();  // the next layer's router may request its rows (it waits for this launch)
+  const uint64_t pol = policy_evict_first();  // every weight row is read once
+
+  if (warp == 0) {
+    // ---- selection and the down rows
+    if (lane == 0) {
+      mbar_arrive_expect_tx(dbar, (uint32_t)nn * (8 * rb + srb));
+      bulk_load(rows + 8 * nn * rb, a.W.ws_down + (size_t)n0 * fs, nn * srb, dbar, pol);
+    }
+    pdl_wait();  // the router's logits (and x) are final
+    named_arrive(2, kStThreads);  // releases the slot warps (parked on the same barrier)
+    select_top8(a.dw.logits, lane, s_ids, s_w);
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      mbar_arrive(sel_ready);
+    }
+    // the routed down rows once the slot warps have issued all but their last items: HBM then
+    // serves the gate/up rows first (the grid barrier waits for those) and the down rows during
+    // the last items and the barrier (the combine after it waits for these)
+    if (lane == 0) {
+      const int want = nitems - kDownLead;
+      const uint64_t t0 = global_timer_ns();
+      while (*reinterpret_cast<volatile int*>(&s_issued) < want &&
+             global_timer_ns() - t0 < kWaitLimitNs)
+        __nanosleep(256);
+    }
+    __syncwarp();
+    if (lane < kTopK)
+      bulk_load(rows + lane * nn * rb, a.W.w_down + ((size_t)s_ids[lane] * d + n0) * f, nn * rb,
+                dbar, pol);
+    if (b == 0 && lane < kTopK) {
+      a.topk_idx[lane] = s_ids[lane];
+      a.topk_w[lane] = s_w[lane];
+    }
+  } else {
+    // ---- slot warp s: items s, s + 8, ..., each refilled by its own warp as soon as the warp
+    // has read the previous one
+    const int s = warp - 1;
+    auto item_rows = [&](int k, const __nv_bfloat16*& g, const __nv_bfloat16*& u) {
+      if (k < ns) {
+        g = a.W.ws_gate + (size_t)(b + k * G) * d;
+        u = a.W.ws_up + (size_t)(b + k * G) * d;
+      } else {
+        const int r = b + (k - ns) * G, j = r / f;
+        const size_t row = ((size_t)s_ids[j] * f + (r - j * f)) * d;
+        g = a.W.w_gate + row;
+        u = a.W.w_up + row;
+      }
+    };
+    auto issue = [&](int k) {  // lane 0; a routed item needs the selection
+      const __nv_bfloat16 *g, *u;
+      item_rows(k, g, u);
+      mbar_arrive_expect_tx(&full[s], slot_bytes);
+      bulk_load(ring + s * slot_bytes, g, row_bytes, &full[s], pol);
+      bulk_load(ring + s * slot_bytes + row_bytes, u, row_bytes, &full[s], pol);
+      atomicAdd(&s_issued, 1);
+    };
+    bool sel = false;  // lane 0 has seen the selection
+    auto ensure_sel = [&]() {
+      if (!sel) sel = mbar_wait(sel_ready, 0, a.err);
+      return sel;
+    };
+    int k = s, u = 0;
+    if (lane == 0 && k < ns) issue(k);  // a shared feature: before the router has finished
+    named_sync(2, kStThreads);          // warp 0 has passed its wait: x is final
+    const uint4* xsrc = reinterpret_cast<const uint4*>(a.x);
+    for (int i = threadIdx.x - 32; i < nch; i += kStThreads - 32) xs[i] = __ldcg(xsrc + i);
+    named_sync(1, kStThreads - 32);
+    bool ok = true;
+    if (lane == 0 && k >= ns && k < nitems) {
+      ok = ensure_sel();
+      if (ok) issue(k);
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    // the rows of item kk requested into L2, one 128-byte line per lane and request (lane 0
+    // has seen the selection if kk is routed); each warp keeps the two items after the one in
+    // its slot requested, about 190 KB per SM in flight: HBM needs about 20 MB in flight over
+    // the chip to run at full rate, far more than the ring holds, and the requests still come
+    // back roughly in the order the slots consume them
+    auto prefetch_item = [&](int kk) {
+      const __nv_bfloat16 *g, *uu;
+      item_rows(kk, g, uu);
+      for (uint32_t o = lane * 128u; o < row_bytes; o += 32 * 128u) {
+        prefetch_l2_line(reinterpret_cast<const char*>(g) + o);
+        prefetch_l2_line(reinterpret_cast<const char*>(uu) + o);
+      }
+    };
+    bool selw = false;  // the whole warp has seen the selection
+    auto prefetch_ahead = [&](int kk) {
+      if (kk >= nitems) return;
+      if (kk >= ns && !selw) selw = __all_sync(0xffffffffu, mbar_wait(sel_ready, 0, a.err));
+      if (kk < ns || selw) prefetch_item(kk);
+    };
+    if (ok) {
+      prefetch_ahead(k + kStSlots);
+      prefetch_ahead(k + 2 * kStSlots);
+    }
+    const uint4* gr = reinterpret_cast<const uint4*>(ring + s * slot_bytes);
+    const uint4* ur = gr + nch;
+    for (; ok && k < nitems; ++u, k += kStSlots) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], u & 1, a.err))) {
+        ok = false;
+        break;
+      }
+      float g0 = 0.f, g1 = 0.f, v0 = 0.f, v1 = 0.f;
+#pragma unroll 4
+      for (int c = lane; c < nch; c += 32) {
+        const uint4 xv = xs[c], wg = gr[c], wu = ur[c];
+        const float x0 = bf16_lo(xv.x), x1 = bf16_hi(xv.x), x2 = bf16_lo(xv.y), x3 = bf16_hi(xv.y);
+        const float x4 = bf16_lo(xv.z), x5 = bf16_hi(xv.z), x6 = bf16_lo(xv.w), x7 = bf16_hi(xv.w);
+        g0 = fmaf(bf16_lo(wg.x), x0, g0);
+        g1 = fmaf(bf16_hi(wg.x), x1, g1);
+        v0 = fmaf(bf16_lo(wu.x), x0, v0);
+        v1 = fmaf(bf16_hi(wu.x), x1, v1);
+        g0 = fmaf(bf16_lo(wg.y), x2, g0);
+        g1 = fmaf(bf16_hi(wg.y), x3, g1);
+        v0 = fmaf(bf16_lo(wu.y), x2, v0);
+        v1 = fmaf(bf16_hi(wu.y), x3, v1);
+        g0 = fmaf(bf16_lo(wg.z), x4, g0);
+        g1 = fmaf(bf16_hi(wg.z), x5, g1);
+        v0 = fmaf(bf16_lo(wu.z), x4, v0);
+        v1 = fmaf(bf16_hi(wu.z), x5, v1);
+        g0 = fmaf(bf16_lo(wg.w), x6, g0);
+        g1 = fmaf(bf16_hi(wg.w), x7, g1);
+        v0 = fmaf(bf16_lo(wu.w), x6, v0);
+        v1 = fmaf(bf16_hi(wu.w), x7, v1);
+      }
+      const float g = warp_sum(g0 + g1), v = warp_sum(v0 + v1);
+      __syncwarp();  // every lane has read the slot: refill it
+      const int kn = k + kStSlots;
+      prefetch_ahead(k + 3 * kStSlots);
+      bool issued = true;
+      if (lane == 0 && kn < nitems) {
+        if (kn < ns || ensure_sel()) issue(kn);
+        else issued = false;
+      }
+      if (lane == 0) {
+        int hidx;
+        if (k < ns) {
+          hidx = 8 * hdim + b + k * G;
+        } else {
+          const int r = b + (k - ns) * G, j = r / f;
+          hidx = j * hdim + (r - j * f);
+        }
+        a.dw.hdec[hidx] = silu_mul(g, v);
+      }
+      if (!__all_sync(0xffffffffu, issued)) {
+        ok = false;
+        ++u;  // the slot holds no copy in flight
+        k = nitems;
+        break;
+      }
+    }
+    if (!ok) {
+      // after a timeout: the slot's copy, if one is in flight, gets another bounded chance to
+      // land before the block can leave; the block still takes part in every barrier below
+      if (lane == 0) {
+        if (k < nitems) mbar_wait(&full[s], u & 1, a.err);
+        s_fail = 1;
+      }
+    }
+  }
+
+  // ---- grid-wide: every block's h is in global memory
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(a.dw.gu_next, 1);
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.dw.gu_next) : "memory");
+      if (v >= G) break;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicExch(a.err, kDevErrTimeout);
+        s_fail = 1;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  {
+    // float4 q of h (expert rank q / (hdim / 4)) goes to plane q % 2, piece (q % (hdim / 4)) / 2
+    const float4* src = reinterpret_cast<const float4*>(a.dw.hdec);
+    float4* dst = reinterpret_cast<float4*>(hs);
+    const int n4 = 9 * hdim / 4, per = hdim / 4;
+    for (int base = threadIdx.x; base < n4; base += 8 * kStThreads) {
+      float4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (base + i * kStThreads < n4) v[i] = __ldcg(src + base + i * kStThreads);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = base + i * kStThreads;
+        if (q < n4) dst[(q & 1) * (n4 / 2) + (q / per) * (per / 2) + (q % per) / 2] = v[i];
+      }
+    }
+  }
+  if (warp == 0) {
+    const bool landed = mbar_wait(dbar, 0, a.err);
+    // after a timeout: one more bounded chance for the copies to land before the block leaves
+    if (!landed) mbar_wait(dbar, 0, a.err);
+    if (lane == 0 && !landed) s_fail = 1;
+  }
+  __syncthreads();
+  if (s_fail || warp == 0) return;
+  dn_combine_rows(rows, reinterpret_cast<const float4*>(hs), nn, f, fs, hdim, s_w, s_part,
+                  a.y + n0, warp - 1, threadIdx.x - 32);
+}
+
 }  // namespace
 
 namespace {
@@ -696,8 +1095,11 @@ cudaError_t launch_decode_router_shared(const __nv_bfloat16* x, const DecodeWeig
                                         int32_t* offsets, int32_t* perm, const DecodeWs& dw,
                                         int* err, cudaStream_t s, bool with_shared) {
   RouterSharedArgs a{x, W, D, topk_idx, offsets, perm, topk_w, dw, kE / kWarps, err};
-  const int blocks = a.router_blocks + (with_shared ? (D.fs + kWarps - 1) / kWarps : 0);
-  return launch_pdl(dec_router_shared_kernel, dim3(blocks), dim3(kWarps * 32),
+  if (!with_shared)
+    return launch_pdl(dec_router_shared_kernel<false>, dim3(a.router_blocks), dim3(kWarps * 32),
+                      (size_t)D.d * 2, s, a);
+  const int blocks = a.router_blocks + (D.fs + kWarps - 1) / kWarps;
+  return launch_pdl(dec_router_shared_kernel<true>, dim3(blocks), dim3(kWarps * 32),
                     (size_t)D.d * 2, s, a);
 }
 
@@ -715,6 +1117,43 @@ cudaError_t launch_decode_down_combine(const DecodeWeights& W, const Dims& D, co
   const int grid = std::min(g_down_grid, (D.d + kWarps - 1) / kWarps);
   return launch_pdl(dec_down_combine_kernel, dim3(grid), dim3(kWarps * 32),
                     (size_t)9 * D.hdim * sizeof(float), s, a);
+}
+
+// ---- streamed batch-1 decode
+
+namespace {
+int stream_grid(const Dims& D, int sms) { return D.d < sms ? D.d : sms; }
+}  // namespace
+
+bool decode_stream_fits(const Dims& D, int sms) {
+  const int G = stream_grid(D, sms);
+  return D.d <= kStreamMaxD && (D.d + G - 1) / G <= kStMaxOut &&
+         st_layout(D, G).total <= (uint32_t)kStreamMaxSmem;
+}
+
+cudaError_t prepare_decode_stream_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(dec_stream_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kStreamMaxSmem);
+  if (e != cudaSuccess) return e;
+  // an SM's split between L1 and shared memory is set when a block starts on an idle SM: both
+  // launches of a layer ask for the largest shared memory, so that the next layer's router
+  // block fits beside a streaming block
+  const void* ks[2] = {reinterpret_cast<const void*>(dec_stream_kernel),
+                       reinterpret_cast<const void*>(dec_router_shared_kernel<false>)};
+  for (const void* k : ks)
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+      return e;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_stream(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
+                                 int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
+                                 __nv_bfloat16* y, int* err, int sms, cudaStream_t s) {
+  StreamArgs a{x, W, D, topk_idx, topk_w, dw, y, err};
+  const int G = stream_grid(D, sms);
+  return launch_pdl(dec_stream_kernel, dim3(G), dim3(kStThreads), st_layout(D, G).total, s, a);
 }
 
 // ---- small batches

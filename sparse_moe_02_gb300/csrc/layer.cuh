@@ -149,6 +149,7 @@ constexpr int kBatchMaxTD = 65536;    // T * d
 struct DecodeWs {
   float* logits;   // [kGemvMaxTokens][E]
   int* counter;    // last-block detection of the router
+  int* gu_next;    // grid barrier counter of the streamed launch (zeroed by the router launch)
   float* hdec;     // [kGemvMaxTokens][9][hdim] fp32: routed experts j = 0..7, shared = 8
 };
 
@@ -156,6 +157,20 @@ struct DecodeWeights {
   const __nv_bfloat16 *w_r, *w_gate, *w_up, *w_down, *ws_gate, *ws_up, *ws_down;
   const float* bias;
 };
+
+// Streamed batch-1 decode: after the router launch (routing only), one launch of one block per
+// SM that selects, streams the shared expert's and the 8 selected experts' gate/up rows (h into
+// dw.hdec), meets at a grid-wide barrier (counter dw.gu_next, zeroed by the router launch) and
+// combines its slice of outputs from the down rows it copied meanwhile; block 0 writes
+// topk_idx / topk_w.  Shapes whose buffers exceed these limits use the per-warp kernels
+// (launch_decode_gateup, launch_decode_down_combine).
+constexpr int kStreamMaxD = 2048;
+constexpr int kStreamMaxSmem = 218 * 1024;  // leaves room for a router block on the same SM
+bool decode_stream_fits(const Dims& D, int sms);
+cudaError_t prepare_decode_stream_kernels();
+cudaError_t launch_decode_stream(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
+                                 int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
+                                 __nv_bfloat16* y, int* err, int sms, cudaStream_t s);
 
 // Router GEMV (logits) and the shared expert's gate/up GEMV, one launch.  When topk_idx is
 // not NULL (routing requested) the last router block to finish also writes the top 8.

@@ -11,6 +11,42 @@ __device__ __forceinline__ uint32_t float_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// (v, e) ranks above (w, f): larger value, or equal value and lower expert id.
+__device__ __forceinline__ bool ranks_above(float v, int e, float w, int f) {
+  return v > w || (v == w && e < f);
+}
+
+__device__ __forceinline__ void cas_pair(float& v0, int& i0, float& v1, int& i1) {
+  const bool sw = ranks_above(v1, i1, v0, i0);
+  const float a = sw ? v1 : v0, b = sw ? v0 : v1;
+  const int ia = sw ? i1 : i0, ib = sw ? i0 : i1;
+  v0 = a; v1 = b; i0 = ia; i1 = ib;
+}
+
+// Merges the descending list of the lane `o` apart (xor) into this lane's: the better of
+// entry i and the partner's entry 7 - i keeps the top 8 of both as a bitonic sequence, which
+// three half-cleaner stages sort.
+__device__ __forceinline__ void top8_merge_xor(float (&v)[8], int (&id)[8], int o) {
+  float w[8];
+  int f[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    w[i] = __shfl_xor_sync(0xffffffffu, v[7 - i], o);
+    f[i] = __shfl_xor_sync(0xffffffffu, id[7 - i], o);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool tk = ranks_above(w[i], f[i], v[i], id[i]);
+    v[i] = tk ? w[i] : v[i];
+    id[i] = tk ? f[i] : id[i];
+  }
+#pragma unroll
+  for (int h = 4; h > 0; h >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & h) == 0) cas_pair(v[i], id[i], v[i + h], id[i + h]);
+}
+
 // Warp-level selection from logits[256] (read through L2): the 8 largest (ties: lower id),
 // listed in ascending expert id with their softmax weights; lanes 0..7 write ids[rank],
 // w[rank].  Lane l holds the logits of ids l + 32 i.  Eight rounds, each taking the warp-wide
