@@ -687,12 +687,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) dec_batch_down_combine_kernel(
 //   - warp 0 selects the top 8 once the router launch has finished and copies the block's slice
 //     of down rows -- outputs [n0, n1) of the 8 experts and of the shared expert, about 126 KB
 //     -- into shared memory, the routed ones while the slot warps fetch their last items;
-//   - each of eight further warps owns one ring slot (one feature's gate and up rows) and takes
-//     every G-th feature (the shared expert's, then the selected experts'): it requests the rows
-//     of all its later items into L2 at once (HBM needs about 20 MB in flight over the chip to
-//     run at full rate, far more than the ring holds), refills the slot by bulk asynchronous
-//     copies as soon as it has read it, takes the dot products with x and writes
-//     h = silu(gate . x) * (up . x) (fp32) to global memory;
+//   - the block's gate/up items are every G-th feature (the shared expert's, then the selected
+//     experts'); each of eight further warps owns one ring slot (one feature's gate and up
+//     rows), takes the block's next item whenever its slot is free, refills the slot by bulk
+//     asynchronous copies, takes the dot products with x and writes
+//     h = silu(gate . x) * (up . x) (fp32) to global memory; items are requested into L2 two
+//     rounds ahead of their copy (HBM needs about 20 MB in flight over the chip to run at full
+//     rate, far more than the ring holds);
 //   - the blocks then meet at a grid-wide barrier (a counter the router launch zeroes; the
 //     launch's blocks are all resident, one per SM, once the previous layer's have left), load
 //     all of h and combine their outputs in fixed order.
@@ -821,6 +822,7 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
   __shared__ float s_part[kCbWarps * 4];
   __shared__ int s_fail;
   __shared__ int s_issued;  // gate/up items whose copies the slot warps have issued
+  __shared__ int s_next;    // next gate/up item to hand out (items 0..7: one per slot warp)
   const int d = a.D.d, f = a.D.f, fs = a.D.fs, hdim = a.D.hdim, nch = d / 8;
   const int G = gridDim.x, b = blockIdx.x;
   const StLayout Ly = st_layout(a.D, G);
@@ -847,6 +849,7 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
     mbar_init(dbar, 1);
     s_fail = 0;
     s_issued = 0;
+    s_next = kStSlots;
     fence_mbar_init();
   }
   __syncthreads();
@@ -944,13 +947,16 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
       if (kk >= ns && !selw) selw = __all_sync(0xffffffffu, mbar_wait(sel_ready, 0, a.err));
       if (kk < ns || selw) prefetch_item(kk);
     };
+    // items are handed out in index order (each slot warp takes the next one when its slot is
+    // free); item i is requested into L2 when item i - 16 is handed out, items 8 .. 23 here
     if (ok) {
       prefetch_ahead(k + kStSlots);
       prefetch_ahead(k + 2 * kStSlots);
     }
+    int kn = 0;  // lane 0: the item this warp takes next
     const uint4* gr = reinterpret_cast<const uint4*>(ring + s * slot_bytes);
     const uint4* ur = gr + nch;
-    for (; ok && k < nitems; ++u, k += kStSlots) {
+    for (; ok && k < nitems; ++u, k = __shfl_sync(0xffffffffu, kn, 0)) {
       if (!__all_sync(0xffffffffu, mbar_wait(&full[s], u & 1, a.err))) {
         ok = false;
         break;
@@ -980,8 +986,8 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
       }
       const float g = warp_sum(g0 + g1), v = warp_sum(v0 + v1);
       __syncwarp();  // every lane has read the slot: refill it
-      const int kn = k + kStSlots;
-      prefetch_ahead(k + 3 * kStSlots);
+      if (lane == 0) kn = atomicAdd(&s_next, 1);
+      prefetch_ahead(__shfl_sync(0xffffffffu, kn, 0) + 2 * kStSlots);
       bool issued = true;
       if (lane == 0 && kn < nitems) {
         if (kn < ns || ensure_sel()) issue(kn);
@@ -1000,6 +1006,11 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
       if (!__all_sync(0xffffffffu, issued)) {
         ok = false;
         ++u;  // the slot holds no copy in flight
+        k = nitems;
+        break;
+      }
+      if (__shfl_sync(0xffffffffu, kn, 0) >= nitems) {
+        ++u;
         k = nitems;
         break;
       }
