@@ -14,7 +14,9 @@ Also measured in the same run and reported in the same line:
        inside the timed region);
   cpu_baseline: the CPU oracle on a bounded sample of the same workload (rank 0 only);
   prefill_skewed: the same layer with skewed routing (router bias -2.4 ln(rank_e)), timed
-       and set against the floor of its own bytes and FLOPs; --sweep adds T = 256 .. 131072.
+       and set against the floor of its own bytes and FLOPs;
+  prefill_sweep: the balanced layer at T = 256 .. 131072 (bf16; --sweep-q4 adds 4-bit experts),
+       each T with the floor of its bytes and FLOPs.
 --impl reference times only the CPU oracle (the reference arm of this benchmark).
 """
 import argparse
@@ -58,10 +60,12 @@ def parse_args():
     p.add_argument("--no-q4", action="store_true", help="skip the 4-bit prefill and decode lines")
     p.add_argument("--no-small-batch", action="store_true",
                    help="skip the T = 2..5 decode lines")
-    p.add_argument("--sweep", action="store_true",
-                   help="also time the prefill layer at T = 256 .. 131072 (balanced)")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the prefill length sweep (T = 256 .. 131072, balanced, bf16)")
+    p.add_argument("--sweep-q4", action="store_true",
+                   help="also run the length sweep with 4-bit experts")
     p.add_argument("--sweep-tokens", type=str, default=None,
-                   help="comma-separated T values for --sweep (default: 256 .. 131072)")
+                   help="comma-separated T values of the sweep (default: 256 .. 131072)")
     return p.parse_args()
 
 
@@ -442,7 +446,7 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
             "bytes_per_layer": DECODE_BYTES_PER_LAYER,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": P_hbm, "unit": "GB/s",
                          "frac": gbs / P_hbm},
-            "kernel_us_eager": {k: round(v / nc * 1e3, 3) for k, v in zip(KERNELS_GEMV, kms)},
+            "kernel_us_eager": decode_kernel_times(kms, nc),
             "read_probe": {"GB_per_s": read_gbs, "frac_of_read_probe": gbs / read_gbs,
                            "how": "moe_read_probe over 4 GiB, best of 10 (a read-only stream; "
                                   "the roofline peak above stays the measured copy rate)"},
@@ -450,6 +454,16 @@ def run_decode(torch, moe, args, rank, world, P_hbm):
             "graph": f"{nl} stream-ordered layer calls, replayed per step",
             "small_batch": small,
             "q4": q4}
+
+
+def decode_kernel_times(kms, nc):
+    """Per-kernel eager times (us) of one batch-1 layer from moe_profile_end: the router
+    launch, then either the streamed launch (its second slot empty) or the gate/up and the
+    down+combine launches."""
+    us = [v / nc * 1e3 for v in kms]
+    if len(us) == 3 and us[2] < 0.05 * max(us[1], 1e-9):
+        return {"decode_router": round(us[0], 3), "decode_expert_stream": round(us[1], 3)}
+    return {k: round(v, 3) for k, v in zip(KERNELS_GEMV, us)}
 
 
 def q4_device_weights(torch, seed, layer, dims, bias=None):
@@ -715,11 +729,11 @@ def main():
     skewed = None if args.no_skew else time_prefill(
         torch, moe, T_PREFILL, True, min(args.steps, 50), max(3, args.warmup), rank, P_hbm, P_tc)
     sweep = None
-    if args.sweep:
+    if not args.no_sweep:
         ts = [int(t) for t in args.sweep_tokens.split(",")] if args.sweep_tokens else SWEEP_T
         sweep = [time_prefill(torch, moe, t, False, min(args.steps, 20), 3, rank, P_hbm, P_tc)
                  for t in ts]
-        if not args.no_q4:
+        if args.sweep_q4:
             sweep += [time_prefill(torch, moe, t, False, min(args.steps, 20), 3, rank, P_hbm,
                                    P_tc, q4=True) for t in ts]
     pre_q4 = None if args.no_q4 else run_prefill_q4(torch, moe, args, rank, P_hbm, P_tc)

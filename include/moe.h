@@ -166,6 +166,16 @@ int moe_forward_host(moe_handle h, const void* x_host, int T, void* y_host, void
  * (MOE_OK if no kernel reported a failure since the last call). */
 int moe_get_device_error(moe_handle h, void* stream);
 
+/* Test hook for the kernels' bounded waits (failure detection without a GPU fault): the next
+ * n_calls batch-1 forwards on this bf16 handle run the streamed decode launch with its grid-wide
+ * barrier waiting for one block more than the launch has and giving up after 1 ms.  Each such
+ * call leaves y undefined and records MOE_ERR_TIMEOUT in the device error word
+ * (moe_get_device_error); its blocks still let their own copies land before they leave, so
+ * the next forward runs normally.  MOE_ERR_UNSUPPORTED: a 4-bit handle, or a shape the
+ * streamed launch does not take (d > 2048 or too many down rows per block); the calls of
+ * other schedules are not affected. */
+int moe_test_expire_waits(moe_handle h, int n_calls);
+
 /* Frees the workspace and the handle (synchronises the device).  NULL is accepted. */
 int moe_destroy(moe_handle h);
 

@@ -29,7 +29,8 @@ MOE_SCHEDULE_GEMV = 2
 
 EXPORTS = ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_get_device_error",
            "moe_destroy", "moe_status_string", "moe_last_cuda_error", "moe_profile_begin",
-           "moe_profile_end", "moe_route_one_noalloc", "moe_create_q4", "moe_read_probe")
+           "moe_profile_end", "moe_route_one_noalloc", "moe_create_q4", "moe_read_probe",
+           "moe_test_expire_waits")
 
 # kernel order reported by moe_profile_end
 KERNELS_GEMM = ("router_topk", "route_plan_scatter", "experts", "combine")
@@ -90,9 +91,11 @@ def lib():
                                       ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]
         L.moe_route_one_noalloc.argtypes = [_c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                             _c_void_p, _c_void_p]
+        L.moe_test_expire_waits.argtypes = [_c_void_p, _c_int]
         for fn in ("moe_create", "moe_create_q4", "moe_read_probe", "moe_route", "moe_forward", "moe_forward_host",
                    "moe_get_device_error", "moe_destroy", "moe_last_cuda_error",
-                   "moe_profile_begin", "moe_profile_end", "moe_route_one_noalloc"):
+                   "moe_profile_begin", "moe_profile_end", "moe_route_one_noalloc",
+                   "moe_test_expire_waits"):
             getattr(L, fn).restype = _c_int
         _lib = L
     return _lib
@@ -147,6 +150,12 @@ def moe_last_cuda_error():
 def moe_route_one_noalloc(x, d, w_router, router_bias, topk_idx, topk_w, stream):
     """Routing of one token with no device allocation (see include/moe.h)."""
     return lib().moe_route_one_noalloc(x, d, w_router, router_bias, topk_idx, topk_w, stream)
+
+
+def moe_test_expire_waits(h, n_calls):
+    """Test hook: the next n_calls batch-1 forwards time out at their grid barrier (see
+    include/moe.h)."""
+    return lib().moe_test_expire_waits(h, n_calls)
 
 
 def moe_profile_begin(h, n_calls):

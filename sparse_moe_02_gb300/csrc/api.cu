@@ -109,6 +109,7 @@ struct moe_handle_s {
   static constexpr int kMaxKernels = 6;
   std::vector<cudaEvent_t> prof_ev;  // [n_calls][kMaxKernels + 1]
   int prof_calls = 0, prof_done = 0, prof_nk = 0;
+  int expire_calls = 0;  // moe_test_expire_waits: streamed decode launches left to expire
 };
 
 namespace {
@@ -503,9 +504,11 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
       if (moe::decode_stream_fits(h->D, h->sms)) {
         // selection, gate/up and down with the combine in one launch (its profiling slot 2
         // stays empty)
+        const bool expire = h->expire_calls > 0;
+        if (expire) --h->expire_calls;
         if ((st = cuda_status(moe::launch_decode_stream(xt, W, h->D, h->rws.topk_idx,
                                                         h->rws.topk_w, h->dws, yt, h->rws.err,
-                                                        h->sms, s))))
+                                                        h->sms, s, expire))))
           return st;
         if ((st = prof_mark(h, s, 3 * t + 2))) return st;
         continue;
@@ -646,6 +649,13 @@ int moe_profile_end(moe_handle h, float* ms, int capacity, int* n_kernels, int* 
   *n_calls = done;
   prof_release(h);
   return st;
+}
+
+int moe_test_expire_waits(moe_handle h, int n_calls) {
+  if (!h || n_calls < 0) return MOE_ERR_INVALID_ARG;
+  if (h->q4 || !moe::decode_stream_fits(h->D, h->sms)) return MOE_ERR_UNSUPPORTED;
+  h->expire_calls = n_calls;
+  return MOE_OK;
 }
 
 int moe_destroy(moe_handle h) {

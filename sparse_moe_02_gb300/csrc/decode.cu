@@ -714,6 +714,8 @@ struct StreamArgs {
   DecodeWs dw;
   __nv_bfloat16* y;
   int* err;
+  int bar_extra;      // arrivals the grid barrier waits for beyond the launch's blocks (0)
+  uint64_t limit_ns;  // how long the grid barrier waits before it reports a timeout
 };
 
 // Shared-memory layout of a block: the ring, x (bf16), the down rows (up to nn = ceil(d / G)
@@ -1034,8 +1036,8 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
     while (true) {
       int v;
       asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.dw.gu_next) : "memory");
-      if (v >= G) break;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (v >= G + a.bar_extra) break;
+      if (global_timer_ns() - t0 > a.limit_ns) {
         atomicExch(a.err, kDevErrTimeout);
         s_fail = 1;
         break;
@@ -1161,8 +1163,11 @@ cudaError_t prepare_decode_stream_kernels() {
 
 cudaError_t launch_decode_stream(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
                                  int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
-                                 __nv_bfloat16* y, int* err, int sms, cudaStream_t s) {
-  StreamArgs a{x, W, D, topk_idx, topk_w, dw, y, err};
+                                 __nv_bfloat16* y, int* err, int sms, cudaStream_t s,
+                                 bool expire) {
+  // expire: one arrival more than the launch has, 1 ms limit (the barrier's timeout path)
+  StreamArgs a{x, W, D, topk_idx, topk_w, dw, y, err, expire ? 1 : 0,
+               expire ? 1000000ull : kWaitLimitNs};
   const int G = stream_grid(D, sms);
   return launch_pdl(dec_stream_kernel, dim3(G), dim3(kStThreads), st_layout(D, G).total, s, a);
 }

@@ -76,6 +76,7 @@ def test_calls_on_null_handle_are_rejected():
     assert moe.moe_forward_host(None, None, 1, None, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_route(None, None, 1, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_get_device_error(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_test_expire_waits(None, 1) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_destroy(None) == moe.MOE_OK
 
 

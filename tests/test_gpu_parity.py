@@ -188,16 +188,20 @@ def test_prefill_4096(skew):
         assert counts.max() > 1000 and (counts == 0).sum() > 0
     else:
         assert counts.min() > 64 and counts.max() < 256
-    toks = sample_tokens(c.T)
-    assert_close(got["y"][toks], oracle_outputs(c, toks), f"prefill skew={skew}")
+    assert_close(got["y"], oracle_outputs(c), f"prefill skew={skew} (all 4096 tokens)")
 
 
-@pytest.mark.parametrize("T", [256, 1024, 8192])
+# The prefill length sweep of the benchmark (T = 256 .. 128K at d = 2048, f = fs = 512,
+# balanced routing), in the launch configuration the benchmark times: expert ids, offsets and
+# the token permutation bit-exact against the oracle's routing of every token; outputs against
+# the oracle on every token up to T = 4096 and above on the first and last 64 tokens plus every
+# 17th (the oracle takes about 1.5 ms per token on 16 cores).
+@pytest.mark.parametrize("T", [256, 512, 1024, 2048, 8192, 16384, 32768, 65536, 131072])
 def test_prefill_sweep_sizes(T):
     c = build_case("sweep", d=2048, f=512, fs=512, T=T, seed=11, full_host=False)
     got = _run(c, moe.MOE_SCHEDULE_AUTO)
     _check_routing(c, got)
-    toks = sample_tokens(T, n_edge=16, stride=97)
+    toks = np.arange(T) if T <= 4096 else sample_tokens(T)
     assert_close(got["y"][toks], oracle_outputs(c, toks), f"sweep T={T}")
 
 

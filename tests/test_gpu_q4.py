@@ -72,14 +72,16 @@ def test_q4_prefill_matches_oracle(d, f, fs, T, seed, skew):
 @pytest.mark.parametrize("skew", [False, True], ids=["balanced", "skewed"])
 def test_q4_prefill_4096(skew):
     """The benchmark's prefill shape (T=4096, d=2048, f=fs=512) in the launch configuration
-    the benchmark times; outputs on sampled tokens."""
+    the benchmark times: the routing of every token bit-exact, outputs on every token."""
     c = build_case("q4-prefill-4096", d=2048, f=512, fs=512, T=4096, seed=0, skew=skew,
                    full_host=False)
     got = _run_q4(c)
-    toks = sample_tokens(c.T, n_edge=16, stride=67)
-    idx, w = oracle.select(oracle.router_logits_f32(c.x[toks], c.w_r, c.bias), c.dims.k)
-    assert np.array_equal(got["topk_idx"][toks], idx)
-    assert_close(got["y"][toks], oracle_outputs_q4(c, toks), f"q4 prefill 4096 skew={skew}")
+    ref = oracle.route(c.x, c.w_r, c.dims.k, c.bias)
+    assert np.array_equal(got["topk_idx"], ref["topk_idx"])
+    assert np.max(np.abs(got["topk_w"] - ref["topk_w"])) <= 1e-5
+    assert np.array_equal(got["offsets"], ref["offsets"])
+    assert np.array_equal(got["perm"], ref["perm"])
+    assert_close(got["y"], oracle_outputs_q4(c), f"q4 prefill 4096 skew={skew} (all tokens)")
 
 
 @pytest.mark.parametrize("d,f", [(8192, 512), (4096, 2048)])
