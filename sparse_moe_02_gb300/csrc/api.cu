@@ -479,6 +479,15 @@ int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {
                                                            h->rws.err, s, false))))
       return st;
     if ((st = prof_mark(h, s, 1))) return st;
+    if (moe::decode_stream_fits(h->D, h->sms, true)) {
+      // selection, gate/up and down with the combine in one launch (profiling slot 2 empty)
+      if ((st = cuda_status(moe::launch_decode_stream(xd, decode_weights(h), h->D,
+                                                      h->rws.topk_idx, h->rws.topk_w, h->dws, yd,
+                                                      h->rws.err, h->sms, s, false, &h->wq))))
+        return st;
+      if ((st = prof_mark(h, s, 2))) return st;
+      return prof_finish_call(h, s, 3);
+    }
     if ((st = cuda_status(moe::launch_decode_q4_gateup(xd, h->wq, h->D, h->rws.topk_idx,
                                                        h->rws.topk_w, h->dws, h->sms, s))))
       return st;

@@ -19,6 +19,7 @@
 #include "plan.cuh"
 #include "ptx.cuh"
 #include "select.cuh"
+#include "q4.cuh"
 
 namespace moe {
 namespace {
@@ -707,7 +708,8 @@ constexpr int kDownLead = 12;                  // gate/up items left when the do
 
 struct StreamArgs {
   const __nv_bfloat16* x;
-  DecodeWeights W;
+  DecodeWeights W;    // the router; the experts of a bf16 launch
+  Q4Weights Q;        // the experts of a 4-bit launch
   Dims D;
   int32_t* topk_idx;  // written by block 0 (the selection behind this forward)
   float* topk_w;
@@ -718,19 +720,39 @@ struct StreamArgs {
   uint64_t limit_ns;  // how long the grid barrier waits before it reports a timeout
 };
 
-// Shared-memory layout of a block: the ring, x (bf16), the down rows (up to nn = ceil(d / G)
-// outputs x (8 f + fs) bf16), h as two planes (see h_piece), the mbarriers.
+// Shared-memory layout of a block, in bytes: the ring (kStSlots slots of one feature's gate and
+// up rows, two per slot warp with 4-bit rows), x, the down rows of up to nn = ceil(d / G) outputs of the 8 experts and the shared
+// expert, h, the mbarriers.  bf16: x as bf16, h as two fp32 planes (see h_piece).  4-bit: a
+// slot holds the two rows' codes, then their scales and biases; x and h as swizzled fp32 with
+// their sums per 32 (see q4.cuh); the down rows as codes [9][nn][K/2], then scales, then biases
+// (K = f, or fs for the shared expert).  A 4-bit block is padded to more than half an SM's
+// shared memory, so that one block runs on every SM.
 struct StLayout {
-  uint32_t xs, rows, hp, bars, total;
+  uint32_t slot, xs, xsum, rows, sc, bi, hp, hsum, bars, total;
 };
+template <bool Q4>
 __host__ __device__ inline StLayout st_layout(const Dims& D, int G) {
   StLayout L;
   const int nn = (D.d + G - 1) / G;
-  L.xs = (uint32_t)kStSlots * 4 * D.d;
-  L.rows = L.xs + 2 * D.d;
-  L.hp = L.rows + round_up(nn * (8 * D.f + D.fs) * 2, 16);
-  L.bars = L.hp + 9 * D.hdim * 4;
-  L.total = L.bars + (kStSlots + 2) * 8;
+  if (!Q4) {
+    L.slot = 4 * D.d;
+    L.xs = kStSlots * L.slot;
+    L.xsum = L.rows = L.xs + 2 * D.d;
+    L.sc = L.bi = L.hp = L.rows + round_up(nn * (8 * D.f + D.fs) * 2, 16);
+    L.hsum = L.bars = L.hp + 9 * D.hdim * 4;
+  } else {
+    L.slot = D.d + D.d / 8;  // codes d/2 each, scales and biases d/32 bytes each
+    L.xs = 2 * kStSlots * L.slot;  // two slots per slot warp
+    L.xsum = L.xs + 4 * D.d;
+    L.rows = L.xsum + 4 * (D.d / 32);
+    L.sc = L.rows + nn * (8 * D.f + D.fs) / 2;
+    L.bi = L.sc + nn * (8 * D.f + D.fs) / 32;
+    L.hp = L.bi + nn * (8 * D.f + D.fs) / 32;
+    L.hsum = L.hp + 9 * D.hdim * 4;
+    L.bars = L.hsum + 9 * (D.hdim / 32) * 4;
+  }
+  L.total = L.bars + (2 * kStSlots + 2) * 8;
+  if (Q4 && L.total < 120 * 1024) L.total = 120 * 1024;
   return L;
 }
 
@@ -816,8 +838,80 @@ __device__ __forceinline__ void dn_combine_rows(const uint8_t* rows, const float
 }
 static_assert(kCbWarps == 8, "the combine pairs warps w and w + 4 (two halves of K)");
 
+// Stages v (n bf16 values, n a multiple of 32) as swizzled fp32 in vf and the sums of each 32 in
+// vs, by the nthreads threads of named barrier `bar` (thread index t); ends with that barrier.
+__device__ __forceinline__ void stage_f32_named(const __nv_bfloat16* src, float* vf, float* vs,
+                                                int n, int t, int nthreads, int bar) {
+  const uint4* s16 = reinterpret_cast<const uint4*>(src);
+  for (int m = t; m < n / 8; m += nthreads) {
+    const uint4 v = __ldcg(s16 + m);
+    *reinterpret_cast<float4*>(vf + swz(8 * m)) =
+        make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+    *reinterpret_cast<float4*>(vf + swz(8 * m + 4)) =
+        make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+  }
+  named_sync(bar, nthreads);
+  // a piece's 32 values are its 32 slots in some order: summed in slot order
+  for (int p = t; p < n / 32; p += nthreads) {
+    const float4* q = reinterpret_cast<const float4*>(vf + 32 * p);
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 u = q[i];
+      sum += u.x;
+      sum += u.y;
+      sum += u.z;
+      sum += u.w;
+    }
+    vs[p] = sum;
+  }
+  named_sync(bar, nthreads);
+}
+
+__device__ __forceinline__ float bf16_at(const uint8_t* p) {
+  return __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(p) << 16);
+}
+
+// The 4-bit combine: out[i] for i < nn (nn <= 16) over the rows in shared memory (layout in
+// st_layout) and h (swizzled rows at hf + j hdim, sums per 32 at hs + j hdim / 32).  Combine warp
+// cw takes outputs cw and cw + 8; lane l the pieces P = l, l + 32, ... of the nine rows of an
+// output taken as one run (P < 8 f / 32: routed row j = P / (f / 32); then the shared row),
+// summing w_j (scale * codes . h_j + bias * sum h_j) into four partial sums (P / 32 mod 4, each
+// in run order); one warp reduction per output.
+__device__ __forceinline__ void dn_combine_q4(const uint8_t* codes, const uint8_t* sc,
+                                              const uint8_t* bi, const float* hf, const float* hs,
+                                              int nn, int f, int fs, int hdim, const float* w,
+                                              __nv_bfloat16* out, int cw, int lane) {
+  const int npr = f / 32, nps = fs / 32, npt = 8 * npr + nps;
+  for (int i = cw; i < nn; i += kCbWarps) {
+    float accs[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums (P / 32 mod 4)
+    for (int P0 = lane; P0 < npt; P0 += 128) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int P = P0 + 32 * q;
+        if (P >= npt) break;
+        const int j = P < 8 * npr ? P / npr : 8, p = P - j * npr;
+        // the row's codes and its scales / biases (bytes) in their regions
+        const size_t cbase = j < 8 ? ((size_t)j * nn + i) * (f / 2)
+                                   : (size_t)8 * nn * (f / 2) + (size_t)i * (fs / 2);
+        const size_t gbase = j < 8 ? ((size_t)j * nn + i) * (f / 32)
+                                   : (size_t)8 * nn * (f / 32) + (size_t)i * (fs / 32);
+        const uint4 c = *reinterpret_cast<const uint4*>(codes + cbase + (size_t)p * 16);
+        const float s = bf16_at(sc + gbase + (p / 2) * 2), b = bf16_at(bi + gbase + (p / 2) * 2);
+        const float t =
+            s * q4_dot32(c, hf + (size_t)j * hdim, p) + b * hs[(size_t)j * (hdim / 32) + p];
+        accs[q] = fmaf(j < 8 ? w[j] : 1.0f, t, accs[q]);
+      }
+    }
+    const float acc = warp_sum((accs[0] + accs[1]) + (accs[2] + accs[3]));
+    if (lane == 0) out[i] = __float2bfloat16_rn(acc);
+  }
+}
+
 // At most 168 registers: beside a router block (256 x 64 registers) on the same SM.
+template <bool Q4>
 __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
+  constexpr int kSpw = Q4 ? 2 : 1;  // ring slots per slot warp (items in flight per warp)
   extern __shared__ __align__(128) uint8_t ssm[];
   __shared__ int s_ids[kTopK];
   __shared__ float s_w[kTopK];
@@ -827,18 +921,21 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
   __shared__ int s_next;    // next gate/up item to hand out (items 0..7: one per slot warp)
   const int d = a.D.d, f = a.D.f, fs = a.D.fs, hdim = a.D.hdim, nch = d / 8;
   const int G = gridDim.x, b = blockIdx.x;
-  const StLayout Ly = st_layout(a.D, G);
-  const uint32_t row_bytes = (uint32_t)d * 2, slot_bytes = 2 * row_bytes;
+  const StLayout Ly = st_layout<Q4>(a.D, G);
+  const uint32_t slot_bytes = Ly.slot;
+  const uint32_t row_bytes = Q4 ? (uint32_t)d / 2 : (uint32_t)d * 2;  // codes / bf16 of a row
+  const uint32_t grp_bytes = (uint32_t)d / 32;                        // a 4-bit row's scales
   uint8_t* ring = ssm;
-  uint4* xs = reinterpret_cast<uint4*>(ssm + Ly.xs);
   uint8_t* rows = ssm + Ly.rows;
   float* hs = reinterpret_cast<float*>(ssm + Ly.hp);
   uint64_t* full = reinterpret_cast<uint64_t*>(ssm + Ly.bars);
-  uint64_t* sel_ready = full + kStSlots;  // s_ids holds this forward's selection
+  uint64_t* sel_ready = full + kStSlots * kSpw;  // s_ids holds this forward's selection
   uint64_t* dbar = sel_ready + 1;         // the down rows have landed
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = (int)((long long)b * d / G), nn = (int)((long long)(b + 1) * d / G) - n0;
-  const uint32_t rb = (uint32_t)f * 2, srb = (uint32_t)fs * 2;
+  // bytes per down row: bf16 rows, or codes (then scales and biases in their own regions)
+  const uint32_t rb = Q4 ? (uint32_t)f / 2 : (uint32_t)f * 2;
+  const uint32_t srb = Q4 ? (uint32_t)fs / 2 : (uint32_t)fs * 2;
   // this block's gate/up items: the shared expert's features b, b + G, ..., then the routed
   // features r = j f + c (j: rank of the expert in ascending id) b, b + G, ...: at any moment
   // the blocks together request consecutive rows, a few sequential sweeps for DRAM
@@ -846,23 +943,44 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
   const int nr = kTopK * f;
   const int nitems = ns + (nr > b ? (nr - b + G - 1) / G : 0);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStSlots; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kStSlots * kSpw; ++i) mbar_init(&full[i], 1);
     mbar_init(sel_ready, 1);
     mbar_init(dbar, 1);
     s_fail = 0;
     s_issued = 0;
-    s_next = kStSlots;
+    s_next = kStSlots * kSpw;
     fence_mbar_init();
   }
   __syncthreads();
   pdl_trigger();  // the next layer's router may request its rows (it waits for this launch)
   const uint64_t pol = policy_evict_first();  // every weight row is read once
 
+  // down rows of expert rank j (j = 8: the shared expert) into shared memory, completing on dbar
+  auto copy_down = [&](int j, int e) {
+    if (!Q4) {
+      const __nv_bfloat16* src = j < 8 ? a.W.w_down + ((size_t)e * d + n0) * f
+                                       : a.W.ws_down + (size_t)n0 * fs;
+      bulk_load(rows + (j < 8 ? j * nn * rb : 8 * nn * rb), src, nn * (j < 8 ? rb : srb), dbar,
+                pol);
+    } else {
+      const Q4Matrix& m = j < 8 ? a.Q.down : a.Q.s_down;
+      const int K = j < 8 ? f : fs;
+      const size_t r0 = j < 8 ? (size_t)e * d + n0 : (size_t)n0;
+      const uint32_t coff = j < 8 ? j * nn * (f / 2) : 8 * nn * (f / 2);
+      const uint32_t goff = j < 8 ? j * nn * (f / 32) : 8 * nn * (f / 32);
+      bulk_load(rows + coff, m.codes + r0 * (K / 2), nn * (K / 2), dbar, pol);
+      bulk_load(ssm + Ly.sc + goff, m.scales + r0 * (K / 64), nn * (K / 32), dbar, pol);
+      bulk_load(ssm + Ly.bi + goff, m.biases + r0 * (K / 64), nn * (K / 32), dbar, pol);
+    }
+  };
+
   if (warp == 0) {
     // ---- selection and the down rows
     if (lane == 0) {
-      mbar_arrive_expect_tx(dbar, (uint32_t)nn * (8 * rb + srb));
-      bulk_load(rows + 8 * nn * rb, a.W.ws_down + (size_t)n0 * fs, nn * srb, dbar, pol);
+      const uint32_t down_bytes =
+          Q4 ? (uint32_t)nn * (8 * f + fs) * 9 / 16 : (uint32_t)nn * (8 * rb + srb);
+      mbar_arrive_expect_tx(dbar, down_bytes);
+      copy_down(8, 0);
     }
     pdl_wait();  // the router's logits (and x) are final
     named_arrive(2, kStThreads);  // releases the slot warps (parked on the same barrier)
@@ -883,34 +1001,51 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
         __nanosleep(256);
     }
     __syncwarp();
-    if (lane < kTopK)
-      bulk_load(rows + lane * nn * rb, a.W.w_down + ((size_t)s_ids[lane] * d + n0) * f, nn * rb,
-                dbar, pol);
+    if (lane < kTopK) copy_down(lane, s_ids[lane]);
     if (b == 0 && lane < kTopK) {
       a.topk_idx[lane] = s_ids[lane];
       a.topk_w[lane] = s_w[lane];
     }
   } else {
-    // ---- slot warp s: items s, s + 8, ..., each refilled by its own warp as soon as the warp
-    // has read the previous one
-    const int s = warp - 1;
-    auto item_rows = [&](int k, const __nv_bfloat16*& g, const __nv_bfloat16*& u) {
+    // ---- slot warp w (warp - 1) owns slots w * kSpw .. w * kSpw + kSpw - 1 (kSpw items in
+    // flight per warp) and takes the block's next item whenever one of its slots is free
+    const int w = warp - 1;
+    // the expert row of item k (a routed item needs the selection): feature row index in
+    // matrix gate/up of expert e (e < 0: the shared expert)
+    auto item_row = [&](int k, int& e, size_t& r) {
       if (k < ns) {
-        g = a.W.ws_gate + (size_t)(b + k * G) * d;
-        u = a.W.ws_up + (size_t)(b + k * G) * d;
+        e = -1;
+        r = (size_t)(b + k * G);
       } else {
-        const int r = b + (k - ns) * G, j = r / f;
-        const size_t row = ((size_t)s_ids[j] * f + (r - j * f)) * d;
-        g = a.W.w_gate + row;
-        u = a.W.w_up + row;
+        const int rr = b + (k - ns) * G, j = rr / f;
+        e = s_ids[j];
+        r = (size_t)e * f + (rr - j * f);
       }
     };
-    auto issue = [&](int k) {  // lane 0; a routed item needs the selection
-      const __nv_bfloat16 *g, *u;
-      item_rows(k, g, u);
-      mbar_arrive_expect_tx(&full[s], slot_bytes);
-      bulk_load(ring + s * slot_bytes, g, row_bytes, &full[s], pol);
-      bulk_load(ring + s * slot_bytes + row_bytes, u, row_bytes, &full[s], pol);
+    auto issue = [&](int k, int sl_i) {  // lane 0: item k into slot sl_i
+      int e;
+      size_t r;
+      item_row(k, e, r);
+      uint8_t* sl = ring + sl_i * slot_bytes;
+      uint64_t* fb = &full[sl_i];
+      mbar_arrive_expect_tx(fb, slot_bytes);
+      if (!Q4) {
+        const __nv_bfloat16* g = (e < 0 ? a.W.ws_gate : a.W.w_gate) + r * d;
+        const __nv_bfloat16* u = (e < 0 ? a.W.ws_up : a.W.w_up) + r * d;
+        bulk_load(sl, g, row_bytes, fb, pol);
+        bulk_load(sl + row_bytes, u, row_bytes, fb, pol);
+      } else {
+        const Q4Matrix& mg = e < 0 ? a.Q.s_gate : a.Q.gate;
+        const Q4Matrix& mu = e < 0 ? a.Q.s_up : a.Q.up;
+        bulk_load(sl, mg.codes + r * (d / 2), row_bytes, fb, pol);
+        bulk_load(sl + row_bytes, mu.codes + r * (d / 2), row_bytes, fb, pol);
+        bulk_load(sl + 2 * row_bytes, mg.scales + r * (d / 64), grp_bytes, fb, pol);
+        bulk_load(sl + 2 * row_bytes + grp_bytes, mg.biases + r * (d / 64), grp_bytes, fb, pol);
+        bulk_load(sl + 2 * row_bytes + 2 * grp_bytes, mu.scales + r * (d / 64), grp_bytes, fb,
+                  pol);
+        bulk_load(sl + 2 * row_bytes + 3 * grp_bytes, mu.biases + r * (d / 64), grp_bytes, fb,
+                  pol);
+      }
       atomicAdd(&s_issued, 1);
     };
     bool sel = false;  // lane 0 has seen the selection
@@ -918,110 +1053,181 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
       if (!sel) sel = mbar_wait(sel_ready, 0, a.err);
       return sel;
     };
-    int k = s, u = 0;
-    if (lane == 0 && k < ns) issue(k);  // a shared feature: before the router has finished
-    named_sync(2, kStThreads);          // warp 0 has passed its wait: x is final
-    const uint4* xsrc = reinterpret_cast<const uint4*>(a.x);
-    for (int i = threadIdx.x - 32; i < nch; i += kStThreads - 32) xs[i] = __ldcg(xsrc + i);
-    named_sync(1, kStThreads - 32);
+    // slot t of this warp starts with item w + kStSlots * t (shared features before the
+    // router has finished); later items come from s_next, in index order
+    int kk[kSpw], uu[kSpw];
+#pragma unroll
+    for (int t = 0; t < kSpw; ++t) {
+      kk[t] = w + kStSlots * t;
+      uu[t] = 0;
+      if (lane == 0 && kk[t] < ns) issue(kk[t], w * kSpw + t);
+    }
+    named_sync(2, kStThreads);  // warp 0 has passed its wait: x is final
+    if (!Q4) {
+      const uint4* xsrc = reinterpret_cast<const uint4*>(a.x);
+      uint4* xs = reinterpret_cast<uint4*>(ssm + Ly.xs);
+      for (int i = threadIdx.x - 32; i < nch; i += kStThreads - 32) xs[i] = __ldcg(xsrc + i);
+      named_sync(1, kStThreads - 32);
+    } else {
+      stage_f32_named(a.x, reinterpret_cast<float*>(ssm + Ly.xs),
+                      reinterpret_cast<float*>(ssm + Ly.xsum), d, threadIdx.x - 32,
+                      kStThreads - 32, 1);
+    }
     bool ok = true;
-    if (lane == 0 && k >= ns && k < nitems) {
-      ok = ensure_sel();
-      if (ok) issue(k);
-    }
+#pragma unroll
+    for (int t = 0; t < kSpw; ++t)
+      if (lane == 0 && kk[t] >= ns && kk[t] < nitems) {
+        ok = ok && ensure_sel();
+        if (ok) issue(kk[t], w * kSpw + t);
+      }
     ok = __all_sync(0xffffffffu, ok);
-    // the rows of item kk requested into L2, one 128-byte line per lane and request (lane 0
-    // has seen the selection if kk is routed); each warp keeps the two items after the one in
-    // its slot requested, about 190 KB per SM in flight: HBM needs about 20 MB in flight over
-    // the chip to run at full rate, far more than the ring holds, and the requests still come
-    // back roughly in the order the slots consume them
-    auto prefetch_item = [&](int kk) {
-      const __nv_bfloat16 *g, *uu;
-      item_rows(kk, g, uu);
-      for (uint32_t o = lane * 128u; o < row_bytes; o += 32 * 128u) {
-        prefetch_l2_line(reinterpret_cast<const char*>(g) + o);
-        prefetch_l2_line(reinterpret_cast<const char*>(uu) + o);
-      }
-    };
-    bool selw = false;  // the whole warp has seen the selection
-    auto prefetch_ahead = [&](int kk) {
-      if (kk >= nitems) return;
-      if (kk >= ns && !selw) selw = __all_sync(0xffffffffu, mbar_wait(sel_ready, 0, a.err));
-      if (kk < ns || selw) prefetch_item(kk);
-    };
-    // items are handed out in index order (each slot warp takes the next one when its slot is
-    // free); item i is requested into L2 when item i - 16 is handed out, items 8 .. 23 here
-    if (ok) {
-      prefetch_ahead(k + kStSlots);
-      prefetch_ahead(k + 2 * kStSlots);
+    if (!ok) {
+#pragma unroll
+      for (int t = 0; t < kSpw; ++t) kk[t] = nitems;  // (the shared items' copies are drained below)
     }
-    int kn = 0;  // lane 0: the item this warp takes next
-    const uint4* gr = reinterpret_cast<const uint4*>(ring + s * slot_bytes);
-    const uint4* ur = gr + nch;
-    for (; ok && k < nitems; ++u, k = __shfl_sync(0xffffffffu, kn, 0)) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&full[s], u & 1, a.err))) {
-        ok = false;
-        break;
-      }
-      float g0 = 0.f, g1 = 0.f, v0 = 0.f, v1 = 0.f;
-#pragma unroll 4
-      for (int c = lane; c < nch; c += 32) {
-        const uint4 xv = xs[c], wg = gr[c], wu = ur[c];
-        const float x0 = bf16_lo(xv.x), x1 = bf16_hi(xv.x), x2 = bf16_lo(xv.y), x3 = bf16_hi(xv.y);
-        const float x4 = bf16_lo(xv.z), x5 = bf16_hi(xv.z), x6 = bf16_lo(xv.w), x7 = bf16_hi(xv.w);
-        g0 = fmaf(bf16_lo(wg.x), x0, g0);
-        g1 = fmaf(bf16_hi(wg.x), x1, g1);
-        v0 = fmaf(bf16_lo(wu.x), x0, v0);
-        v1 = fmaf(bf16_hi(wu.x), x1, v1);
-        g0 = fmaf(bf16_lo(wg.y), x2, g0);
-        g1 = fmaf(bf16_hi(wg.y), x3, g1);
-        v0 = fmaf(bf16_lo(wu.y), x2, v0);
-        v1 = fmaf(bf16_hi(wu.y), x3, v1);
-        g0 = fmaf(bf16_lo(wg.z), x4, g0);
-        g1 = fmaf(bf16_hi(wg.z), x5, g1);
-        v0 = fmaf(bf16_lo(wu.z), x4, v0);
-        v1 = fmaf(bf16_hi(wu.z), x5, v1);
-        g0 = fmaf(bf16_lo(wg.w), x6, g0);
-        g1 = fmaf(bf16_hi(wg.w), x7, g1);
-        v0 = fmaf(bf16_lo(wu.w), x6, v0);
-        v1 = fmaf(bf16_hi(wu.w), x7, v1);
-      }
-      const float g = warp_sum(g0 + g1), v = warp_sum(v0 + v1);
-      __syncwarp();  // every lane has read the slot: refill it
-      if (lane == 0) kn = atomicAdd(&s_next, 1);
-      prefetch_ahead(__shfl_sync(0xffffffffu, kn, 0) + 2 * kStSlots);
-      bool issued = true;
-      if (lane == 0 && kn < nitems) {
-        if (kn < ns || ensure_sel()) issue(kn);
-        else issued = false;
-      }
-      if (lane == 0) {
-        int hidx;
-        if (k < ns) {
-          hidx = 8 * hdim + b + k * G;
-        } else {
-          const int r = b + (k - ns) * G, j = r / f;
-          hidx = j * hdim + (r - j * f);
+    // the rows of item i requested into L2, one 128-byte line per lane and request (the warp has
+    // seen the selection if i is routed); items are handed out in index order, item i is
+    // requested when item i - 2 R (R = kStSlots kSpw, the items in flight in the ring) is
+    // handed out, items R .. 3R - 1 here: with bf16 rows about 190 KB per SM in flight -- HBM
+    // needs about 20 MB in flight over the chip to run at full rate, far more than the ring
+    // holds -- and the requests come back roughly in the order the slots consume them
+    constexpr int kRing = kStSlots * kSpw;
+    bool selw = false;  // the whole warp has seen the selection
+    auto prefetch_ahead = [&](int i) {
+      if (i >= nitems) return;
+      if (i >= ns && !selw) selw = __all_sync(0xffffffffu, mbar_wait(sel_ready, 0, a.err));
+      if (i >= ns && !selw) return;
+      int e;
+      size_t r;
+      item_row(i, e, r);
+      if (!Q4) {
+        const char* g = reinterpret_cast<const char*>((e < 0 ? a.W.ws_gate : a.W.w_gate) + r * d);
+        const char* uq = reinterpret_cast<const char*>((e < 0 ? a.W.ws_up : a.W.w_up) + r * d);
+        for (uint32_t o = lane * 128u; o < row_bytes; o += 32 * 128u) {
+          prefetch_l2_line(g + o);
+          prefetch_l2_line(uq + o);
         }
-        a.dw.hdec[hidx] = silu_mul(g, v);
+      } else {
+        const Q4Matrix& mg = e < 0 ? a.Q.s_gate : a.Q.gate;
+        const Q4Matrix& mu = e < 0 ? a.Q.s_up : a.Q.up;
+        for (uint32_t o = lane * 128u; o < row_bytes; o += 32 * 128u) {
+          prefetch_l2_line(mg.codes + r * (d / 2) + o);
+          prefetch_l2_line(mu.codes + r * (d / 2) + o);
+        }
+        if (lane < 4) {
+          const Q4Matrix& m = lane & 1 ? mu : mg;
+          prefetch_l2_line((lane & 2 ? m.biases : m.scales) + r * (d / 64));
+        }
       }
-      if (!__all_sync(0xffffffffu, issued)) {
-        ok = false;
-        ++u;  // the slot holds no copy in flight
-        k = nitems;
-        break;
-      }
-      if (__shfl_sync(0xffffffffu, kn, 0) >= nitems) {
-        ++u;
-        k = nitems;
-        break;
+    };
+    if (ok)
+      for (int t = kSpw; t < 3 * kSpw; ++t) prefetch_ahead(w + kStSlots * t);
+    bool any = true;
+    while (ok && any) {
+      any = false;
+#pragma unroll
+      for (int t = 0; t < kSpw; ++t) {
+        if (!ok || kk[t] >= nitems) continue;
+        any = true;
+        const int si = w * kSpw + t, k = kk[t];
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[si], uu[t] & 1, a.err))) {
+          ok = false;
+          break;
+        }
+        const uint8_t* sl = ring + si * slot_bytes;
+        float gsum, vsum;
+        if (!Q4) {
+          const uint4* gr = reinterpret_cast<const uint4*>(sl);
+          const uint4* ur = gr + nch;
+          const uint4* xs = reinterpret_cast<const uint4*>(ssm + Ly.xs);
+          float g0 = 0.f, g1 = 0.f, v0 = 0.f, v1 = 0.f;
+#pragma unroll 4
+          for (int c = lane; c < nch; c += 32) {
+            const uint4 xv = xs[c], wg = gr[c], wu = ur[c];
+            const float x0 = bf16_lo(xv.x), x1 = bf16_hi(xv.x), x2 = bf16_lo(xv.y),
+                        x3 = bf16_hi(xv.y);
+            const float x4 = bf16_lo(xv.z), x5 = bf16_hi(xv.z), x6 = bf16_lo(xv.w),
+                        x7 = bf16_hi(xv.w);
+            g0 = fmaf(bf16_lo(wg.x), x0, g0);
+            g1 = fmaf(bf16_hi(wg.x), x1, g1);
+            v0 = fmaf(bf16_lo(wu.x), x0, v0);
+            v1 = fmaf(bf16_hi(wu.x), x1, v1);
+            g0 = fmaf(bf16_lo(wg.y), x2, g0);
+            g1 = fmaf(bf16_hi(wg.y), x3, g1);
+            v0 = fmaf(bf16_lo(wu.y), x2, v0);
+            v1 = fmaf(bf16_hi(wu.y), x3, v1);
+            g0 = fmaf(bf16_lo(wg.z), x4, g0);
+            g1 = fmaf(bf16_hi(wg.z), x5, g1);
+            v0 = fmaf(bf16_lo(wu.z), x4, v0);
+            v1 = fmaf(bf16_hi(wu.z), x5, v1);
+            g0 = fmaf(bf16_lo(wg.w), x6, g0);
+            g1 = fmaf(bf16_hi(wg.w), x7, g1);
+            v0 = fmaf(bf16_lo(wu.w), x6, v0);
+            v1 = fmaf(bf16_hi(wu.w), x7, v1);
+          }
+          gsum = g0 + g1;
+          vsum = v0 + v1;
+        } else {
+          // per piece of 32 inputs: scale * codes . x + bias * sum x
+          const float* xf = reinterpret_cast<const float*>(ssm + Ly.xs);
+          const float* xsum = reinterpret_cast<const float*>(ssm + Ly.xsum);
+          const uint8_t* gs = sl + 2 * row_bytes;
+          float gp[2] = {0.f, 0.f}, vp[2] = {0.f, 0.f};  // independent per piece parity
+          for (int p0 = lane; p0 < d / 32; p0 += 64) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int p = p0 + 32 * h;
+              if (p < d / 32) {
+                const uint4 cg = *reinterpret_cast<const uint4*>(sl + (size_t)p * 16);
+                const uint4 cu = *reinterpret_cast<const uint4*>(sl + row_bytes + (size_t)p * 16);
+                const float xp = xsum[p];
+                gp[h] += bf16_at(gs + (p / 2) * 2) * q4_dot32(cg, xf, p) +
+                         bf16_at(gs + grp_bytes + (p / 2) * 2) * xp;
+                vp[h] += bf16_at(gs + 2 * grp_bytes + (p / 2) * 2) * q4_dot32(cu, xf, p) +
+                         bf16_at(gs + 3 * grp_bytes + (p / 2) * 2) * xp;
+              }
+            }
+          }
+          gsum = gp[0] + gp[1];
+          vsum = vp[0] + vp[1];
+        }
+        const float g = warp_sum(gsum), v = warp_sum(vsum);
+        __syncwarp();  // every lane has read the slot: refill it
+        int kn = 0;
+        if (lane == 0) kn = atomicAdd(&s_next, 1);
+        kn = __shfl_sync(0xffffffffu, kn, 0);
+        prefetch_ahead(kn + 2 * kRing);
+        bool issued = true;
+        if (lane == 0 && kn < nitems) {
+          if (kn < ns || ensure_sel()) issue(kn, si);
+          else issued = false;
+        }
+        if (lane == 0) {
+          int hidx;
+          if (k < ns) {
+            hidx = 8 * hdim + b + k * G;
+          } else {
+            const int rr = b + (k - ns) * G, j = rr / f;
+            hidx = j * hdim + (rr - j * f);
+          }
+          a.dw.hdec[hidx] = silu_mul(g, v);
+        }
+        ++uu[t];
+        kk[t] = kn;
+        if (!__all_sync(0xffffffffu, issued)) {
+          ok = false;
+          kk[t] = nitems;  // nothing in flight in this slot
+          break;
+        }
       }
     }
     if (!ok) {
-      // after a timeout: the slot's copy, if one is in flight, gets another bounded chance to
+      // after a timeout: each slot's copy, if one is in flight, gets another bounded chance to
       // land before the block can leave; the block still takes part in every barrier below
       if (lane == 0) {
-        if (k < nitems) mbar_wait(&full[s], u & 1, a.err);
+#pragma unroll
+        for (int t = 0; t < kSpw; ++t)
+          if (kk[t] < nitems) mbar_wait(&full[w * kSpw + t], uu[t] & 1, a.err);
         s_fail = 1;
       }
     }
@@ -1046,7 +1252,6 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
   }
   __syncthreads();
   {
-    // float4 q of h (expert rank q / (hdim / 4)) goes to plane q % 2, piece (q % (hdim / 4)) / 2
     const float4* src = reinterpret_cast<const float4*>(a.dw.hdec);
     float4* dst = reinterpret_cast<float4*>(hs);
     const int n4 = 9 * hdim / 4, per = hdim / 4;
@@ -1058,8 +1263,33 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int q = base + i * kStThreads;
-        if (q < n4) dst[(q & 1) * (n4 / 2) + (q / per) * (per / 2) + (q % per) / 2] = v[i];
+        if (q >= n4) continue;
+        if (!Q4) {
+          // float4 q of h (expert rank q / (hdim / 4)) goes to plane q % 2, piece (q % per) / 2
+          dst[(q & 1) * (n4 / 2) + (q / per) * (per / 2) + (q % per) / 2] = v[i];
+        } else {
+          // each row h_j swizzled on its own (the swizzle moves float4 groups whole)
+          const int j = q / per, c = (q - j * per) * 4;
+          *reinterpret_cast<float4*>(hs + j * hdim + swz(c)) = v[i];
+        }
       }
+    }
+  }
+  if (Q4) {
+    __syncthreads();
+    float* hsum = reinterpret_cast<float*>(ssm + Ly.hsum);
+    for (int q = threadIdx.x; q < 9 * (hdim / 32); q += kStThreads) {
+      const float4* t4 = reinterpret_cast<const float4*>(hs + 32 * q);
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 t = t4[i];
+        sum += t.x;
+        sum += t.y;
+        sum += t.z;
+        sum += t.w;
+      }
+      hsum[q] = sum;
     }
   }
   if (warp == 0) {
@@ -1070,8 +1300,12 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
   }
   __syncthreads();
   if (s_fail || warp == 0) return;
-  dn_combine_rows(rows, reinterpret_cast<const float4*>(hs), nn, f, fs, hdim, s_w, s_part,
-                  a.y + n0, warp - 1, threadIdx.x - 32);
+  if (!Q4)
+    dn_combine_rows(rows, reinterpret_cast<const float4*>(hs), nn, f, fs, hdim, s_w, s_part,
+                    a.y + n0, warp - 1, threadIdx.x - 32);
+  else
+    dn_combine_q4(rows, ssm + Ly.sc, ssm + Ly.bi, hs, reinterpret_cast<const float*>(ssm + Ly.hsum),
+                  nn, f, fs, hdim, s_w, a.y + n0, warp - 1, lane);
 }
 
 }  // namespace
@@ -1138,38 +1372,47 @@ namespace {
 int stream_grid(const Dims& D, int sms) { return D.d < sms ? D.d : sms; }
 }  // namespace
 
-bool decode_stream_fits(const Dims& D, int sms) {
+bool decode_stream_fits(const Dims& D, int sms, bool q4) {
   const int G = stream_grid(D, sms);
-  return D.d <= kStreamMaxD && (D.d + G - 1) / G <= kStMaxOut &&
-         st_layout(D, G).total <= (uint32_t)kStreamMaxSmem;
+  if (D.d > kStreamMaxD || (D.d + G - 1) / G > kStMaxOut) return false;
+  // 4-bit: a row's scales (K / 64 bf16) must fill whole 16-byte pieces for the bulk copies
+  if (q4) return D.d % 512 == 0 && D.f % 512 == 0 && D.fs % 512 == 0 &&
+                 st_layout<true>(D, G).total <= (uint32_t)kStreamMaxSmem;
+  return st_layout<false>(D, G).total <= (uint32_t)kStreamMaxSmem;
 }
 
 cudaError_t prepare_decode_stream_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(dec_stream_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kStreamMaxSmem);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   // an SM's split between L1 and shared memory is set when a block starts on an idle SM: both
   // launches of a layer ask for the largest shared memory, so that the next layer's router
   // block fits beside a streaming block
-  const void* ks[2] = {reinterpret_cast<const void*>(dec_stream_kernel),
+  const void* ks[3] = {reinterpret_cast<const void*>(dec_stream_kernel<false>),
+                       reinterpret_cast<const void*>(dec_stream_kernel<true>),
                        reinterpret_cast<const void*>(dec_router_shared_kernel<false>)};
-  for (const void* k : ks)
-    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+  for (int i = 0; i < 3; ++i) {
+    if (i < 2 && (e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kStreamMaxSmem)) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(ks[i], cudaFuncAttributePreferredSharedMemoryCarveout,
                                   cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
       return e;
+  }
   return cudaSuccess;
 }
 
 cudaError_t launch_decode_stream(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
                                  int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
                                  __nv_bfloat16* y, int* err, int sms, cudaStream_t s,
-                                 bool expire) {
+                                 bool expire, const Q4Weights* q4) {
   // expire: one arrival more than the launch has, 1 ms limit (the barrier's timeout path)
-  StreamArgs a{x, W, D, topk_idx, topk_w, dw, y, err, expire ? 1 : 0,
+  StreamArgs a{x, W, q4 ? *q4 : Q4Weights{}, D, topk_idx, topk_w, dw, y, err, expire ? 1 : 0,
                expire ? 1000000ull : kWaitLimitNs};
   const int G = stream_grid(D, sms);
-  return launch_pdl(dec_stream_kernel, dim3(G), dim3(kStThreads), st_layout(D, G).total, s, a);
+  if (q4)
+    return launch_pdl(dec_stream_kernel<true>, dim3(G), dim3(kStThreads),
+                      st_layout<true>(D, G).total, s, a);
+  return launch_pdl(dec_stream_kernel<false>, dim3(G), dim3(kStThreads),
+                    st_layout<false>(D, G).total, s, a);
 }
 
 // ---- small batches

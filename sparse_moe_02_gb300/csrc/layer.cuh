@@ -166,7 +166,7 @@ struct DecodeWeights {
 // (launch_decode_gateup, launch_decode_down_combine).
 constexpr int kStreamMaxD = 2048;
 constexpr int kStreamMaxSmem = 218 * 1024;  // leaves room for a router block on the same SM
-bool decode_stream_fits(const Dims& D, int sms);
+bool decode_stream_fits(const Dims& D, int sms, bool q4 = false);
 cudaError_t prepare_decode_stream_kernels();
 // expire: the launch's grid barrier waits for one arrival more than there are blocks, for
 // 1 ms, then records MOE_ERR_TIMEOUT and the blocks leave without combining (the test of the
@@ -174,7 +174,7 @@ cudaError_t prepare_decode_stream_kernels();
 cudaError_t launch_decode_stream(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
                                  int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
                                  __nv_bfloat16* y, int* err, int sms, cudaStream_t s,
-                                 bool expire = false);
+                                 bool expire = false, const Q4Weights* q4 = nullptr);
 
 // Router GEMV (logits) and the shared expert's gate/up GEMV, one launch.  When topk_idx is
 // not NULL (routing requested) the last router block to finish also writes the top 8.
