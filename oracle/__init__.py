@@ -1,8 +1,10 @@
-"""CPU oracle of the MoE FFN layer -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracles of the MoE FFN layer and of the Gated DeltaNet recurrent scan -- TEST
+INFRASTRUCTURE ONLY.
 
 Only the tests, the smoke check and the CPU-baseline timing leg of the benchmark use this
 package; the product library and its Python binding never import it.  The arithmetic lives in
-moe_oracle.cpp (plain loops, fp32 over bf16 inputs); this module marshals numpy arrays and
+moe_oracle.cpp (plain loops, fp32 over bf16 inputs) and gdn_oracle.cpp (the scan, fp64); this
+module marshals numpy arrays and
 implements the input-drawing rule that keeps routing decisions well separated:
 
   a token is kept only if the gap between its k-th and (k+1)-th largest router logit,
@@ -52,7 +54,8 @@ def lib():
         L.oracle_forward_q4.argtypes = [ctypes.POINTER(_Dims), _P, _I64, _P, _P, _P, _P, _P,
                                         ctypes.POINTER(_Q4), ctypes.POINTER(_Q4),
                                         ctypes.POINTER(_Q4), _P, _I64, _P, _P, _P, _I]
-        for fn in ("oracle_router_logits_f64", "oracle_router_logits_f32", "oracle_select",
+        L.oracle_gdn_scan.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _P, _P, _I]
+        for fn in ("oracle_gdn_scan", "oracle_router_logits_f64", "oracle_router_logits_f32", "oracle_select",
                    "oracle_route_structure", "oracle_expert_ffn", "oracle_forward",
                    "oracle_dequant_q4", "oracle_forward_q4"):
             getattr(L, fn).restype = _I
@@ -270,3 +273,25 @@ def draw_x_with_gap(seed, layer, T, d, routers, k, min_gap=1e-3, max_rounds=64):
             x[t] = synth.normal_bf16(seed, synth.stream_id(synth.X, layer, int(rounds[t])),
                                      int(t) * d, d, synth.SIGMA_X)
     raise RuntimeError("gap rule not met after max_rounds redraws")
+
+
+def gdn_scan(q, k, v, alpha, beta, s0=None, nthreads=None):
+    """Gated DeltaNet scan (gdn_oracle.h): q, k [T][H][dk] and v [T][H][dv] bf16 bits, alpha,
+    beta [T][H] fp32, s0 [H][dk][dv] fp32 or None (zeros).  Returns (o [T][H][dv], s [H][dk][dv])
+    in fp64."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    assert k.shape == (T, H, dk) and v.shape == (T, H, dv)
+    alpha = np.ascontiguousarray(alpha, dtype=np.float32)
+    beta = np.ascontiguousarray(beta, dtype=np.float32)
+    assert alpha.shape == (T, H) and beta.shape == (T, H)
+    if s0 is not None:
+        s0 = np.ascontiguousarray(s0, dtype=np.float32)
+        assert s0.shape == (H, dk, dv)
+    o = np.empty((T, H, dv), dtype=np.float64)
+    s = np.empty((H, dk, dv), dtype=np.float64)
+    _check(lib().oracle_gdn_scan(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta),
+                                 None if s0 is None else _ptr(s0), T, H, dk, dv, _ptr(o),
+                                 _ptr(s), _threads(nthreads)), "oracle_gdn_scan")
+    return o, s

@@ -1,10 +1,11 @@
-"""Builds liboracle.so (the CPU oracle, test infrastructure) in this directory with g++."""
+"""Builds liboracle.so (the CPU oracles of the MoE layer and of the Gated DeltaNet scan, test
+infrastructure) in this directory with g++."""
 import os
 import subprocess
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB = os.path.join(HERE, "liboracle.so")
-SOURCES = ["moe_oracle.cpp"]
+SOURCES = ["moe_oracle.cpp", "gdn_oracle.cpp"]
 
 
 def _stale():
@@ -12,7 +13,7 @@ def _stale():
         return True
     t = os.path.getmtime(LIB)
     return any(os.path.getmtime(os.path.join(HERE, s)) > t
-               for s in SOURCES + ["moe_oracle.h", "build.py"])
+               for s in SOURCES + ["moe_oracle.h", "gdn_oracle.h", "build.py"])
 
 
 def build(force=False):

@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the MoE FFN layer (data only: none of the layer's arithmetic).
+"""Seeded synthetic inputs for the MoE FFN layer and the Gated DeltaNet scan (data only: none
+of their arithmetic).
 
 The generator itself (splitmix64 words, 12-term Irwin-Hall values, bf16 rounding) is C in
 synth_host.c / synth_dev.cu; its definition is in synth.h.  This module composes streams
@@ -76,6 +77,14 @@ def lib():
         L.synth_q4_affine_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
                                              ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p,
                                              ctypes.c_void_p, ctypes.c_void_p]
+        L.synth_uniform_f32.restype = None
+        L.synth_uniform_f32.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                        ctypes.c_uint64, ctypes.c_float, ctypes.c_float,
+                                        ctypes.c_void_p]
+        L.synth_uniform_f32_device.restype = ctypes.c_int
+        L.synth_uniform_f32_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
+                                               ctypes.c_uint64, ctypes.c_float, ctypes.c_float,
+                                               ctypes.c_void_p, ctypes.c_void_p]
         L.synth_normal_bf16_device.restype = ctypes.c_int
         L.synth_normal_bf16_device.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64,
                                                ctypes.c_uint64, ctypes.c_float, ctypes.c_void_p,
@@ -230,6 +239,78 @@ def q4_device(seed, layer, name, dims, codes_ptr, scales_ptr, biases_ptr, cuda_s
         raise RuntimeError(f"synth device fill failed: cudaError {rc}")
 
 
+def uniform_f32(seed, stream, offset, n, lo, hi):
+    out = np.empty(int(n), dtype=np.float32)
+    if n:
+        lib().synth_uniform_f32(seed, stream, offset, n, lo, hi, out.ctypes.data)
+    return out
+
+
+def uniform_f32_device(seed, stream, offset, n, lo, hi, dev_ptr, cuda_stream=0):
+    rc = lib().synth_uniform_f32_device(seed, stream, offset, n, lo, hi, dev_ptr, cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"synth device fill failed: cudaError {rc}")
+
+
+# ---- inputs of the Gated DeltaNet recurrent scan (one layer, H heads)
+#
+#   q, k   [T][H][dk]   bf16, sigma dk^-1/2 (so that |k|^2 is close to 1, the regime in which the
+#                       delta rule's update I - beta k k^T is a contraction for beta in [0, 1))
+#   v      [T][H][dv]   bf16, sigma 1
+#   alpha  [T][H]       fp32 uniform on [0.80, 1.00): the per-token decay gate
+#   beta   [T][H]       fp32 uniform on [0, 1): the per-token write strength
+#   s0     [H][dk][dv]  fp32 holding bf16 values of sigma 0.25 (the state a previous prompt chunk
+#                       leaves), or zeros (the first chunk)
+# Element (t, h, i) of q is element (t H + h) dk + i of its stream, so a range of tokens can be
+# produced on its own.
+GDN_Q, GDN_K, GDN_V, GDN_ALPHA, GDN_BETA, GDN_S0 = range(40, 46)
+GDN_ALPHA_RANGE = (0.80, 1.0)
+GDN_BETA_RANGE = (0.0, 1.0)
+SIGMA_GDN_V = 1.0
+SIGMA_GDN_S0 = 0.25
+
+
+def gdn_sigma_qk(dk):
+    return float(np.float32(1.0 / np.sqrt(dk)))
+
+
+def gdn_inputs(seed, T, H, dk, dv, layer=0, t0=0, zero_state=False):
+    """Host inputs (q, k, v as bf16 bits; alpha, beta, s0 fp32) of tokens t0 .. t0 + T - 1."""
+    sq = gdn_sigma_qk(dk)
+    q = normal_bf16(seed, stream_id(GDN_Q, layer), t0 * H * dk, T * H * dk, sq).reshape(T, H, dk)
+    k = normal_bf16(seed, stream_id(GDN_K, layer), t0 * H * dk, T * H * dk, sq).reshape(T, H, dk)
+    v = normal_bf16(seed, stream_id(GDN_V, layer), t0 * H * dv, T * H * dv,
+                    SIGMA_GDN_V).reshape(T, H, dv)
+    alpha = uniform_f32(seed, stream_id(GDN_ALPHA, layer), t0 * H, T * H,
+                        *GDN_ALPHA_RANGE).reshape(T, H)
+    beta = uniform_f32(seed, stream_id(GDN_BETA, layer), t0 * H, T * H,
+                       *GDN_BETA_RANGE).reshape(T, H)
+    if zero_state:
+        s0 = np.zeros((H, dk, dv), dtype=np.float32)
+    else:
+        s0 = bf16_to_f32(normal_bf16(seed, stream_id(GDN_S0, layer), 0, H * dk * dv,
+                                     SIGMA_GDN_S0)).reshape(H, dk, dv)
+    return q, k, v, alpha, beta, s0
+
+
+def gdn_inputs_device(seed, T, H, dk, dv, q_ptr, k_ptr, v_ptr, alpha_ptr, beta_ptr,
+                      s0_bf16_ptr=None, layer=0, cuda_stream=0):
+    """Device fills of the same bits as gdn_inputs (t0 = 0).  s0 is filled as bf16 bits; the
+    caller widens it to fp32 (exact) or passes zeros."""
+    sq = gdn_sigma_qk(dk)
+    normal_bf16_device(seed, stream_id(GDN_Q, layer), 0, T * H * dk, sq, q_ptr, cuda_stream)
+    normal_bf16_device(seed, stream_id(GDN_K, layer), 0, T * H * dk, sq, k_ptr, cuda_stream)
+    normal_bf16_device(seed, stream_id(GDN_V, layer), 0, T * H * dv, SIGMA_GDN_V, v_ptr,
+                       cuda_stream)
+    uniform_f32_device(seed, stream_id(GDN_ALPHA, layer), 0, T * H, *GDN_ALPHA_RANGE, alpha_ptr,
+                       cuda_stream)
+    uniform_f32_device(seed, stream_id(GDN_BETA, layer), 0, T * H, *GDN_BETA_RANGE, beta_ptr,
+                       cuda_stream)
+    if s0_bf16_ptr is not None:
+        normal_bf16_device(seed, stream_id(GDN_S0, layer), 0, H * dk * dv, SIGMA_GDN_S0,
+                           s0_bf16_ptr, cuda_stream)
+
+
 def bf16_to_f32(a):
     """Widen bf16 bits (uint16) to float32 exactly."""
     return (np.asarray(a, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
@@ -244,4 +325,5 @@ def f32_to_bf16(a):
 
 __all__ = ["Dims", "stream_id", "normal_bf16", "normal_bf16_device", "permutation",
            "host_weight", "device_weight", "x_rows", "skew_bias", "bf16_to_f32", "f32_to_bf16",
-           "weight_shape", "WEIGHT_NAMES", "q4_shapes", "q4_host", "q4_device", "Q4_NAMES"]
+           "weight_shape", "WEIGHT_NAMES", "q4_shapes", "q4_host", "q4_device", "Q4_NAMES",
+           "uniform_f32", "uniform_f32_device", "gdn_inputs", "gdn_inputs_device"]

@@ -59,11 +59,19 @@ void synth_bytes(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, ui
 void synth_q4_affine(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, float base,
                      uint16_t* scales, uint16_t* biases);
 
+/* Uniform fp32 values on [lo, hi): element j is u = float(top 24 bits of word offset + j) * 2^-24
+ * (exact), then lo + (hi - lo) * u with one IEEE fp32 subtract, one multiply and one add,
+ * each rounded on its own (no fused multiply-add), so every machine produces the same bits. */
+void synth_uniform_f32(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, float lo,
+                       float hi, float* out);
+
 /* Device fills of the same (returns 0 or the cudaError_t of the launch). */
 int synth_bytes_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, void* dst,
                        void* cuda_stream);
 int synth_q4_affine_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n,
                            float base, void* scales, void* biases, void* cuda_stream);
+int synth_uniform_f32_device(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n,
+                             float lo, float hi, void* dst, void* cuda_stream);
 
 #ifdef __cplusplus
 }

@@ -58,6 +58,16 @@ __global__ void affine_kernel(uint64_t key, uint64_t offset, uint64_t n, float b
   }
 }
 
+__global__ void uniform_kernel(uint64_t key, uint64_t offset, uint64_t n, float lo, float hi,
+                               float* dst) {
+  uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  const float span = __fsub_rn(hi, lo);
+  for (uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride) {
+    float u = __fmul_rn((float)(uint32_t)(fin(key + (offset + j + 1) * kGamma) >> 40), 0x1p-24f);
+    dst[j] = __fadd_rn(lo, __fmul_rn(span, u));
+  }
+}
+
 unsigned grid_for(uint64_t n) {
   uint64_t blocks = (n + 255) / 256;
   return (unsigned)(blocks > 152ull * 32 ? 152ull * 32 : blocks);
@@ -89,5 +99,14 @@ extern "C" int synth_q4_affine_device(uint64_t seed, uint64_t stream, uint64_t o
   if (n == 0) return 0;
   affine_kernel<<<grid_for(n), 256, 0, (cudaStream_t)cuda_stream>>>(
       synth_key(seed, stream), offset, n, base, (uint16_t*)scales, (uint16_t*)biases);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int synth_uniform_f32_device(uint64_t seed, uint64_t stream, uint64_t offset,
+                                        uint64_t n, float lo, float hi, void* dst,
+                                        void* cuda_stream) {
+  if (n == 0) return 0;
+  uniform_kernel<<<grid_for(n), 256, 0, (cudaStream_t)cuda_stream>>>(
+      synth_key(seed, stream), offset, n, lo, hi, (float*)dst);
   return (int)cudaGetLastError();
 }

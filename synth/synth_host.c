@@ -111,3 +111,14 @@ void synth_q4_affine(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n
     biases[j] = (uint16_t)(sb ^ 0x8000u) + (uint16_t)(3u << 7); /* -8 s: sign flip, exponent + 3 */
   }
 }
+
+void synth_uniform_f32(uint64_t seed, uint64_t stream, uint64_t offset, uint64_t n, float lo,
+                       float hi, float* out) {
+  uint64_t key = synth_key(seed, stream);
+  const float span = hi - lo;
+  for (uint64_t j = 0; j < n; ++j) {
+    float u = (float)(uint32_t)(synth_word(key, offset + j) >> 40) * 0x1p-24f;
+    float p = span * u;
+    out[j] = lo + p;
+  }
+}
