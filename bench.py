@@ -16,7 +16,10 @@ Also measured in the same run and reported in the same line:
   prefill_skewed: the same layer with skewed routing (router bias -2.4 ln(rank_e)), timed
        and set against the floor of its own bytes and FLOPs;
   prefill_sweep: the balanced layer at T = 256 .. 131072 (bf16; --sweep-q4 adds 4-bit experts),
-       each T with the floor of its bytes and FLOPs.
+       each T with the floor of its bytes and FLOPs;
+  gdn_scan: the Gated DeltaNet recurrent scan of one layer (32 heads, 128 x 128 fp32 state)
+       over 2K- and 16K-token prompts, us per scan against the SMs' fp32 FMA peak, with the
+       scan oracle's rate on the host cores.
 --impl reference times only the CPU oracle (the reference arm of this benchmark).
 """
 import argparse
@@ -66,6 +69,10 @@ def parse_args():
                    help="also run the length sweep with 4-bit experts")
     p.add_argument("--sweep-tokens", type=str, default=None,
                    help="comma-separated T values of the sweep (default: 256 .. 131072)")
+    p.add_argument("--no-gdn", action="store_true",
+                   help="skip the Gated DeltaNet scan line (T = 2048, 32 heads of 128 x 128)")
+    p.add_argument("--gdn-tokens", type=str, default="2048,16384",
+                   help="comma-separated prompt lengths of the Gated DeltaNet scan line")
     return p.parse_args()
 
 
@@ -391,6 +398,96 @@ def time_prefill(torch, moe, T, skew, steps, warmup, seed, P_hbm, P_tc, q4=False
             "frac_of_floor": floor / t, "bound": "hbm" if byts / (P_hbm * 1e9) >= flops /
             (P_tc * 1e12) else "tensor", "nonempty_experts": int((counts > 0).sum()),
             "max_expert_rows": int(counts.max())}
+
+
+# ---------------------------------------------------------------- Gated DeltaNet scan
+
+GDN_H, GDN_DK, GDN_DV = 32, 128, 128
+SM_CLOCK_MHZ = 2070.0  # GB300's maximum SM clock (the clock samples of the run are reported)
+
+
+def gdn_algorithmic(T, H=GDN_H, dk=GDN_DK, dv=GDN_DV):
+    """FLOPs and bytes of one scan as the rule is written: per token and head S^T k (2 dk dv),
+    the delta u (3 dv), alpha S + k u^T (3 dk dv), S^T q (2 dk dv); bytes: q, k, v, o in bf16,
+    the gates in fp32, the state read and written once in fp32."""
+    flops = T * H * (7 * dk * dv + 3 * dv)
+    byts = T * H * (2 * dk * 2 + 2 * dv * 2 + 2 * 4) + 2 * H * dk * dv * 4
+    return flops, byts
+
+
+def run_gdn(torch, moe, args, P_hbm):
+    """The Gated DeltaNet recurrent scan of one layer (32 heads, 128 x 128 fp32 state each)
+    over a prompt of T tokens: device time per scan (L2 flushed before every step), against
+    the fp32 FMA peak of the SMs (the scan is FMA-bound: 4 FMA-pipe operations per state
+    element and token), with the oracle's rate on the host cores beside it."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sms = props.multi_processor_count
+    peak_tf = sms * 128 * 2 * SM_CLOCK_MHZ * 1e6 / 1e12
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    rows = []
+    for T in [int(t) for t in args.gdn_tokens.split(",") if t]:
+        H, dk, dv = GDN_H, GDN_DK, GDN_DV
+        q = torch.empty((T, H, dk), dtype=torch.int16, device="cuda")
+        k = torch.empty_like(q)
+        v = torch.empty((T, H, dv), dtype=torch.int16, device="cuda")
+        al = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        be = torch.empty_like(al)
+        s0b = torch.empty((H, dk, dv), dtype=torch.int16, device="cuda")
+        synth.gdn_inputs_device(0, T, H, dk, dv, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                al.data_ptr(), be.data_ptr(), s0b.data_ptr(),
+                                cuda_stream=stream.cuda_stream)
+        s0 = s0b.view(torch.bfloat16).float()  # exact widening of the bf16 draws
+        s1 = torch.empty_like(s0)
+        o = torch.empty((T, H, dv), dtype=torch.int16, device="cuda")
+
+        def scan():
+            st = moe.gdn_scan(q.data_ptr(), k.data_ptr(), v.data_ptr(), al.data_ptr(),
+                              be.data_ptr(), s0.data_ptr(), s1.data_ptr(), o.data_ptr(), T, H,
+                              dk, dv, stream.cuda_stream)
+            assert st == moe.MOE_OK, moe.moe_status_string(st)
+
+        for _ in range(max(3, args.warmup)):
+            scan()
+        steps = min(args.steps, 50)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            scan()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+        flops, byts = gdn_algorithmic(T)
+        tf = flops / (us * 1e-6) / 1e12
+        rows.append({
+            "T": T, "heads": H, "dk": dk, "dv": dv, "us": us, "tokens_per_s": T / (us * 1e-6),
+            "roofline": {"bound": "alu", "achieved": tf, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": tf / peak_tf,
+                         "peak_source": f"derived: {sms} SMs x 128 fp32 lanes x 2 FLOP x "
+                                        f"{SM_CLOCK_MHZ:.0f} MHz",
+                         "traffic": None},
+            "hbm_frac": byts / (us * 1e-6) / 1e9 / P_hbm,
+            "algorithmic_flops": flops, "algorithmic_bytes": byts, "gpu_launches": steps,
+            "l2": "flushed (256 MB write, untimed) before every timed step"})
+        del q, k, v, al, be, s0b, s0, s1, o
+    return {"rows": rows, "cpu_baseline": None if args.no_cpu else gdn_oracle_rate()}
+
+
+def gdn_oracle_rate(T=2048):
+    """The scan oracle (fp64, one head per host thread) on the T=2048, 32-head layer."""
+    import time
+
+    import oracle
+    q, k, v, al, be, s0 = synth.gdn_inputs(0, T, GDN_H, GDN_DK, GDN_DV)
+    cores = host_cores()
+    t0 = time.perf_counter()
+    oracle.gdn_scan(q, k, v, al, be, s0, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": T / dt, "unit": "tokens/s", "cores": min(cores, GDN_H), "kind": "oracle",
+            "sample": f"the whole T={T}, {GDN_H}-head scan, one head per thread"}
 
 
 def run_decode(torch, moe, args, rank, world, P_hbm):
@@ -742,6 +839,7 @@ def main():
                                    P_tc, q4=True) for t in ts]
     pre_q4 = None if args.no_q4 else run_prefill_q4(torch, moe, args, rank, P_hbm, P_tc)
     dec = None if args.no_decode else run_decode(torch, moe, args, rank, world, P_hbm)
+    gdn = None if args.no_gdn else run_gdn(torch, moe, args, P_hbm)
     clk = clocks.stop()
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -767,6 +865,7 @@ def main():
         "prefill_sweep": sweep,
         "prefill_q4": pre_q4,
         "decode": dec,
+        "gdn_scan": gdn,
         "cpu_baseline": cpu,
         "e2e": {"value": job_value(world, T_PREFILL, pre["e2e_ms"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": T_PREFILL * D * 2, "d2h_bytes_per_step": T_PREFILL * D * 2},

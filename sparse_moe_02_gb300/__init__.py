@@ -30,7 +30,7 @@ MOE_SCHEDULE_GEMV = 2
 EXPORTS = ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_get_device_error",
            "moe_destroy", "moe_status_string", "moe_last_cuda_error", "moe_profile_begin",
            "moe_profile_end", "moe_route_one_noalloc", "moe_create_q4", "moe_read_probe",
-           "moe_test_expire_waits")
+           "moe_test_expire_waits", "gdn_scan")
 
 # kernel order reported by moe_profile_end
 KERNELS_GEMM = ("router_topk", "route_plan_scatter", "experts", "combine")
@@ -92,10 +92,13 @@ def lib():
         L.moe_route_one_noalloc.argtypes = [_c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                             _c_void_p, _c_void_p]
         L.moe_test_expire_waits.argtypes = [_c_void_p, _c_int]
+        L.gdn_scan.argtypes = [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                               _c_void_p, _c_void_p, ctypes.c_int64, _c_int, _c_int, _c_int,
+                               _c_void_p]
         for fn in ("moe_create", "moe_create_q4", "moe_read_probe", "moe_route", "moe_forward", "moe_forward_host",
                    "moe_get_device_error", "moe_destroy", "moe_last_cuda_error",
                    "moe_profile_begin", "moe_profile_end", "moe_route_one_noalloc",
-                   "moe_test_expire_waits"):
+                   "moe_test_expire_waits", "gdn_scan"):
             getattr(L, fn).restype = _c_int
         _lib = L
     return _lib
@@ -150,6 +153,12 @@ def moe_last_cuda_error():
 def moe_route_one_noalloc(x, d, w_router, router_bias, topk_idx, topk_w, stream):
     """Routing of one token with no device allocation (see include/moe.h)."""
     return lib().moe_route_one_noalloc(x, d, w_router, router_bias, topk_idx, topk_w, stream)
+
+
+def gdn_scan(q, k, v, alpha, beta, state_in, state_out, o, T, H, dk, dv, stream):
+    """Gated DeltaNet recurrent scan over T tokens of H heads (see include/gdn.h); device
+    pointers, state_in may be None (zero state)."""
+    return lib().gdn_scan(q, k, v, alpha, beta, state_in, state_out, o, T, H, dk, dv, stream)
 
 
 def moe_test_expire_waits(h, n_calls):

@@ -10,8 +10,8 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 SOURCES = ["api.cu", "route.cu", "experts.cu", "decode.cu", "decode_q4.cu", "noalloc.cu", "probe.cu",
-           "hostio.cu"]
-HEADERS = ["layer.cuh", "plan.cuh", "ptx.cuh", "select.cuh"]
+           "hostio.cu", "gdn.cu"]
+HEADERS = ["layer.cuh", "plan.cuh", "ptx.cuh", "select.cuh", "q4.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + CSRC,
          "-I" + os.path.join(ROOT, "include")]
@@ -22,7 +22,8 @@ def _stale():
         return True
     t = os.path.getmtime(LIB)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    deps += [os.path.join(ROOT, "include", "moe.h"), os.path.abspath(__file__)]
+    deps += [os.path.join(ROOT, "include", h) for h in ("moe.h", "gdn.h")]
+    deps += [os.path.abspath(__file__)]
     return any(os.path.getmtime(p) > t for p in deps)
 
 

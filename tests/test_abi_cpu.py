@@ -1,5 +1,5 @@
 """Host-side checks of the C ABI that need no GPU: the library loads, exports every function
-include/moe.h declares, and rejects invalid arguments before touching CUDA."""
+include/moe.h and include/gdn.h declare, and rejects invalid arguments before touching CUDA."""
 import ctypes
 import os
 import re
@@ -12,14 +12,20 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _declared_functions():
-    src = open(os.path.join(ROOT, "include", "moe.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*]+\s+\**(moe_\w+)\s*\(", src, re.M)))
+    names = set()
+    for hdr in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not hdr.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", hdr)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[\w\*]+\s+\**((?:moe|gdn)_\w+)\s*\(", src,
+                                re.M))
+    return sorted(names)
 
 
 def test_library_exports_every_declared_function():
     declared = _declared_functions()
-    assert "moe_create" in declared and "moe_forward" in declared
+    assert "moe_create" in declared and "moe_forward" in declared and "gdn_scan" in declared
     L = moe.lib()
     for fn in declared:
         assert hasattr(L, fn), f"{fn} declared in include/moe.h but not exported"
@@ -93,3 +99,33 @@ def test_create_without_gpu_reports_cuda_error():
         pytest.skip("a GPU is present")
     st, h = moe.moe_create(_cfg(), _weights())
     assert st == moe.MOE_ERR_CUDA and not h.value
+
+
+def test_scan_rejects_bad_arguments_before_touching_cuda():
+    # 16-byte aligned stand-in addresses, never dereferenced: every case below fails in the
+    # argument checks, before any CUDA call
+    A = 0x100000
+    ok = dict(q=A, k=A + 0x10000, v=A + 0x20000, alpha=A + 0x30000, beta=A + 0x40000,
+              state_in=A + 0x50000, state_out=A + 0x60000, o=A + 0x70000, T=64, H=2, dk=128,
+              dv=64, stream=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return moe.gdn_scan(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["state_in"],
+                            a["state_out"], a["o"], a["T"], a["H"], a["dk"], a["dv"], a["stream"])
+
+    assert call(T=-1) == moe.MOE_ERR_INVALID_ARG
+    assert call(H=0) == moe.MOE_ERR_INVALID_ARG
+    assert call(state_out=None) == moe.MOE_ERR_INVALID_ARG
+    for name in ("q", "k", "v", "alpha", "beta", "o"):
+        assert call(**{name: None}) == moe.MOE_ERR_INVALID_ARG, name
+    assert call(dk=64) == moe.MOE_ERR_UNSUPPORTED
+    assert call(dv=48) == moe.MOE_ERR_UNSUPPORTED
+    assert call(dv=0) == moe.MOE_ERR_UNSUPPORTED
+    assert call(dv=8192) == moe.MOE_ERR_UNSUPPORTED
+    assert call(H=65536) == moe.MOE_ERR_UNSUPPORTED
+    for name in ("q", "k", "v", "o"):
+        assert call(**{name: ok[name] + 8}) == moe.MOE_ERR_ALIGNMENT, name
+    for name in ("alpha", "beta", "state_in", "state_out"):
+        assert call(**{name: ok[name] + 2}) == moe.MOE_ERR_ALIGNMENT, name

@@ -1,0 +1,146 @@
+"""GPU parity of the Gated DeltaNet recurrent scan (gdn_scan, through the C ABI) against the
+CPU oracle (oracle.gdn_scan, fp64).
+
+Bar (derived from the arithmetic): the kernel keeps the state in fp32 and rounds o once to bf16.
+A 128-term fp32 dot product errs by at most about 128 * 2^-24 of the sum of its absolute terms
+(below 1e-5 for states of norm ~1 and unit-norm keys), and the update
+S <- alpha (I - beta k k^T) S + ... contracts an error by alpha <= 1 per token, so the state's
+error stays below about 1e-5 / (1 - 0.9) = 1e-4 of its scale.  Hence
+  state:  |S_gpu - S_ref| <= 1e-4 * max|S_ref|           (elementwise)
+  output: |o_gpu - o_ref| <= 2^-8 |o_ref| + 1e-4 * max|o_ref|
+(2^-8: the bf16 rounding of o, half an ulp, with room for the fp32 error of o itself).
+Exact cases: a scan split at any token continues bit for bit; beta = 0 with alpha = 1 leaves
+the state bit-identical; T = 0 copies the state.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import sparse_moe_02_gb300 as moe
+import synth
+
+pytestmark = pytest.mark.gpu
+
+DK = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    yield
+    torch.cuda.synchronize()
+
+
+def _dev(a, dtype):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype == "bf16":
+        t = t.view(torch.int16)
+    return t.cuda()
+
+
+def run_scan(q, k, v, alpha, beta, s0, state_out=None, in_place=False):
+    """gdn_scan on device copies of the host inputs; returns (o bf16 bits, state fp32)."""
+    import torch
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    qd, kd, vd = _dev(q, "bf16"), _dev(k, "bf16"), _dev(v, "bf16")
+    ad, bd = _dev(alpha, "f32"), _dev(beta, "f32")
+    sin = None if s0 is None else _dev(s0.astype(np.float32), "f32")
+    sout = sin if in_place else torch.full((H, dk, dv), float("nan"), device="cuda")
+    o = torch.zeros((max(T, 1), H, dv), dtype=torch.int16, device="cuda")
+    st = moe.gdn_scan(qd.data_ptr() if T else None, kd.data_ptr() if T else None,
+                      vd.data_ptr() if T else None, ad.data_ptr() if T else None,
+                      bd.data_ptr() if T else None, None if sin is None else sin.data_ptr(),
+                      sout.data_ptr(), o.data_ptr() if T else None, T, H, dk, dv,
+                      torch.cuda.current_stream().cuda_stream)
+    assert st == moe.MOE_OK, moe.moe_status_string(st)
+    torch.cuda.synchronize()
+    return o[:T].cpu().numpy().view(np.uint16), sout.cpu().numpy()
+
+
+def check(o_bits, s_gpu, o_ref, s_ref):
+    o = synth.bf16_to_f32(o_bits).astype(np.float64)
+    o_bound = 2.0 ** -8 * np.abs(o_ref) + 1e-4 * np.abs(o_ref).max()
+    bad = np.abs(o - o_ref) > o_bound
+    assert not bad.any(), (f"{bad.sum()} outputs out of bound; max err "
+                           f"{np.abs(o - o_ref).max()}, max|ref| {np.abs(o_ref).max()}")
+    s_err = np.abs(s_gpu.astype(np.float64) - s_ref).max()
+    assert s_err <= 1e-4 * np.abs(s_ref).max(), f"state error {s_err}"
+
+
+@pytest.mark.parametrize("T,H,dv,zero_state,seed", [
+    (1, 1, 32, False, 1),      # one token, one block
+    (31, 2, 64, True, 2),      # a partial first chunk, zero state
+    (32, 1, 128, False, 3),    # exactly one chunk
+    (100, 3, 128, False, 4),   # three full chunks and a ragged tail
+    (257, 2, 96, False, 5),    # three column blocks per head, a one-token tail
+    (1000, 4, 256, True, 6),   # eight column blocks, zero state
+])
+def test_scan_matches_oracle(T, H, dv, zero_state, seed):
+    q, k, v, alpha, beta, s0 = synth.gdn_inputs(seed, T, H, DK, dv, zero_state=zero_state)
+    o, s = run_scan(q, k, v, alpha, beta, None if zero_state else s0)
+    o_ref, s_ref = oracle.gdn_scan(q, k, v, alpha, beta, None if zero_state else s0)
+    check(o, s, o_ref, s_ref)
+
+
+def test_scan_workload_every_output():
+    # the benchmark's layer: 2K-token prompt, 32 heads of 128 x 128 state, every token and head
+    T, H, dv = 2048, 32, 128
+    q, k, v, alpha, beta, s0 = synth.gdn_inputs(0, T, H, DK, dv)
+    o, s = run_scan(q, k, v, alpha, beta, s0)
+    o_ref, s_ref = oracle.gdn_scan(q, k, v, alpha, beta, s0)
+    check(o, s, o_ref, s_ref)
+
+
+def test_scan_long_prompt():
+    # error growth over a long scan: 32K tokens, 2 heads
+    T, H, dv = 32768, 2, 128
+    q, k, v, alpha, beta, s0 = synth.gdn_inputs(8, T, H, DK, dv)
+    o, s = run_scan(q, k, v, alpha, beta, s0)
+    o_ref, s_ref = oracle.gdn_scan(q, k, v, alpha, beta, s0)
+    check(o, s, o_ref, s_ref)
+
+
+@pytest.mark.parametrize("split", [1, 37, 64, 299])
+def test_split_scan_is_bit_identical(split):
+    T, H, dv = 300, 2, 64
+    q, k, v, alpha, beta, s0 = synth.gdn_inputs(9, T, H, DK, dv)
+    o, s = run_scan(q, k, v, alpha, beta, s0)
+    o1, s1 = run_scan(q[:split], k[:split], v[:split], alpha[:split], beta[:split], s0)
+    o2, s2 = run_scan(q[split:], k[split:], v[split:], alpha[split:], beta[split:], s1)
+    assert np.array_equal(np.concatenate([o1, o2]), o)
+    assert np.array_equal(s2.view(np.uint32), s.view(np.uint32))
+
+
+def test_in_place_state_and_determinism():
+    T, H, dv = 150, 2, 64
+    q, k, v, alpha, beta, s0 = synth.gdn_inputs(10, T, H, DK, dv)
+    o, s = run_scan(q, k, v, alpha, beta, s0)
+    o2, s2 = run_scan(q, k, v, alpha, beta, s0, in_place=True)
+    assert np.array_equal(o, o2) and np.array_equal(s.view(np.uint32), s2.view(np.uint32))
+
+
+def test_no_write_no_decay_keeps_the_state_exactly():
+    # beta = 0, alpha = 1: S <- 1 * S + k * 0 is exact in fp32, so the state comes back bit for
+    # bit and o_t = S0^T q_t (fp32 sums) for every token
+    T, H, dv = 70, 2, 64
+    q, k, v, _, _, s0 = synth.gdn_inputs(11, T, H, DK, dv)
+    ones, zeros = np.ones((T, H), np.float32), np.zeros((T, H), np.float32)
+    o, s = run_scan(q, k, v, ones, zeros, s0)
+    assert np.array_equal(s.view(np.uint32), s0.view(np.uint32))
+    want = np.einsum("thi,hij->thj", synth.bf16_to_f32(q).astype(np.float64),
+                     s0.astype(np.float64))
+    got = synth.bf16_to_f32(o).astype(np.float64)
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-6)
+
+
+def test_zero_tokens_copy_or_clear_the_state():
+    H, dv = 3, 32
+    q, k, v, alpha, beta, s0 = synth.gdn_inputs(12, 0, H, DK, dv)
+    o, s = run_scan(q, k, v, alpha, beta, s0)
+    assert o.shape[0] == 0 and np.array_equal(s.view(np.uint32), s0.view(np.uint32))
+    _, s = run_scan(q, k, v, alpha, beta, None)
+    assert np.array_equal(s, np.zeros_like(s))
