@@ -31,11 +31,14 @@
  *   o         [T][H][dv] bf16: o_t rounded once from fp32
  *
  * Arithmetic: fp32 state and gates; q, k, v widened exactly from bf16.  Per token the kernel
- * takes r = S^T k and p = S^T q from the state before the token, then
- * u = beta (v - alpha r), o = alpha p + (k . q) u and S <- alpha S + k u^T (the same o_t as the
- * rule above: S_t^T q = alpha S_{t-1}^T q + u (k . q)); sums are fp32 in a fixed order, so a
- * call is deterministic, and a scan split into two calls at any token, the second starting
- * from the first's state_out, gives bit-identical outputs and state.
+ * forms r_t = S_{t-1}^T k_t and p_t = S_{t-1}^T q_t, then u_t = beta_t (v_t - alpha_t r_t),
+ * o_t = alpha_t p_t + (k_t . q_t) u_t (= S_t^T q_t) and S_t = alpha_t S_{t-1} + k_t u_t^T.  Inside
+ * each run of 32 tokens (counted from the call's first token) r_t and p_t are taken one token
+ * early, as alpha_{t-1} S_{t-2}^T k_t + (k_{t-1} . k_t) u_{t-1} (and likewise with q_t), which
+ * is the same value rounded differently.  Sums are fp32 in a fixed order, so a call is
+ * deterministic, and a scan split into two calls after a multiple of 32 tokens, the second
+ * starting from the first's state_out, gives bit-identical outputs and state (a split elsewhere
+ * agrees to rounding).
  *
  * Ownership and threading: every pointer is a device pointer owned by the caller; the call
  * only enqueues one kernel on `stream` (a cudaStream_t as void*, NULL = the legacy default
@@ -44,8 +47,8 @@
  * Errors (status values of moe.h): MOE_ERR_INVALID_ARG (T < 0, H < 1, a NULL pointer other
  * than state_in; q, k, v, alpha, beta and o may be NULL when T == 0), MOE_ERR_UNSUPPORTED
  * (dk != 128, dv not a multiple of 32 or above 4096, H above 65535), MOE_ERR_ALIGNMENT (q, k, v, o
- * not 16-byte aligned; alpha, beta, state_in, state_out not 4-byte aligned), MOE_ERR_CUDA (the
- * launch failed).  The kernel has no waits that can time out.
+ * not 16-byte aligned; alpha, beta not 4-byte aligned; state_in, state_out not 8-byte aligned),
+ * MOE_ERR_CUDA (the launch failed).  The kernel has no waits that can time out.
  */
 #ifndef GDN_H
 #define GDN_H
