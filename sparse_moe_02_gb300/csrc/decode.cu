@@ -723,8 +723,8 @@ struct StreamArgs {
 // Shared-memory layout of a block, in bytes: the ring (kStSlots slots of one feature's gate and
 // up rows, two per slot warp with 4-bit rows), x, the down rows of up to nn = ceil(d / G) outputs of the 8 experts and the shared
 // expert, h, the mbarriers.  bf16: x as bf16, h as two fp32 planes (see h_piece).  4-bit: a
-// slot holds the two rows' codes, then their scales and biases; x and h as swizzled fp32 with
-// their sums per 32 (see q4.cuh); the down rows as codes [9][nn][K/2], then scales, then biases
+// slot holds the two rows' codes, then their scales and biases; x as swizzled fp32 with its sums
+// per 32, h as swizzled fp32 (see q4.cuh); the down rows as codes [9][nn][K/2], then scales, then biases
 // (K = f, or fs for the shared expert).  A 4-bit block is padded to more than half an SM's
 // shared memory, so that one block runs on every SM.
 struct StLayout {
@@ -748,8 +748,7 @@ __host__ __device__ inline StLayout st_layout(const Dims& D, int G) {
     L.sc = L.rows + nn * (8 * D.f + D.fs) / 2;
     L.bi = L.sc + nn * (8 * D.f + D.fs) / 32;
     L.hp = L.bi + nn * (8 * D.f + D.fs) / 32;
-    L.hsum = L.hp + 9 * D.hdim * 4;
-    L.bars = L.hsum + 9 * (D.hdim / 32) * 4;
+    L.hsum = L.bars = L.hp + 9 * D.hdim * 4;
   }
   L.total = L.bars + (2 * kStSlots + 2) * 8;
   if (Q4 && L.total < 120 * 1024) L.total = 120 * 1024;
@@ -872,39 +871,60 @@ __device__ __forceinline__ float bf16_at(const uint8_t* p) {
   return __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(p) << 16);
 }
 
-// The 4-bit combine: out[i] for i < nn (nn <= 16) over the rows in shared memory (layout in
-// st_layout) and h (swizzled rows at hf + j hdim, sums per 32 at hs + j hdim / 32).  Combine warp
-// cw takes outputs cw and cw + 8; lane l the pieces P = l, l + 32, ... of the nine rows of an
-// output taken as one run (P < 8 f / 32: routed row j = P / (f / 32); then the shared row),
-// summing w_j (scale * codes . h_j + bias * sum h_j) into four partial sums (P / 32 mod 4, each
-// in run order); one warp reduction per output.
+// The 4-bit combine: out[i] for i < nn (1 <= nn <= 16) over the rows in shared memory (codes
+// [9][nn][K/2], then scales and biases [9][nn][K/64] bf16, K = f, or fs for the shared expert;
+// layout in st_layout) and h (swizzled rows at hf + j hdim), by the kCbWarps warps of the combine
+// (cw: this warp's index among them, ct: this thread's).  The 32-input pieces of the nine rows
+// are taken as one run (P < 8 f / 32: routed row j = P / (f / 32); then the shared row); combine
+// warp w takes the outputs w % 4, w % 4 + 4, ... and half w / 4 of the run, lane l the pieces
+// l, l + 32, ... of that half.  A piece of h and its sum are read once and applied to the
+// warp's four outputs, each term w_j (scale * (codes . h_j) + bias * sum h_j); the two halves
+// are added after.  All combine threads call this (it holds named barrier 4); part is shared
+// scratch of kCbWarps * 4 floats.
 __device__ __forceinline__ void dn_combine_q4(const uint8_t* codes, const uint8_t* sc,
-                                              const uint8_t* bi, const float* hf, const float* hs,
-                                              int nn, int f, int fs, int hdim, const float* w,
-                                              __nv_bfloat16* out, int cw, int lane) {
-  const int npr = f / 32, nps = fs / 32, npt = 8 * npr + nps;
-  for (int i = cw; i < nn; i += kCbWarps) {
-    float accs[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums (P / 32 mod 4)
-    for (int P0 = lane; P0 < npt; P0 += 128) {
+                                              const uint8_t* bi, const float* hf, int nn, int f,
+                                              int fs, int hdim, const float* w, float* part,
+                                              __nv_bfloat16* out, int cw, int ct) {
+  const int lane = ct & 31;
+  const int og = cw & 3, half = cw >> 2;
+  const int npr = f / 32, npt = 8 * npr + fs / 32;
+  // past nn the last row is read again and its sum dropped (no branch per output)
+  int oi[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int P = P0 + 32 * q;
-        if (P >= npt) break;
-        const int j = P < 8 * npr ? P / npr : 8, p = P - j * npr;
-        // the row's codes and its scales / biases (bytes) in their regions
-        const size_t cbase = j < 8 ? ((size_t)j * nn + i) * (f / 2)
-                                   : (size_t)8 * nn * (f / 2) + (size_t)i * (fs / 2);
-        const size_t gbase = j < 8 ? ((size_t)j * nn + i) * (f / 32)
-                                   : (size_t)8 * nn * (f / 32) + (size_t)i * (fs / 32);
-        const uint4 c = *reinterpret_cast<const uint4*>(codes + cbase + (size_t)p * 16);
-        const float s = bf16_at(sc + gbase + (p / 2) * 2), b = bf16_at(bi + gbase + (p / 2) * 2);
-        const float t =
-            s * q4_dot32(c, hf + (size_t)j * hdim, p) + b * hs[(size_t)j * (hdim / 32) + p];
-        accs[q] = fmaf(j < 8 ? w[j] : 1.0f, t, accs[q]);
-      }
+  for (int m = 0; m < 4; ++m) oi[m] = min(og + 4 * m, nn - 1);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int p1 = half ? npt : npt / 2;
+  for (int P = (half ? npt / 2 : 0) + lane; P < p1; P += 32) {
+    const int j = P < 8 * npr ? P / npr : 8, p = P - j * npr;
+    float4 hv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hv[k] = piece_f4(hf + (size_t)j * hdim, p, k);
+    float hsum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hsum += (hv[k].x + hv[k].y) + (hv[k].z + hv[k].w);
+    const float wj = j < 8 ? w[j] : 1.0f;
+    // the row's codes and its scales / biases (bytes) in their regions
+    const size_t kb = j < 8 ? (size_t)f / 2 : (size_t)fs / 2;    // code bytes of a row
+    const size_t gbr = j < 8 ? (size_t)f / 32 : (size_t)fs / 32;  // scale bytes of a row
+    const size_t cbase = j < 8 ? (size_t)j * nn * (f / 2) : (size_t)8 * nn * (f / 2);
+    const size_t gbase = j < 8 ? (size_t)j * nn * (f / 32) : (size_t)8 * nn * (f / 32);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint4 c = *reinterpret_cast<const uint4*>(codes + cbase + oi[m] * kb + (size_t)p * 16);
+      const size_t g = gbase + oi[m] * gbr + (p / 2) * 2;
+      const float t = bf16_at(sc + g) * q4_dot32(c, hv) + bf16_at(bi + g) * hsum;
+      acc[m] = fmaf(wj, t, acc[m]);
     }
-    const float acc = warp_sum((accs[0] + accs[1]) + (accs[2] + accs[3]));
-    if (lane == 0) out[i] = __float2bfloat16_rn(acc);
+  }
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const float v = warp_sum(acc[m]);
+    if (lane == 0) part[cw * 4 + m] = v;
+  }
+  named_sync(4, kCbWarps * 32);
+  if (ct < nn) {
+    const int g = ct & 3, m = ct >> 2;
+    out[ct] = __float2bfloat16_rn(part[g * 4 + m] + part[(g + 4) * 4 + m]);
   }
 }
 
@@ -1275,23 +1295,6 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
       }
     }
   }
-  if (Q4) {
-    __syncthreads();
-    float* hsum = reinterpret_cast<float*>(ssm + Ly.hsum);
-    for (int q = threadIdx.x; q < 9 * (hdim / 32); q += kStThreads) {
-      const float4* t4 = reinterpret_cast<const float4*>(hs + 32 * q);
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 t = t4[i];
-        sum += t.x;
-        sum += t.y;
-        sum += t.z;
-        sum += t.w;
-      }
-      hsum[q] = sum;
-    }
-  }
   if (warp == 0) {
     const bool landed = mbar_wait(dbar, 0, a.err);
     // after a timeout: one more bounded chance for the copies to land before the block leaves
@@ -1304,8 +1307,8 @@ __global__ void __maxnreg__(168) dec_stream_kernel(StreamArgs a) {
     dn_combine_rows(rows, reinterpret_cast<const float4*>(hs), nn, f, fs, hdim, s_w, s_part,
                     a.y + n0, warp - 1, threadIdx.x - 32);
   else
-    dn_combine_q4(rows, ssm + Ly.sc, ssm + Ly.bi, hs, reinterpret_cast<const float*>(ssm + Ly.hsum),
-                  nn, f, fs, hdim, s_w, a.y + n0, warp - 1, lane);
+    dn_combine_q4(rows, ssm + Ly.sc, ssm + Ly.bi, hs, nn, f, fs, hdim, s_w, s_part, a.y + n0,
+                  warp - 1, threadIdx.x - 32);
 }
 
 }  // namespace

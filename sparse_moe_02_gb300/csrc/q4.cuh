@@ -21,12 +21,12 @@ __device__ __forceinline__ float4 piece_f4(const float* v, int p, int k) {
   return *reinterpret_cast<const float4*>(v + 32 * p + 4 * ((k + p) & 7));
 }
 
-// 32 consecutive codes (the lower nibble of a byte first) times piece p of the swizzled
-// vector v: sum_i q_i v_i, in eight fp32 partial sums (four packed pairs, one per group of
+// 32 consecutive codes (the lower nibble of a byte first) times 32 values vv (float4 k holding
+// values 4k .. 4k + 3, in order): sum_i q_i v_i, in eight fp32 partial sums (four packed pairs, one per group of
 // 8 inputs: independent chains) that are added at the end.  Packed fp32 pairs: prmt builds the
 // float 2^23 + q of a code byte, one packed add takes 2^23 off (exact), one packed fma
 // accumulates two products.
-__device__ __forceinline__ float q4_dot32(uint4 c, const float* v, int p) {
+__device__ __forceinline__ float q4_dot32(uint4 c, const float4 (&vv)[8]) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
   unsigned long long acc[4] = {0ull, 0ull, 0ull, 0ull};  // fp32 zero pairs
   const unsigned long long neg_magic = 0xCB000000CB000000ull;  // (-2^23, -2^23)
@@ -34,8 +34,8 @@ __device__ __forceinline__ float q4_dot32(uint4 c, const float* v, int p) {
   for (int k = 0; k < 4; ++k) {
     const uint32_t t0 = w[k] & 0x0F0F0F0Fu;         // codes of inputs 8k, 8k+2, 8k+4, 8k+6
     const uint32_t t1 = (w[k] >> 4) & 0x0F0F0F0Fu;  // codes of inputs 8k+1, 8k+3, ...
-    const float4 a = piece_f4(v, p, 2 * k);
-    const float4 b = piece_f4(v, p, 2 * k + 1);
+    const float4 a = vv[2 * k];
+    const float4 b = vv[2 * k + 1];
     const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -57,6 +57,14 @@ __device__ __forceinline__ float q4_dot32(uint4 c, const float* v, int p) {
   for (int k = 0; k < 4; ++k)
     sum += __uint_as_float((uint32_t)acc[k]) + __uint_as_float((uint32_t)(acc[k] >> 32));
   return sum;
+}
+
+// The same with piece p of the swizzled vector v read from shared memory.
+__device__ __forceinline__ float q4_dot32(uint4 c, const float* v, int p) {
+  float4 vv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) vv[k] = piece_f4(v, p, k);
+  return q4_dot32(c, vv);
 }
 
 __device__ __forceinline__ float ld_bf16(const __nv_bfloat16* p) {
