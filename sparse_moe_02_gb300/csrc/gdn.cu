@@ -24,11 +24,12 @@
 //   S_t = alpha_t S_{t-1} + k_t u_t^T.
 //
 // Four staging warps (one per scheduler) feed the consumers: chunks of 32 tokens' k, q (one
-// head), v (the block's 32 columns) and gates come in by cp.async three chunks ahead, are widened
-// once to fp32 with the per-token dot products k_t . q_t, k_{t-1} . k_t and k_{t-1} . q_t into
-// one of two shared-memory chunk buffers, and the outputs the consumers leave in shared memory go
-// out in 64-byte rows.  One block barrier per chunk hands the buffers over; nothing waits on a
-// flag, so nothing can hang.
+// head), v (the block's 32 columns) and gates come in by cp.async two chunks ahead; the consumers
+// read k and q there as bf16 (half the shared-memory traffic of fp32, widened on the integer
+// pipe), while the staging warps form the per-token dot products k_t . q_t, k_{t-1} . k_t and
+// k_{t-1} . q_t and widen v and the gates into one of two fp32 chunk buffers; the outputs the
+// consumers leave in shared memory go out in 64-byte rows.  One block barrier per chunk hands
+// the buffers over; nothing waits on a flag, so nothing can hang.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -43,17 +44,16 @@ constexpr int kCWarps = 8;                    // consumer warps, 4 columns each
 constexpr int kSWarps = 4;                    // staging warps, 8 tokens of a chunk each
 constexpr int kThreads = 32 * (kCWarps + kSWarps);
 constexpr int kTc = 32;                       // tokens per chunk
-constexpr int kRawStages = 3;                 // bf16 chunks in flight
+constexpr int kRawStages = 3;                 // bf16 chunks: read, landed, in flight
 
 // Shared memory, bytes.
 //   raw stage: k, q [kTc][256] (16-byte piece p of token t at slot p ^ (t & 7)); kprev [4][256]
 //     (staging warp w's copy of the k row of token 8w - 1, plain order); v [kTc][64]; alpha,
 //     beta [kTc];
-//   fp32 stage: k, q [kTc][512] (4-float piece P of token t at slot P ^ (t & 7)); v [kTc][32];
-//     gates [kTc][8] = (alpha, beta, k.q, k_prev.k, k_prev.q, 0, 0, 0);
+//   fp32 stage: v [kTc][32]; gates [kTc][8] = (alpha, beta, k.q, k_prev.k, k_prev.q, 0, 0, 0);
 //   output stage: [kTc][32] bf16.
-// The xor swizzles keep the staging warps' per-token rows and the consumers' per-piece reads
-// free of bank conflicts.
+// The xor swizzle keeps the staging warps' per-token rows and the consumers' reads (16 lanes,
+// 128 consecutive bytes of k or q) free of bank conflicts.
 constexpr int kRawK = 0;
 constexpr int kRawQ = kRawK + kTc * 256;
 constexpr int kRawKp = kRawQ + kTc * 256;
@@ -61,9 +61,7 @@ constexpr int kRawV = kRawKp + kSWarps * 256;
 constexpr int kRawA = kRawV + kTc * 64;
 constexpr int kRawB = kRawA + kTc * 4;
 constexpr int kRawBytes = kRawB + kTc * 4;
-constexpr int kFK = 0;
-constexpr int kFQ = kFK + kTc * 512;
-constexpr int kFV = kFQ + kTc * 512;
+constexpr int kFV = 0;
 constexpr int kFG = kFV + kTc * kCols * 4;
 constexpr int kFBytes = kFG + kTc * 32;
 constexpr int kOBytes = kTc * kCols * 2;
@@ -106,9 +104,9 @@ __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 
-// At most two groups of this thread still pending.
-__device__ __forceinline__ void cp_async_wait2() {
-  asm volatile("cp.async.wait_group 2;\n" ::: "memory");
+// At most one group of this thread still pending.
+__device__ __forceinline__ void cp_async_wait1() {
+  asm volatile("cp.async.wait_group 1;\n" ::: "memory");
 }
 
 // bf16 pairs of a 32-bit word -> fp32 (exact): element 2m in the low half.
@@ -166,8 +164,8 @@ __device__ __forceinline__ void stage_issue(const ScanArgs& a, uint8_t* rs, int6
   cp_async_commit();
 }
 
-// Widens this warp's tokens of chunk cc from raw stage rs into fp32 stage fs, with the dot
-// products k_t . q_t, k_{t-1} . k_t and k_{t-1} . q_t of each token (zero for the chunk's first
+// Widens this warp's tokens' v and gates of chunk cc from raw stage rs into fp32 stage fs, with
+// the dot products k_t . q_t, k_{t-1} . k_t and k_{t-1} . q_t of each token (zero for the chunk's first
 // token, which does not use them): each lane sums its quarter of the rows (32 products in
 // ascending index), then the four quarters are added by two xor shuffles, the same tree in every
 // lane.
@@ -198,11 +196,6 @@ __device__ __forceinline__ void stage_convert(const ScanArgs& a, const uint8_t* 
         kk = fmaf(kp8[e], k8[e], kk);
         kq = fmaf(kp8[e], q8[e], kq);
       }
-      const int s0 = ((2 * p) ^ sw) * 16, s1 = ((2 * p + 1) ^ sw) * 16;
-      *reinterpret_cast<float4*>(fs + kFK + tl * 512 + s0) = make_float4(k8[0], k8[1], k8[2], k8[3]);
-      *reinterpret_cast<float4*>(fs + kFK + tl * 512 + s1) = make_float4(k8[4], k8[5], k8[6], k8[7]);
-      *reinterpret_cast<float4*>(fs + kFQ + tl * 512 + s0) = make_float4(q8[0], q8[1], q8[2], q8[3]);
-      *reinterpret_cast<float4*>(fs + kFQ + tl * 512 + s1) = make_float4(q8[4], q8[5], q8[6], q8[7]);
     }
     float v8[8];
     widen8(*reinterpret_cast<const uint4*>(rs + kRawV + tl * 64 + qd * 16), v8);
@@ -238,23 +231,24 @@ __device__ __forceinline__ void stage_write_out(const ScanArgs& a, const uint8_t
 
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 
-// A token's k and q at the lane's 8 rows, as row pairs (rows 4P + 2i, 4P + 2i + 1 of piece
-// P = r + 16c).
 struct KQ {
   float2 k[4], q[4];
 };
 
-__device__ __forceinline__ void load_kq(const uint8_t* fs, int tt, int r, KQ& x) {
+// A token's k and q at the lane's 8 rows 4(r + 16c) + e, as row pairs (e = 0, 1 and e = 2, 3),
+// read as bf16 from raw stage rs: the rows 64c + 4r .. 64c + 4r + 3 are 8 bytes at offset
+// 8 (r & 1) of the 16-byte piece (r >> 1) + 8c of the token's row.
+__device__ __forceinline__ void load_kq(const uint8_t* rs, int tt, int r, KQ& x) {
   const int sw = tt & 7;
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
-    const int slot = ((r ^ sw) + 16 * c) * 16;
-    const float4 kc = *reinterpret_cast<const float4*>(fs + kFK + tt * 512 + slot);
-    const float4 qc = *reinterpret_cast<const float4*>(fs + kFQ + tt * 512 + slot);
-    x.k[2 * c] = f2(kc.x, kc.y);
-    x.k[2 * c + 1] = f2(kc.z, kc.w);
-    x.q[2 * c] = f2(qc.x, qc.y);
-    x.q[2 * c + 1] = f2(qc.z, qc.w);
+    const int off = tt * 256 + ((((r >> 1) + 8 * c) ^ sw) * 16) + (r & 1) * 8;
+    const uint2 kw = *reinterpret_cast<const uint2*>(rs + kRawK + off);
+    const uint2 qw = *reinterpret_cast<const uint2*>(rs + kRawQ + off);
+    x.k[2 * c] = f2(bf_lo(kw.x), bf_hi(kw.x));
+    x.k[2 * c + 1] = f2(bf_lo(kw.y), bf_hi(kw.y));
+    x.q[2 * c] = f2(bf_lo(qw.x), bf_hi(qw.x));
+    x.q[2 * c + 1] = f2(bf_lo(qw.y), bf_hi(qw.y));
   }
 }
 
@@ -354,16 +348,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(ScanArgs a) {
 
   if (warp >= kCWarps) {  // staging warps
     const int w = warp - kCWarps;
-    for (int c = 0; c < kRawStages; ++c) stage_issue(a, raw + c * kRawBytes, c, h, c0, w, lane);
-    cp_async_wait2();
+    for (int c = 0; c < 2; ++c) stage_issue(a, raw + c * kRawBytes, c, h, c0, w, lane);
+    cp_async_wait1();
     __syncwarp();
     stage_convert(a, raw, fbuf, 0, w, lane);
     __syncthreads();
     for (int64_t cc = 0; cc < nchunks; ++cc) {
-      // the raw stage of chunk cc was widened during the previous chunk: refill it
-      stage_issue(a, raw + (cc % kRawStages) * kRawBytes, cc + kRawStages, h, c0, w, lane);
-      cp_async_wait2();  // chunk cc + 1 has landed (this lane's copies)
-      __syncwarp();      // ... and every lane's of this warp (each warp widens its own tokens)
+      // the consumers read chunk cc's raw stage; the stage of chunk cc - 1 is free again
+      stage_issue(a, raw + ((cc + 2) % kRawStages) * kRawBytes, cc + 2, h, c0, w, lane);
+      cp_async_wait1();  // chunk cc + 1 has landed (this lane's copies; the block barrier below
+      __syncwarp();      // makes every lane's visible to the consumers)
       if (cc + 1 < nchunks)
         stage_convert(a, raw + ((cc + 1) % kRawStages) * kRawBytes,
                       fbuf + ((cc + 1) & 1) * kFBytes, cc + 1, w, lane);
@@ -397,11 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(ScanArgs a) {
   __syncthreads();  // chunk 0 staged
   for (int64_t cc = 0; cc < nchunks; ++cc) {
     const uint8_t* fs = fbuf + (cc & 1) * kFBytes;
+    const uint8_t* rs = raw + (cc % kRawStages) * kRawBytes;
     uint8_t* os = obuf + (cc & 1) * kOBytes;
     const int n = (int)chunk_tokens(a.T, cc);
     // the chunk's first token: its sums taken directly from the current state
     KQ x0, x1;
-    load_kq(fs, 0, r, x0);
+    load_kq(rs, 0, r, x0);
     Carry cy;
     {
       float d[4];
@@ -410,17 +405,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan_kernel(ScanArgs a) {
       cy.al_prev = 1.f;
       cy.u_prev[0] = cy.u_prev[1] = 0.f;
     }
-    load_kq(fs, 1, r, x1);  // slot 1 exists even when n == 1 (stale, unused)
+    load_kq(rs, 1, r, x1);  // slot 1 exists even when n == 1 (stale, unused)
     // two buffers in turn: x0 holds the even token's k and q, x1 the odd one's
     int tt = 0;
     float o;
     for (; tt + 1 < n; tt += 2) {
       token_step(s, cy, fs, tt, col0, r, x0, x1, true, &o);
       store_o(os, tt, col0, r, o);
-      if (tt + 2 < kTc) load_kq(fs, tt + 2, r, x0);
+      if (tt + 2 < kTc) load_kq(rs, tt + 2, r, x0);
       token_step(s, cy, fs, tt + 1, col0, r, x1, x0, tt + 2 < n, &o);
       store_o(os, tt + 1, col0, r, o);
-      if (tt + 3 < kTc) load_kq(fs, tt + 3, r, x1);
+      if (tt + 3 < kTc) load_kq(rs, tt + 3, r, x1);
     }
     if (tt < n) {
       token_step(s, cy, fs, tt, col0, r, x0, x1, false, &o);
