@@ -151,6 +151,24 @@ int moe_create_q4(const moe_config* cfg, const moe_weights_q4* w, moe_handle* ou
 int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk_w,
               int32_t* offsets, int32_t* perm, void* stream);
 
+/* Consistency check of a routing as moe_route writes it (device pointers, caller-owned; E = 256,
+ * k = 8): topk_idx [T][8] ids in [0, E) and strictly ascending within each token; offsets [E+1]
+ * with offsets[0] = 0, non-decreasing, offsets[E] = 8T; perm [8T] such that the slots of group
+ * e (offsets[e] <= s < offsets[e+1]) hold entries p = t*8+j with topk_idx[p] = e in strictly
+ * ascending order -- which together make perm a permutation whose groups are the experts'
+ * histogram in stable token order (§ "Keep expert routing on the GPU").  Enqueues a clear of
+ * *status (a device int) and one kernel that sets it to MOE_ERR_DEVICE if any condition fails;
+ * read it after the stream has run.  The kernel range-checks every value before using it as an
+ * index and reads only within the three arrays' sizes, so arrays in any state give a status,
+ * never a fault.  The debug build of the library (libmoe_debug.so, compiled with MOE_DEBUG) runs
+ * this check inside every moe_route and every tensor-core forward on the routing it produced,
+ * recording MOE_ERR_DEVICE in the handle's device error word (moe_get_device_error).
+ * Errors: MOE_ERR_INVALID_ARG (NULL status or offsets, NULL topk_idx/perm with T > 0, T < 0),
+ * MOE_ERR_UNSUPPORTED (T > 2^20), MOE_ERR_ALIGNMENT (a pointer not 4-byte aligned),
+ * MOE_ERR_CUDA. */
+int moe_check_routing(const int32_t* topk_idx, const int32_t* offsets, const int32_t* perm, int T,
+                      int* status, void* stream);
+
 /* The layer: y [T][d] bf16 from x [T][d] bf16 (device pointers).  T == 0: no-op. */
 int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream);
 

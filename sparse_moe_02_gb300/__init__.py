@@ -7,12 +7,17 @@ import-time use fails loudly.
 
 MoeLayer is a small convenience wrapper that takes torch CUDA tensors (PyTorch is used only
 for device memory and streams) and raises MoeError on a non-zero status.
+
+With MOE_DEBUG_LIBRARY=1 in the environment the binding loads libmoe_debug.so instead: the same
+library built with MOE_DEBUG, which checks every routing it produces (moe_check_routing) and
+records a failure in the handle's device error word.
 """
 import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe.so")
+LIB_PATH = os.path.join(_HERE, "libmoe_debug.so" if os.environ.get("MOE_DEBUG_LIBRARY") == "1"
+                        else "libmoe.so")
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -30,7 +35,7 @@ MOE_SCHEDULE_GEMV = 2
 EXPORTS = ("moe_create", "moe_route", "moe_forward", "moe_forward_host", "moe_get_device_error",
            "moe_destroy", "moe_status_string", "moe_last_cuda_error", "moe_profile_begin",
            "moe_profile_end", "moe_route_one_noalloc", "moe_create_q4", "moe_read_probe",
-           "moe_test_expire_waits", "gdn_scan")
+           "moe_test_expire_waits", "gdn_scan", "moe_check_routing")
 
 # kernel order reported by moe_profile_end
 KERNELS_GEMM = ("router_topk", "route_plan_scatter", "experts", "combine")
@@ -70,7 +75,8 @@ def lib():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise OSError(f"libmoe.so not built ({LIB_PATH}); run __graft_entry__.build()")
+            raise OSError(f"{os.path.basename(LIB_PATH)} not built ({LIB_PATH}); "
+                          "run __graft_entry__.build()")
         L = ctypes.CDLL(LIB_PATH)
         L.moe_create.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(moe_weights),
                                  ctypes.POINTER(_c_void_p)]
@@ -92,13 +98,15 @@ def lib():
         L.moe_route_one_noalloc.argtypes = [_c_void_p, _c_int, _c_void_p, _c_void_p, _c_void_p,
                                             _c_void_p, _c_void_p]
         L.moe_test_expire_waits.argtypes = [_c_void_p, _c_int]
+        L.moe_check_routing.argtypes = [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_void_p,
+                                        _c_void_p]
         L.gdn_scan.argtypes = [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                _c_void_p, _c_void_p, ctypes.c_int64, _c_int, _c_int, _c_int,
                                _c_void_p]
         for fn in ("moe_create", "moe_create_q4", "moe_read_probe", "moe_route", "moe_forward", "moe_forward_host",
                    "moe_get_device_error", "moe_destroy", "moe_last_cuda_error",
                    "moe_profile_begin", "moe_profile_end", "moe_route_one_noalloc",
-                   "moe_test_expire_waits", "gdn_scan"):
+                   "moe_test_expire_waits", "gdn_scan", "moe_check_routing"):
             getattr(L, fn).restype = _c_int
         _lib = L
     return _lib
@@ -153,6 +161,12 @@ def moe_last_cuda_error():
 def moe_route_one_noalloc(x, d, w_router, router_bias, topk_idx, topk_w, stream):
     """Routing of one token with no device allocation (see include/moe.h)."""
     return lib().moe_route_one_noalloc(x, d, w_router, router_bias, topk_idx, topk_w, stream)
+
+
+def moe_check_routing(topk_idx, offsets, perm, T, status, stream):
+    """Consistency check of a routing (see include/moe.h); *status (a device int) ends as
+    MOE_OK or MOE_ERR_DEVICE once the stream has run."""
+    return lib().moe_check_routing(topk_idx, offsets, perm, T, status, stream)
 
 
 def gdn_scan(q, k, v, alpha, beta, state_in, state_out, o, T, H, dk, dv, stream):

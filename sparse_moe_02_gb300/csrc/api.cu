@@ -311,6 +311,12 @@ int forward_gemm(moe_handle h, const __nv_bfloat16* xd, int T, __nv_bfloat16* yd
   if ((st = run_route_gemm(h, xd, T, h->rws.topk_idx, h->rws.topk_w, nullptr, h->rws.perm, s,
                            prof, small)))
     return st;
+#ifdef MOE_DEBUG
+  // debug build: the routing's invariants, into the device error word
+  if ((st = cuda_status(moe::launch_check_routing(h->rws.topk_idx, h->rws.offsets, h->rws.perm, T,
+                                                  h->rws.err, s))))
+    return st;
+#endif
   if (prof && (st = prof_mark(h, s, 2))) return st;
   if ((st = cuda_status(moe::launch_experts(xd, h->tm_wg, h->tm_wu, h->tm_wsg, h->tm_wsu,
                                             h->tm_h, h->tm_wd, h->tm_wsd, h->D, h->rws, h->h,
@@ -446,15 +452,23 @@ int moe_route(moe_handle h, const void* x, int T, int32_t* topk_idx, float* topk
   int32_t* idx = topk_idx ? topk_idx : h->rws.topk_idx;
   float* wt = topk_w ? topk_w : h->rws.topk_w;
   int32_t* pm = perm ? perm : h->rws.perm;
+  int32_t* off = offsets ? offsets : h->rws.offsets;
   if (use_gemv(h, T))
-    return cuda_status(moe::launch_decode_router_shared(
-        static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, idx, wt,
-        offsets ? offsets : h->rws.offsets, pm, h->dws, h->rws.err, s, false));
-  if (!h->q4 && use_batch(h, T))
-    return cuda_status(moe::launch_decode_batch_router_shared(
-        static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, T, idx, wt,
-        offsets ? offsets : h->rws.offsets, pm, h->dws, s, false));
-  return run_route_gemm(h, x, T, idx, wt, offsets, pm, s, false, small_router(h, T));
+    st = cuda_status(moe::launch_decode_router_shared(
+        static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, idx, wt, off, pm, h->dws,
+        h->rws.err, s, false));
+  else if (!h->q4 && use_batch(h, T))
+    st = cuda_status(moe::launch_decode_batch_router_shared(
+        static_cast<const __nv_bfloat16*>(x), decode_weights(h), h->D, T, idx, wt, off, pm,
+        h->dws, s, false));
+  else
+    st = run_route_gemm(h, x, T, idx, wt, offsets, pm, s, false, small_router(h, T));
+#ifdef MOE_DEBUG
+  // debug build: the routing's invariants, into the device error word
+  if (st == MOE_OK)
+    st = cuda_status(moe::launch_check_routing(idx, off, pm, T, h->rws.err, s));
+#endif
+  return st;
 }
 
 int moe_forward(moe_handle h, const void* x, int T, void* y, void* stream) {

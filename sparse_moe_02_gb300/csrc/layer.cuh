@@ -171,6 +171,11 @@ cudaError_t prepare_decode_stream_kernels();
 // expire: the launch's grid barrier waits for one arrival more than there are blocks, for
 // 1 ms, then records MOE_ERR_TIMEOUT and the blocks leave without combining (the test of the
 // timeout path).
+// moe_check_routing's kernel (check.cu): sets *status to the device-state error if the routing
+// (topk_idx [T][8], offsets [E+1], perm [8T]) is inconsistent; leaves it unchanged otherwise.
+cudaError_t launch_check_routing(const int32_t* topk_idx, const int32_t* offsets,
+                                 const int32_t* perm, int T, int* status, cudaStream_t s);
+
 cudaError_t launch_decode_stream(const __nv_bfloat16* x, const DecodeWeights& W, const Dims& D,
                                  int32_t* topk_idx, float* topk_w, const DecodeWs& dw,
                                  __nv_bfloat16* y, int* err, int sms, cudaStream_t s,

@@ -83,6 +83,13 @@ def test_calls_on_null_handle_are_rejected():
     assert moe.moe_route(None, None, 1, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_get_device_error(None, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_test_expire_waits(None, 1) == moe.MOE_ERR_INVALID_ARG
+    A = 0x100000  # aligned stand-in device addresses: every case fails before any CUDA call
+    assert moe.moe_check_routing(A, A, A, 4, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_routing(A, None, A, 4, A, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_routing(None, A, A, 4, A, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_routing(A, A, A, -1, A, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_check_routing(A, A, A, (1 << 20) + 1, A, None) == moe.MOE_ERR_UNSUPPORTED
+    assert moe.moe_check_routing(A + 2, A, A, 4, A, None) == moe.MOE_ERR_ALIGNMENT
     assert moe.moe_destroy(None) == moe.MOE_OK
 
 
