@@ -59,8 +59,11 @@ cudaError_t launch_check_routing(const int32_t* topk_idx, const int32_t* offsets
                                  const int32_t* perm, int T, int* status, cudaStream_t s) {
   const int n = T * kTopK;
   const int blocks = n / 256 + 1 < 152 ? n / 256 + 1 : 152;
-  check_routing_kernel<<<blocks, 256, 0, s>>>(topk_idx, offsets, perm, T, status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, check_routing_kernel, topk_idx, offsets, perm, T, status);
 }
 
 }  // namespace moe

@@ -457,6 +457,12 @@ extern "C" int gdn_scan(const void* q, const void* k, const void* v, const float
   ScanArgs a{static_cast<const uint8_t*>(q), static_cast<const uint8_t*>(k),
              static_cast<const uint8_t*>(v), alpha, beta, state_in, state_out,
              static_cast<uint8_t*>(o), T, H, dv};
-  gdn_scan_kernel<<<dim3(dv / kCols, H), kThreads, kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  // the launch's own status (not cudaGetLastError, which would also take and clear an earlier,
+  // unrelated error)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(dv / kCols, H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  return cudaLaunchKernelEx(&cfg, gdn_scan_kernel, a) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -29,9 +29,12 @@ cudaError_t launch_host_copy(const void* src, void* dst, size_t bytes, int sms, 
   size_t blocks = (n16 + per_block - 1) / per_block;
   if (blocks > (size_t)sms * 4) blocks = (size_t)sms * 4;
   if (blocks == 0) return cudaSuccess;
-  host_copy_kernel<<<(unsigned)blocks, 256, 0, s>>>(static_cast<const uint4*>(src),
-                                                    static_cast<uint4*>(dst), n16);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};  // the launch's own status, not an earlier pending error
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, host_copy_kernel, static_cast<const uint4*>(src),
+                            static_cast<uint4*>(dst), n16);
 }
 
 }  // namespace moe

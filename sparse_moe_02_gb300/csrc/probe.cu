@@ -36,7 +36,12 @@ extern "C" int moe_read_probe(const void* buf, size_t bytes, void* sink, void* s
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
-  read_probe_kernel<<<sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(buf), bytes / 16, static_cast<uint32_t*>(sink));
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};  // the launch's own status, not an earlier pending error
+  cfg.gridDim = dim3(sms * 4);
+  cfg.blockDim = dim3(256);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  return cudaLaunchKernelEx(&cfg, read_probe_kernel, static_cast<const uint4*>(buf),
+                            (size_t)(bytes / 16), static_cast<uint32_t*>(sink)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
