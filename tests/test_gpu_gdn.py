@@ -158,3 +158,20 @@ def test_zero_tokens_copy_or_clear_the_state():
     assert o.shape[0] == 0 and np.array_equal(s.view(np.uint32), s0.view(np.uint32))
     _, s = run_scan(q, k, v, alpha, beta, None)
     assert np.array_equal(s, np.zeros_like(s))
+
+
+def test_scan_largest_accepted_shapes():
+    # dv = 4096 (128 column blocks of one head) on every output
+    q, k, v, alpha, beta, s0 = synth.gdn_inputs(13, 40, 1, DK, 4096)
+    o, s = run_scan(q, k, v, alpha, beta, s0)
+    o_ref, s_ref = oracle.gdn_scan(q, k, v, alpha, beta, s0)
+    check(o, s, o_ref, s_ref)
+    # H = 65535 (the grid's second dimension at its limit), zero state; heads are independent,
+    # so the oracle runs on a sample of them
+    T, H, dv = 2, 65535, 32
+    q, k, v, alpha, beta, _ = synth.gdn_inputs(14, T, H, DK, dv, zero_state=True)
+    o, s = run_scan(q, k, v, alpha, beta, None)
+    heads = np.unique(np.concatenate([np.arange(8), np.arange(H - 8, H), np.arange(0, H, 4099)]))
+    o_ref, s_ref = oracle.gdn_scan(q[:, heads], k[:, heads], v[:, heads], alpha[:, heads],
+                                   beta[:, heads], None)
+    check(o[:, heads], s[heads], o_ref, s_ref)

@@ -29,7 +29,12 @@ def _run_q4(c, schedule=moe.MOE_SCHEDULE_AUTO):
 
 
 @pytest.mark.parametrize("d,f,fs,seed", [(512, 128, 256, 1), (2048, 512, 512, 0),
-                                         (4096, 2048, 2048, 2), (640, 384, 128, 3)])
+                                         (4096, 2048, 2048, 2), (640, 384, 128, 3),
+                                         # the streamed launch (d, f, fs multiples of 512,
+                                         # d <= 2048): fs > f, f > fs, the largest f it
+                                         # takes at d = 2048, four outputs per block
+                                         (1024, 512, 1024, 4), (1536, 1024, 512, 5),
+                                         (2048, 1536, 512, 6), (512, 512, 512, 7)])
 def test_q4_decode_matches_oracle(d, f, fs, seed):
     c = build_case("q4-decode", d=d, f=f, fs=fs, T=1, seed=seed, full_host=False)
     for sched in (moe.MOE_SCHEDULE_AUTO, moe.MOE_SCHEDULE_GEMV):
