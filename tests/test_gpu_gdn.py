@@ -175,3 +175,17 @@ def test_scan_largest_accepted_shapes():
     o_ref, s_ref = oracle.gdn_scan(q[:, heads], k[:, heads], v[:, heads], alpha[:, heads],
                                    beta[:, heads], None)
     check(o[:, heads], s[heads], o_ref, s_ref)
+
+
+def test_gate_extremes():
+    # decay 0 (the state is forgotten before the write), 1 (no decay) and 0.5, write strength 0
+    # and 1, mixed per token and head: the early sums' correction alpha_{t-1} S + (k.k) u must
+    # also hold when alpha_{t-1} S vanishes
+    T, H, dv = 200, 3, 64
+    q, k, v, _, _, s0 = synth.gdn_inputs(15, T, H, DK, dv)
+    rng = np.random.default_rng(15)
+    alpha = rng.choice(np.array([0.0, 0.5, 1.0], np.float32), size=(T, H))
+    beta = rng.choice(np.array([0.0, 1.0], np.float32), size=(T, H))
+    o, s = run_scan(q, k, v, alpha, beta, s0)
+    o_ref, s_ref = oracle.gdn_scan(q, k, v, alpha, beta, s0)
+    check(o, s, o_ref, s_ref)
