@@ -415,7 +415,7 @@ def gdn_algorithmic(T, H=GDN_H, dk=GDN_DK, dv=GDN_DV):
     return flops, byts
 
 
-def run_gdn(torch, moe, args, P_hbm):
+def run_gdn(torch, moe, args, P_hbm, rank=0, world=1):
     """The Gated DeltaNet recurrent scan of one layer (32 heads, 128 x 128 fp32 state each)
     over a prompt of T tokens: device time per scan (L2 flushed before every step), against
     the fp32 FMA peak of the SMs (the scan is FMA-bound: 4 FMA-pipe operations per state
@@ -473,7 +473,9 @@ def run_gdn(torch, moe, args, P_hbm):
             "algorithmic_flops": flops, "algorithmic_bytes": byts, "gpu_launches": steps,
             "l2": "flushed (256 MB write, untimed) before every timed step"})
         del q, k, v, al, be, s0b, s0, s1, o
-    return {"rows": rows, "cpu_baseline": None if args.no_cpu else gdn_oracle_rate()}
+    # the oracle's rate on the host cores: rank 0 of a one-GPU run only
+    cpu = None if args.no_cpu or rank != 0 or world != 1 else gdn_oracle_rate()
+    return {"rows": rows, "cpu_baseline": cpu}
 
 
 def gdn_oracle_rate(T=2048):
@@ -839,10 +841,10 @@ def main():
                                    P_tc, q4=True) for t in ts]
     pre_q4 = None if args.no_q4 else run_prefill_q4(torch, moe, args, rank, P_hbm, P_tc)
     dec = None if args.no_decode else run_decode(torch, moe, args, rank, world, P_hbm)
-    gdn = None if args.no_gdn else run_gdn(torch, moe, args, P_hbm)
+    gdn = None if args.no_gdn else run_gdn(torch, moe, args, P_hbm, rank, world)
     clk = clocks.stop()
     cpu = None
-    if rank == 0 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu:
         rate, sample, cores = oracle_sample_rate(args.cpu_seconds)
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": sample}
