@@ -243,6 +243,26 @@ def test_chunked_forward_is_byte_identical(chunk):
     L1.close()
 
 
+@pytest.mark.parametrize("chunk", [3000, 4096])
+def test_chunked_forward_at_the_benchmark_shape(chunk):
+    # d = 2048, f = fs = 512, 8192 tokens in chunks of 3000 (a ragged last chunk) or 4096:
+    # every token is computed independently, so the output is the unchunked output, byte for
+    # byte, and the routing of the whole call is the same
+    T = 8192
+    c = build_case("chunked-bench", d=2048, f=512, fs=512, T=T, seed=37, full_host=False)
+    W, x = to_device(c)
+    L0 = moe.MoeLayer(W, T)
+    L1 = moe.MoeLayer(W, T, chunk_tokens=chunk)
+    y0 = bf16_bits(L0.forward(x))
+    y1 = bf16_bits(L1.forward(x))
+    assert L0.device_error() == moe.MOE_OK and L1.device_error() == moe.MOE_OK
+    assert np.array_equal(y0, y1)
+    toks = sample_tokens(T, n_edge=8, stride=257)
+    assert_close(y1[toks], oracle_outputs(c, toks), f"chunked T={T} chunk={chunk}")
+    L0.close()
+    L1.close()
+
+
 # ---------------------------------------------------------------- API behaviour on the GPU
 
 def test_deterministic_and_host_entry_point():
