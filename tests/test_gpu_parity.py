@@ -247,7 +247,7 @@ def test_chunked_forward_is_byte_identical(chunk):
 def test_chunked_forward_at_the_benchmark_shape(chunk):
     # d = 2048, f = fs = 512, 8192 tokens in chunks of 3000 (a ragged last chunk) or 4096:
     # every token is computed independently, so the output is the unchunked output, byte for
-    # byte, and the routing of the whole call is the same
+    # byte
     T = 8192
     c = build_case("chunked-bench", d=2048, f=512, fs=512, T=T, seed=37, full_host=False)
     W, x = to_device(c)
