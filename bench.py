@@ -468,7 +468,9 @@ def run_gdn(torch, moe, args, P_hbm, rank=0, world=1):
                          "frac": tf / peak_tf,
                          "peak_source": f"derived: {sms} SMs x 128 fp32 lanes x 2 FLOP x "
                                         f"{SM_CLOCK_MHZ:.0f} MHz",
-                         "traffic": None},
+                         # DRAM bytes of one launch from the committed capture (taken at
+                         # T = 2048 on this kernel source), for that row only
+                         "traffic": profiled_traffic("gdn_scan") if T == 2048 else None},
             "hbm_frac": byts / (us * 1e-6) / 1e9 / P_hbm,
             "algorithmic_flops": flops, "algorithmic_bytes": byts, "gpu_launches": steps,
             "l2": "flushed (256 MB write, untimed) before every timed step"})
@@ -770,7 +772,7 @@ def profiled_traffic(kernel):
     if not os.path.exists(path):
         return None
     src = {"router_topk": "route.cu", "route_plan_scatter": "route.cu",
-           "experts": "experts.cu", "combine": "experts.cu"}.get(kernel)
+           "experts": "experts.cu", "combine": "experts.cu", "gdn_scan": "gdn.cu"}.get(kernel)
     if not src:
         return None
     sha = hashlib.sha1(open(os.path.join(ROOT, "sparse_moe_02_gb300", "csrc", src), "rb")
